@@ -1,0 +1,384 @@
+#!/usr/bin/env python
+"""Benchmark of two-stream BDLM attention (forward + backward) on GB300.
+
+One step = the whole hot path over one batch: the two-stream forward (O, LSE)
+and the backward (row statistic D, dK/dV pass, dQ pass) of the long-context
+workload L = 131072 clean + 131072 corrupted tokens, B = 512, 16 query heads,
+8 KV heads, head dim 128, bf16 inputs ~ N(0, 1), through the library's C ABI.
+
+Metric: useful (mask-visible) fwd+bwd TFLOP/s, 14 d L (L + B) Hq FLOP per
+step (the backward counted as 2.5 forwards), plus tokens/s (2L per step) and
+the fraction of the bf16 tensor peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+Under torchrun each rank runs its own replica of the workload on its GPU (no
+data-path collective); rank 0 prints one JSON line.  ``--impl reference``
+times the fp64 CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "long-128k"
+METRIC = "useful fwd+bwd TFLOP/s & tokens/s at 1 GB300; % of bf16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def useful_flops(L, B, Hq, d):
+    return 14.0 * d * L * (L + B) * Hq
+
+
+def strict_flops(L, B, Hq, d):
+    return 12.0 * d * L * (L + B) * Hq
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def peak_value(peaks, key):
+    """Reads a peak from MEASURED_PEAKS.json, tolerating nesting and units."""
+    if key in peaks and isinstance(peaks[key], (int, float)):
+        return float(peaks[key])
+    for v in peaks.values():
+        if isinstance(v, dict) and key in v and isinstance(v[key], (int, float)):
+            return float(v[key])
+    return FALLBACK_PEAKS[key]
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "power_w_median": statistics.median(power) if power else None,
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle sample
+def oracle_sample(L, B, Hq, Hkv, d, budget_s, seed=0):
+    """Times the fp64 oracle on the last blocks of one query head of the
+    workload (forward, row statistic, backward), until ~budget_s seconds.
+    Returns (useful FLOP, seconds, blocks done, threads)."""
+    import numpy as np
+
+    import oracle.bdlm_oracle as orc
+    from structured_mask_attention_gb300.inputs import make_numpy
+
+    X = make_numpy(L, 1, 1, d, seed=seed)  # one query head, its KV head
+    X = {k: v.astype(np.float64) for k, v in X.items()}
+    names = ("Qc", "Kc", "Vc", "Qn", "Kn", "Vn")
+    sc = 1.0 / math.sqrt(d)
+    N = L // B
+    flops = 0.0
+    t0 = time.perf_counter()
+    done = 0
+    for b in range(N - 1, -1, -1):
+        Oc, On, LSEc, LSEn = orc.fwd_partial(*[X[k] for k in names], B, sc, heads=[0], blocks=[b])
+        Dc, Dn = orc.bwd_preprocess(Oc, X["dOc"]), orc.bwd_preprocess(On, X["dOn"])
+        orc.bwd_partial(*[X[k] for k in names], X["dOc"], X["dOn"], LSEc, LSEn, Dc, Dn, B, sc, heads=[0],
+                        blocks=[b])
+        flops += 14.0 * d * 2 * B * (b + 1) * B
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return flops, dt, done, blas_threads()
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(v):
+            return int(os.environ[v])
+    return os.cpu_count()
+
+
+# ------------------------------------------------------------------ traffic
+def committed_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        d = json.load(fh)
+    ent = d.get(kernel)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, ent["source"])
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as fh:
+        h = hashlib.sha256(fh.read()).hexdigest()[:16]
+    if h != ent.get("source_sha256_16"):
+        return None
+    return ent.get("dram_bytes_per_launch_full")
+
+
+# ------------------------------------------------------------------ native arm
+def run_native(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import structured_mask_attention_gb300 as m
+    from structured_mask_attention_gb300.inputs import WORKLOADS, make_torch
+
+    m.load_library()
+    w = WORKLOADS[WORKLOAD]
+    L, B, Hq, Hkv, d = w["L"], w["B"], w["Hq"], w["Hkv"], w["d"]
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    X = make_torch(L, Hq, Hkv, d, seed=rank, device=dev)
+    names = ("Qc", "Kc", "Vc", "Qn", "Kn", "Vn")
+    ins = [X[k] for k in names]
+    sc = 1.0 / math.sqrt(d)
+    e = lambda H, dt=torch.bfloat16: torch.empty((L, H, d), dtype=dt, device=dev)
+    fout = (e(Hq), e(Hq), torch.empty((Hq, L), dtype=torch.float32, device=dev),
+            torch.empty((Hq, L), dtype=torch.float32, device=dev))
+    gout = (e(Hq), e(Hkv), e(Hkv), e(Hq), e(Hkv), e(Hkv))
+    ws_f = torch.empty(m.bdlm_workspace_size(m.OP_FWD, L, B, Hq, Hkv, d), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(m.bdlm_workspace_size(m.OP_BWD, L, B, Hq, Hkv, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        Oc, On, LSEc, LSEn = m.bdlm_attn_fwd(*ins, B, sc, out=fout, workspace=ws_f)
+        m.bdlm_attn_bwd(*ins, Oc, On, X["dOc"], X["dOn"], LSEc, LSEn, B, sc, out=gout, workspace=ws_b)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    m.bdlm_sync_status(ws_f)
+    m.bdlm_sync_status(ws_b)
+
+    m.bdlm_timing_report(reset=True)
+    m.bdlm_timing_enable(True)
+    clocks = ClockSampler(local_rank)
+    time.sleep(0.5)
+    barrier()
+    torch.cuda.synchronize()
+    n0 = m.bdlm_kernel_launches()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    launches = m.bdlm_kernel_launches() - n0
+    clk = clocks.stop()
+    m.bdlm_timing_enable(False)
+    ktimes = m.bdlm_timing_report(reset=True)
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    m.bdlm_sync_status(ws_f)
+    m.bdlm_sync_status(ws_b)
+    ms_step = ms / args.steps
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h_in = {k: pin(X[k]) for k in (*names, "dOc", "dOn")}
+        for k in h_in:
+            h_in[k].copy_(X[k])
+        h_out = [pin(t) for t in (*fout, *gout)]
+        h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in h_out)
+        dX = {k: torch.empty_like(X[k]) for k in h_in}
+
+        def e2e_step():
+            for k in h_in:
+                dX[k].copy_(h_in[k], non_blocking=True)
+            Oc, On, LSEc, LSEn = m.bdlm_attn_fwd(*[dX[k] for k in names], B, sc, out=fout, workspace=ws_f)
+            m.bdlm_attn_bwd(*[dX[k] for k in names], Oc, On, dX["dOc"], dX["dOn"], LSEc, LSEn, B, sc, out=gout,
+                            workspace=ws_b)
+            for hd, dv in zip(h_out, (*fout, *gout)):
+                hd.copy_(dv, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        k2 = max(1, min(args.steps, 3))
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(k2):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ems = a.elapsed_time(b) / k2
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": round(world * useful_flops(L, B, Hq, d) / (ems * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+               "ms_per_step": round(ems, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "tokens_per_s": round(world * 2 * L / (ems * 1e-3), 1)}
+        del dX, h_in, h_out
+
+    # ---- roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    peak_tf = peak_value(peaks, "bf16_tflops_sustained")
+    pairs = L * (L + B) * Hq
+    alg = {"bdlm_fwd_tc": 4.0 * d * pairs, "bdlm_bwd_dkv": 8.0 * d * pairs, "bdlm_bwd_dq": 6.0 * d * pairs}
+    per_kernel = {}
+    for k, (cnt, tot) in ktimes.items():
+        per_kernel[k] = {"launches": cnt, "ms_per_launch": round(tot / max(cnt, 1), 4),
+                         "share": round(tot / max(sum(v[1] for v in ktimes.values()), 1e-9), 4)}
+    dom = max((k for k in ktimes if k in alg), key=lambda k: ktimes[k][1])
+    dom_ms = ktimes[dom][1] / ktimes[dom][0]
+    achieved = alg[dom] / (dom_ms * 1e-3) / 1e12
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf,
+                "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4), "traffic": committed_traffic(dom),
+                "peak_source": f"{peak_src} bf16_tflops_sustained" + (" (of measured)" if peak_src == "measured"
+                                                                      else " (of fallback)"),
+                "algorithmic_flop_per_launch": alg[dom]}
+
+    value = world * useful_flops(L, B, Hq, d) / (ms_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), bf16)",
+        "config": {"workload": WORKLOAD, "L": L, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d, "batch": 1,
+                   "tokens_per_step": 2 * L, "l2": "inputs larger than L2 (3 GiB per step)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "tokens_per_s": round(world * 2 * L / (ms_step * 1e-3), 1),
+        "strict_tflops": round(world * strict_flops(L, B, Hq, d) / (ms_step * 1e-3) / 1e12, 3),
+        "pct_of_peak": round(100.0 * value / world / peak_tf, 2),
+        "clocks": clk, "gpu_launches": int(launches), "kernels": per_kernel, "roofline": roofline,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        flops, dt, blocks, thr = oracle_sample(L, B, Hq, Hkv, d, args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": thr,
+                                "kind": "oracle",
+                                "sample": f"fp64 oracle fwd+bwd of the last {blocks} block(s) of one query head "
+                                          f"of {WORKLOAD} (both streams), {dt:.1f} s"}
+    return line
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    from structured_mask_attention_gb300.inputs import WORKLOADS
+    w = WORKLOADS[WORKLOAD]
+    L, B, Hq, Hkv, d = w["L"], w["B"], w["Hq"], w["Hkv"], w["d"]
+    budget = max(1.0, min(args.cpu_budget, 240.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(L, B, Hq, Hkv, d, budget * 0.25)
+    tot_f, tot_t, blocks, thr = 0.0, 0.0, 0, 1
+    for _ in range(args.steps):
+        f, t, nb, thr = oracle_sample(L, B, Hq, Hkv, d, budget)
+        tot_f += f; tot_t += t; blocks += nb
+    value = tot_f / tot_t / 1e12
+    sample = (f"fp64 oracle fwd+bwd of the last blocks of one query head of {WORKLOAD} (both streams), "
+              f"{blocks} blocks over {args.steps} steps")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / args.steps, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1), bf16-rounded)",
+            "config": {"workload": WORKLOAD, "L": L, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("native", "reference"), default="native")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for the CPU baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    line = run_native(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,594 @@
+// abi.cu -- the C ABI declared in include/bdlm_attn.h: argument validation,
+// TMA tensor-map encoding, work-list export and kernel launches.
+//
+// Every entry point validates on the host before enqueuing anything, catches
+// every C++ exception, and reports failures as bdlm_status plus a
+// thread-local message.  The library allocates no device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <initializer_list>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/bdlm_attn.h"
+#include "geometry.cuh"
+#include "kernels.h"
+
+using namespace bdlm;
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<uint64_t> g_launches{0};
+
+// ---------------------------------------------------------------- timing
+enum KernelKind { K_FWD = 0, K_DKV, K_DQ, K_PREP, K_MERGE, K_WATCHDOG, K_COUNT };
+const char* const kKindNames[K_COUNT] = {"bdlm_fwd_tc", "bdlm_bwd_dkv", "bdlm_bwd_dq",
+                                         "bdlm_preprocess", "bdlm_merge", "bdlm_watchdog"};
+
+struct Timing {
+  std::mutex mu;
+  std::atomic<bool> on{false};
+  std::vector<cudaEvent_t> pool;
+  struct Pending {
+    int kind;
+    cudaEvent_t a, b;
+  };
+  std::vector<Pending> pending;
+  double total_ms[K_COUNT] = {};
+  uint64_t count[K_COUNT] = {};
+};
+Timing& timing() {
+  static Timing* t = new Timing();  // never destroyed: events may outlive static teardown order
+  return *t;
+}
+
+cudaEvent_t take_event(Timing& t) {
+  if (!t.pool.empty()) {
+    cudaEvent_t e = t.pool.back();
+    t.pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Brackets one kernel launch with events on its stream when timing is on.
+struct ScopedKernelTimer {
+  int kind;
+  cudaStream_t st;
+  cudaEvent_t a = nullptr, b = nullptr;
+  ScopedKernelTimer(int k, cudaStream_t s) : kind(k), st(s) {
+    Timing& t = timing();
+    if (!t.on.load()) return;
+    std::lock_guard<std::mutex> lock(t.mu);
+    a = take_event(t);
+    b = take_event(t);
+    if (a && b) cudaEventRecord(a, st);
+  }
+  void stop() {
+    if (!a || !b) return;
+    Timing& t = timing();
+    cudaEventRecord(b, st);
+    std::lock_guard<std::mutex> lock(t.mu);
+    t.pending.push_back({kind, a, b});
+    a = b = nullptr;
+  }
+  ~ScopedKernelTimer() { stop(); }
+};
+
+bdlm_status fail(bdlm_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+bdlm_status fail(bdlm_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+bdlm_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(BDLM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr size_t kWsHeader = 256;  // status word + padding
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bdlm_status check_shape(int64_t L, int64_t B, int Hq, int Hkv, int d) {
+  if (L <= 0 || B <= 0) return fail(BDLM_ERR_SHAPE, "L=%lld and B=%lld must be positive", (long long)L, (long long)B);
+  if (L % B) return fail(BDLM_ERR_SHAPE, "L=%lld is not a multiple of B=%lld", (long long)L, (long long)B);
+  if (L > (int64_t)1 << 30) return fail(BDLM_ERR_SHAPE, "L=%lld exceeds 2^30", (long long)L);
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv)
+    return fail(BDLM_ERR_SHAPE, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
+  if (Hq > 4096) return fail(BDLM_ERR_SHAPE, "Hq=%d exceeds 4096", Hq);
+  if (d != 64 && d != 128) return fail(BDLM_ERR_SHAPE, "head dim d=%d must be 64 or 128", d);
+  return BDLM_OK;
+}
+
+bdlm_status check_scale(float scale) {
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(BDLM_ERR_INVALID_ARG, "scale=%g must be finite and > 0", scale);
+  return BDLM_OK;
+}
+
+#define BDLM_CHECK(expr)            \
+  do {                              \
+    bdlm_status _s = (expr);        \
+    if (_s != BDLM_OK) return _s;   \
+  } while (0)
+
+bdlm_status check_ptrs(const char* names, std::initializer_list<const void*> ptrs) {
+  int i = 0;
+  for (const void* p : ptrs) {
+    if (!p) return fail(BDLM_ERR_INVALID_ARG, "null pointer (argument %d of %s)", i, names);
+    if (!aligned16(p)) return fail(BDLM_ERR_ALIGN, "pointer not 16-byte aligned (argument %d of %s)", i, names);
+    ++i;
+  }
+  return BDLM_OK;
+}
+
+bdlm_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (!ws) return fail(BDLM_ERR_WORKSPACE, "workspace is null (need %zu bytes)", need);
+  if (!aligned16(ws)) return fail(BDLM_ERR_ALIGN, "workspace not 16-byte aligned");
+  if (ws_bytes < need) return fail(BDLM_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  return BDLM_OK;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  int major = 0, minor = 0;
+};
+
+bdlm_status device_info(DeviceInfo& info) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  static bool have[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(BDLM_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!have[dev]) {
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+    cache[dev].sms = prop.multiProcessorCount;
+    cache[dev].major = prop.major;
+    cache[dev].minor = prop.minor;
+    have[dev] = true;
+  }
+  info = cache[dev];
+  if (info.major != 10 || info.minor != 3)
+    return fail(BDLM_ERR_UNSUPPORTED, "device is sm_%d%d; this library is built for sm_103a", info.major, info.minor);
+  return BDLM_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+bdlm_status get_encoder(EncodeTiledFn& fn) {
+  static std::once_flag once;
+  static EncodeTiledFn cached = nullptr;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) cached = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  if (!cached) return fail(BDLM_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(err));
+  fn = cached;
+  return BDLM_OK;
+}
+
+// [L, H, d] bf16 tensor as a 3-D TMA map (d innermost), box 64 x 1 x 128,
+// 128-byte swizzle; out-of-range rows read as zero.
+bdlm_status encode_lhd(EncodeTiledFn fn, CUtensorMap* m, const void* ptr, int64_t L, int H, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)L};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(BDLM_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  return BDLM_OK;
+}
+
+uint64_t wait_limit_ns() {
+  static uint64_t v = [] {
+    const char* s = std::getenv("BDLM_WAIT_LIMIT_MS");
+    long ms = s ? std::strtol(s, nullptr, 10) : 2000;
+    if (ms <= 0) ms = 2000;
+    return (uint64_t)ms * 1000000ull;
+  }();
+  return v;
+}
+
+bdlm_status clear_status(void* ws, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(ws, 0, 4, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
+  return BDLM_OK;
+}
+
+bdlm_status finish(cudaError_t e, int launches, const char* what) {
+  g_launches.fetch_add((uint64_t)launches);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return BDLM_OK;
+}
+
+bdlm_status fwd_common(const void* Qc, const void* Kc, const void* Vc, const void* Qn, const void* Kn,
+                       const void* Vn, int64_t L, int64_t B, int Hq, int Hkv, int d, float scale, int64_t kv_begin,
+                       int64_t kv_end, int include_local, void* Oc, void* On, int o_f32, float* LSEc, float* LSEn,
+                       void* ws, size_t ws_bytes, cudaStream_t st) {
+  DeviceInfo info;
+  BDLM_CHECK(device_info(info));
+  EncodeTiledFn enc;
+  BDLM_CHECK(get_encoder(enc));
+  FwdMaps maps;
+  BDLM_CHECK(encode_lhd(enc, &maps.Qc, Qc, L, Hq, d));
+  BDLM_CHECK(encode_lhd(enc, &maps.Qn, Qn, L, Hq, d));
+  BDLM_CHECK(encode_lhd(enc, &maps.Kc, Kc, L, Hkv, d));
+  BDLM_CHECK(encode_lhd(enc, &maps.Kn, Kn, L, Hkv, d));
+  BDLM_CHECK(encode_lhd(enc, &maps.Vc, Vc, L, Hkv, d));
+  BDLM_CHECK(encode_lhd(enc, &maps.Vn, Vn, L, Hkv, d));
+  FwdParams p;
+  p.g = Geom{L, B, Hq, Hkv, kv_begin, kv_end, include_local ? 1 : 0};
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.Oc = Oc;
+  p.On = On;
+  p.o_f32 = o_f32;
+  p.LSEc = LSEc;
+  p.LSEn = LSEn;
+  p.n_items = q_items(p.g, kFwdTileQ);
+  p.status = static_cast<uint32_t*>(ws);
+  p.limit_ns = wait_limit_ns();
+  BDLM_CHECK(clear_status(ws, st));
+  int launches = 0;
+  ScopedKernelTimer tm(K_FWD, st);
+  cudaError_t e = launch_fwd(maps, p, d, info.sms, st, &launches);
+  tm.stop();
+  return finish(e, launches, "forward launch");
+}
+
+BwdParams bwd_params(const void* Qc, const void* Kc, const void* Vc, const void* Qn, const void* Kn, const void* Vn,
+                     const void* dOc, const void* dOn, const float* LSEc, const float* LSEn, const float* Dc,
+                     const float* Dn, int64_t L, int64_t B, int Hq, int Hkv, int d, float scale, int64_t kv_begin,
+                     int64_t kv_end, int include_local) {
+  BwdParams p;
+  p.g = Geom{L, B, Hq, Hkv, kv_begin, kv_end, include_local ? 1 : 0};
+  p.d = d;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.Qc = Qc; p.Kc = Kc; p.Vc = Vc; p.Qn = Qn; p.Kn = Kn; p.Vn = Vn;
+  p.dOc = dOc; p.dOn = dOn;
+  p.LSEc = LSEc; p.LSEn = LSEn; p.Dc = Dc; p.Dn = Dn;
+  p.dQc = p.dQn = p.dKc = p.dVc = p.dKn = p.dVn = nullptr;
+  p.g_f32 = 0;
+  p.dq_accumulate = 0;
+  return p;
+}
+
+template <typename F>
+bdlm_status guarded(F&& f) {
+  try {
+    return f();
+  } catch (const std::exception& ex) {
+    return fail(BDLM_ERR_INVALID_ARG, "internal exception: %s", ex.what());
+  } catch (...) {
+    return fail(BDLM_ERR_INVALID_ARG, "internal exception");
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t bdlm_workspace_size(int op, int64_t L, int64_t B, int Hq, int Hkv, int d, int P) {
+  (void)P;
+  if (check_shape(L, B, Hq, Hkv, d) != BDLM_OK) return 0;
+  switch (op) {
+    case BDLM_OP_FWD:
+    case BDLM_OP_FWD_SHARD:
+    case BDLM_OP_BWD_SHARD:
+      return kWsHeader;
+    case BDLM_OP_BWD:
+      return kWsHeader + 2 * (size_t)Hq * (size_t)L * sizeof(float);
+    default:
+      return 0;
+  }
+}
+
+bdlm_status bdlm_attn_fwd(const void* Qc, const void* Kc, const void* Vc, const void* Qn, const void* Kn,
+                          const void* Vn, int64_t L, int64_t B, int Hq, int Hkv, int d, float scale, void* Oc,
+                          void* On, bdlm_dtype o_dtype, float* LSEc, float* LSEn, void* workspace, size_t ws_bytes,
+                          bdlm_stream stream) {
+  return guarded([&]() -> bdlm_status {
+    BDLM_CHECK(check_shape(L, B, Hq, Hkv, d));
+    BDLM_CHECK(check_scale(scale));
+    if (o_dtype != BDLM_BF16 && o_dtype != BDLM_F32) return fail(BDLM_ERR_INVALID_ARG, "bad o_dtype %d", (int)o_dtype);
+    BDLM_CHECK(check_ptrs("bdlm_attn_fwd(Qc,Kc,Vc,Qn,Kn,Vn,Oc,On,LSEc,LSEn)",
+                          {Qc, Kc, Vc, Qn, Kn, Vn, Oc, On, LSEc, LSEn}));
+    BDLM_CHECK(check_ws(workspace, ws_bytes, bdlm_workspace_size(BDLM_OP_FWD, L, B, Hq, Hkv, d, 1)));
+    return fwd_common(Qc, Kc, Vc, Qn, Kn, Vn, L, B, Hq, Hkv, d, scale, 0, L, 1, Oc, On, o_dtype == BDLM_F32, LSEc,
+                      LSEn, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+  });
+}
+
+bdlm_status bdlm_attn_fwd_shard(const void* Qc, const void* Kc, const void* Vc, const void* Qn, const void* Kn,
+                                const void* Vn, int64_t L, int64_t B, int Hq, int Hkv, int d, float scale,
+                                int64_t kv_begin, int64_t kv_end, int include_local, float* Op_c, float* Op_n,
+                                float* LSEp_c, float* LSEp_n, void* workspace, size_t ws_bytes, bdlm_stream stream) {
+  return guarded([&]() -> bdlm_status {
+    BDLM_CHECK(check_shape(L, B, Hq, Hkv, d));
+    BDLM_CHECK(check_scale(scale));
+    if (kv_begin < 0 || kv_end < kv_begin || kv_end > L)
+      return fail(BDLM_ERR_SHAPE, "clean key range [%lld, %lld) is not inside [0, %lld)", (long long)kv_begin,
+                  (long long)kv_end, (long long)L);
+    BDLM_CHECK(check_ptrs("bdlm_attn_fwd_shard(Qc,Kc,Vc,Qn,Kn,Vn,Op_c,Op_n,LSEp_c,LSEp_n)",
+                          {Qc, Kc, Vc, Qn, Kn, Vn, Op_c, Op_n, LSEp_c, LSEp_n}));
+    BDLM_CHECK(check_ws(workspace, ws_bytes, bdlm_workspace_size(BDLM_OP_FWD_SHARD, L, B, Hq, Hkv, d, 1)));
+    return fwd_common(Qc, Kc, Vc, Qn, Kn, Vn, L, B, Hq, Hkv, d, scale, kv_begin, kv_end, include_local, Op_c, Op_n,
+                      1, LSEp_c, LSEp_n, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+  });
+}
+
+bdlm_status bdlm_lse_merge(int n_parts, const float* const* O_parts, const float* const* LSE_parts, int64_t rows,
+                           int H, int d, void* O, bdlm_dtype o_dtype, float* LSE, bdlm_stream stream) {
+  return guarded([&]() -> bdlm_status {
+    if (n_parts < 1 || n_parts > kMaxParts)
+      return fail(BDLM_ERR_INVALID_ARG, "n_parts=%d must be in [1, %d]", n_parts, kMaxParts);
+    if (!O_parts || !LSE_parts) return fail(BDLM_ERR_INVALID_ARG, "null partial pointer array");
+    if (rows <= 0 || H <= 0) return fail(BDLM_ERR_SHAPE, "rows=%lld and H=%d must be positive", (long long)rows, H);
+    if (d != 64 && d != 128) return fail(BDLM_ERR_SHAPE, "head dim d=%d must be 64 or 128", d);
+    if (o_dtype != BDLM_BF16 && o_dtype != BDLM_F32) return fail(BDLM_ERR_INVALID_ARG, "bad o_dtype %d", (int)o_dtype);
+    BDLM_CHECK(check_ptrs("bdlm_lse_merge(O)", {O}));
+    if (LSE && !aligned16(LSE)) return fail(BDLM_ERR_ALIGN, "LSE output not 16-byte aligned");
+    MergeParams p;
+    for (int i = 0; i < n_parts; ++i) {
+      BDLM_CHECK(check_ptrs("bdlm_lse_merge(O_parts[i], LSE_parts[i])", {O_parts[i], LSE_parts[i]}));
+      p.O[i] = O_parts[i];
+      p.LSE[i] = LSE_parts[i];
+    }
+    for (int i = n_parts; i < kMaxParts; ++i) p.O[i] = p.LSE[i] = nullptr;
+    DeviceInfo info;
+    BDLM_CHECK(device_info(info));
+    p.n = n_parts;
+    p.rows = rows;
+    p.H = H;
+    p.d = d;
+    p.out = O;
+    p.out_f32 = o_dtype == BDLM_F32;
+    p.lse_out = LSE;
+    int launches = 0;
+    ScopedKernelTimer tm(K_MERGE, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_merge(p, static_cast<cudaStream_t>(stream), &launches);
+    tm.stop();
+    return finish(e, launches, "merge launch");
+  });
+}
+
+bdlm_status bdlm_bwd_preprocess(const void* O, bdlm_dtype o_dtype, const void* dO, int64_t rows, int H, int d,
+                                float* D, bdlm_stream stream) {
+  return guarded([&]() -> bdlm_status {
+    if (rows <= 0 || H <= 0) return fail(BDLM_ERR_SHAPE, "rows=%lld and H=%d must be positive", (long long)rows, H);
+    if (d != 64 && d != 128) return fail(BDLM_ERR_SHAPE, "head dim d=%d must be 64 or 128", d);
+    if (o_dtype != BDLM_BF16 && o_dtype != BDLM_F32) return fail(BDLM_ERR_INVALID_ARG, "bad o_dtype %d", (int)o_dtype);
+    BDLM_CHECK(check_ptrs("bdlm_bwd_preprocess(O,dO,D)", {O, dO, D}));
+    DeviceInfo info;
+    BDLM_CHECK(device_info(info));
+    int launches = 0;
+    ScopedKernelTimer tm(K_PREP, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_preprocess(O, o_dtype == BDLM_F32, dO, rows, H, d, D, static_cast<cudaStream_t>(stream),
+                                      &launches);
+    tm.stop();
+    return finish(e, launches, "preprocess launch");
+  });
+}
+
+bdlm_status bdlm_attn_bwd(const void* Qc, const void* Kc, const void* Vc, const void* Qn, const void* Kn,
+                          const void* Vn, const void* Oc, const void* On, const void* dOc, const void* dOn,
+                          const float* LSEc, const float* LSEn, int64_t L, int64_t B, int Hq, int Hkv, int d,
+                          float scale, void* dQc, void* dKc, void* dVc, void* dQn, void* dKn, void* dVn,
+                          bdlm_dtype g_dtype, void* workspace, size_t ws_bytes, bdlm_stream stream) {
+  return guarded([&]() -> bdlm_status {
+    BDLM_CHECK(check_shape(L, B, Hq, Hkv, d));
+    BDLM_CHECK(check_scale(scale));
+    if (g_dtype != BDLM_BF16 && g_dtype != BDLM_F32) return fail(BDLM_ERR_INVALID_ARG, "bad g_dtype %d", (int)g_dtype);
+    BDLM_CHECK(check_ptrs("bdlm_attn_bwd(Qc,Kc,Vc,Qn,Kn,Vn,Oc,On,dOc,dOn,LSEc,LSEn)",
+                          {Qc, Kc, Vc, Qn, Kn, Vn, Oc, On, dOc, dOn, LSEc, LSEn}));
+    BDLM_CHECK(check_ptrs("bdlm_attn_bwd(dQc,dKc,dVc,dQn,dKn,dVn)", {dQc, dKc, dVc, dQn, dKn, dVn}));
+    BDLM_CHECK(check_ws(workspace, ws_bytes, bdlm_workspace_size(BDLM_OP_BWD, L, B, Hq, Hkv, d, 1)));
+    DeviceInfo info;
+    BDLM_CHECK(device_info(info));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float* Dc = reinterpret_cast<float*>(static_cast<char*>(workspace) + kWsHeader);
+    float* Dn = Dc + (size_t)Hq * L;
+    BDLM_CHECK(clear_status(workspace, st));
+    int launches = 0;
+    cudaError_t e;
+    {
+      ScopedKernelTimer tm(K_PREP, st);
+      e = launch_preprocess(Oc, 0, dOc, L, Hq, d, Dc, st, &launches);
+    }
+    if (e == cudaSuccess) {
+      ScopedKernelTimer tm(K_PREP, st);
+      e = launch_preprocess(On, 0, dOn, L, Hq, d, Dn, st, &launches);
+    }
+    BwdParams p = bwd_params(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn, L, B, Hq, Hkv, d, scale, 0, L, 1);
+    p.dQc = dQc; p.dQn = dQn; p.dKc = dKc; p.dVc = dVc; p.dKn = dKn; p.dVn = dVn;
+    p.g_f32 = g_dtype == BDLM_F32;
+    if (e == cudaSuccess) {
+      ScopedKernelTimer tm(K_DKV, st);
+      e = launch_bwd_dkv(p, st, &launches);
+    }
+    if (e == cudaSuccess) {
+      ScopedKernelTimer tm(K_DQ, st);
+      e = launch_bwd_dq(p, st, &launches);
+    }
+    return finish(e, launches, "backward launch");
+  });
+}
+
+bdlm_status bdlm_attn_bwd_shard(const void* Qc, const void* Kc, const void* Vc, const void* Qn, const void* Kn,
+                                const void* Vn, const void* dOc, const void* dOn, const float* LSEc,
+                                const float* LSEn, const float* Dc, const float* Dn, int64_t L, int64_t B, int Hq,
+                                int Hkv, int d, float scale, int64_t kv_begin, int64_t kv_end, int include_local,
+                                float* dQc_acc, float* dQn_acc, float* dKc, float* dVc, float* dKn, float* dVn,
+                                void* workspace, size_t ws_bytes, bdlm_stream stream) {
+  return guarded([&]() -> bdlm_status {
+    BDLM_CHECK(check_shape(L, B, Hq, Hkv, d));
+    BDLM_CHECK(check_scale(scale));
+    if (kv_begin < 0 || kv_end < kv_begin || kv_end > L)
+      return fail(BDLM_ERR_SHAPE, "clean key range [%lld, %lld) is not inside [0, %lld)", (long long)kv_begin,
+                  (long long)kv_end, (long long)L);
+    BDLM_CHECK(check_ptrs("bdlm_attn_bwd_shard(Qc,Kc,Vc,Qn,Kn,Vn,dOc,dOn,LSEc,LSEn,Dc,Dn)",
+                          {Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn}));
+    BDLM_CHECK(check_ptrs("bdlm_attn_bwd_shard(dQc_acc,dQn_acc,dKc,dVc,dKn,dVn)",
+                          {dQc_acc, dQn_acc, dKc, dVc, dKn, dVn}));
+    BDLM_CHECK(check_ws(workspace, ws_bytes, bdlm_workspace_size(BDLM_OP_BWD_SHARD, L, B, Hq, Hkv, d, 1)));
+    DeviceInfo info;
+    BDLM_CHECK(device_info(info));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    BDLM_CHECK(clear_status(workspace, st));
+    BwdParams p = bwd_params(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn, L, B, Hq, Hkv, d, scale, kv_begin,
+                             kv_end, include_local);
+    p.dQc = dQc_acc; p.dQn = dQn_acc; p.dKc = dKc; p.dVc = dVc; p.dKn = dKn; p.dVn = dVn;
+    p.g_f32 = 1;
+    p.dq_accumulate = 1;
+    int launches = 0;
+    cudaError_t e;
+    {
+      ScopedKernelTimer tm(K_DKV, st);
+      e = launch_bwd_dkv(p, st, &launches);
+    }
+    if (e == cudaSuccess) {
+      ScopedKernelTimer tm(K_DQ, st);
+      e = launch_bwd_dq(p, st, &launches);
+    }
+    return finish(e, launches, "sharded backward launch");
+  });
+}
+
+int64_t bdlm_worklist(int64_t L, int64_t B, int Hq, int Hkv, int tile_q, int tile_k, int64_t kv_begin,
+                      int64_t kv_end, int include_local, int32_t* out, int64_t cap) {
+  try {
+    if (L <= 0 || B <= 0 || L % B || Hq <= 0 || Hkv <= 0 || Hq % Hkv || tile_q <= 0 || tile_k <= 0) return -1;
+    if (kv_begin < 0 || kv_end < kv_begin || kv_end > L) return -1;
+    if (cap > 0 && !out) return -1;
+    const Geom g{L, B, Hq, Hkv, kv_begin, kv_end, include_local ? 1 : 0};
+    const int64_t n = q_items(g, tile_q);
+    for (int64_t i = 0; i < n && i < cap; ++i) {
+      const QItem it = q_item(g, tile_q, i);
+      const int64_t r0 = it.qtile * tile_q, r1 = imin64(r0 + tile_q, L);
+      const QTileRanges q = qtile_ranges(g, it.stream, r0, r1, tile_k);
+      int32_t* o = out + 8 * i;
+      o[0] = it.stream;
+      o[1] = it.head;
+      o[2] = (int32_t)it.qtile;
+      o[3] = (int32_t)q.c0;
+      o[4] = (int32_t)q.c1;
+      o[5] = (int32_t)q.n0;
+      o[6] = (int32_t)q.n1;
+      o[7] = (int32_t)((q.c1 - q.c0) + (q.n1 - q.n0));
+    }
+    return n;
+  } catch (...) {
+    return -1;
+  }
+}
+
+bdlm_status bdlm_sync_status(void* workspace, bdlm_stream stream) {
+  return guarded([&]() -> bdlm_status {
+    if (!workspace) return fail(BDLM_ERR_WORKSPACE, "workspace is null");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    uint32_t word = 0;
+    e = cudaMemcpy(&word, workspace, 4, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+    e = cudaMemset(workspace, 0, 4);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+    if (word != 0)
+      return fail(BDLM_ERR_TIMEOUT, "device wait limit expired (status 0x%x, wait site %u)", word, word & 0xffu);
+    return BDLM_OK;
+  });
+}
+
+bdlm_status bdlm_watchdog_selftest(void* workspace, size_t ws_bytes, uint32_t limit_us, bdlm_stream stream) {
+  return guarded([&]() -> bdlm_status {
+    BDLM_CHECK(check_ws(workspace, ws_bytes, kWsHeader));
+    if (limit_us == 0 || limit_us > 10000000u) return fail(BDLM_ERR_INVALID_ARG, "limit_us=%u out of (0, 1e7]", limit_us);
+    DeviceInfo info;
+    BDLM_CHECK(device_info(info));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    BDLM_CHECK(clear_status(workspace, st));
+    cudaError_t e = launch_watchdog(static_cast<uint32_t*>(workspace), (uint64_t)limit_us * 1000ull, st);
+    g_launches.fetch_add(1);
+    if (e != cudaSuccess) return cuda_fail(e, "watchdog launch");
+    return bdlm_sync_status(workspace, stream);
+  });
+}
+
+bdlm_status bdlm_timing_enable(int on) {
+  timing().on.store(on != 0);
+  return BDLM_OK;
+}
+
+int64_t bdlm_timing_report(char* buf, int64_t cap, int reset) {
+  try {
+    Timing& t = timing();
+    std::lock_guard<std::mutex> lock(t.mu);
+    bool cuda_ok = true;
+    for (auto& pd : t.pending) {
+      float ms = 0.f;
+      if (cudaEventSynchronize(pd.b) != cudaSuccess || cudaEventElapsedTime(&ms, pd.a, pd.b) != cudaSuccess)
+        cuda_ok = false;
+      t.total_ms[pd.kind] += ms;
+      t.count[pd.kind] += 1;
+      t.pool.push_back(pd.a);
+      t.pool.push_back(pd.b);
+    }
+    t.pending.clear();
+    std::string out;
+    for (int k = 0; k < K_COUNT; ++k) {
+      if (!t.count[k]) continue;
+      char line[160];
+      snprintf(line, sizeof(line), "%s %llu %.6f\n", kKindNames[k], (unsigned long long)t.count[k], t.total_ms[k]);
+      out += line;
+    }
+    if (buf && cap > 0) {
+      const size_t n = out.size() < (size_t)(cap - 1) ? out.size() : (size_t)(cap - 1);
+      memcpy(buf, out.data(), n);
+      buf[n] = 0;
+    }
+    if (reset) {
+      for (int k = 0; k < K_COUNT; ++k) {
+        t.total_ms[k] = 0.0;
+        t.count[k] = 0;
+      }
+    }
+    return cuda_ok ? (int64_t)out.size() : -1;
+  } catch (...) {
+    return -1;
+  }
+}
+
+uint64_t bdlm_kernel_launches(void) { return g_launches.load(); }
+
+const char* bdlm_last_error(void) { return g_last_error.c_str(); }
+
+const char* bdlm_version(void) { return "bdlm_attn 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,208 @@
+// geometry.cuh -- tile geometry of the two-stream BDLM block mask, shared by
+// the host work-list builder and the device kernels.
+//
+// Mask ("Block Parallelism For Efficient Distributed Long-Context Diffusion
+// Language Model Training", arxiv.science abstract: autoregressive across
+// blocks, parallel inside a block; evolve.pub review FAQ on CSBP: corrupted
+// blocks read the shared clean prefix and keep their own keys), with
+// blk(i) = i / B:
+//   clean row i     -> clean key j      iff blk(j) <= blk(i)
+//   corrupted row i -> clean key j      iff blk(j) <  blk(i)
+//   corrupted row i -> corrupted key j  iff blk(j) == blk(i)
+// A call may restrict the clean keys to one shard [kv_begin, kv_end) and drop
+// the corrupted own-block keys (include_local = 0): the per-shard view of CSBP.
+//
+// For one query row every visible key set is a half-open interval per key
+// stream, so masking a partially visible tile is an interval test, and the
+// visible key tiles of a query tile are two contiguous tile ranges.
+#pragma once
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define BDLM_HD __host__ __device__ __forceinline__
+#else
+#define BDLM_HD inline
+#endif
+
+namespace bdlm {
+
+struct Geom {
+  int64_t L, B;
+  int Hq, Hkv;
+  int64_t kv_begin, kv_end;  // clean key range of this call
+  int include_local;         // corrupted rows also read their own block
+};
+
+BDLM_HD int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+BDLM_HD int64_t imax64(int64_t a, int64_t b) { return a > b ? a : b; }
+BDLM_HD int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Visible clean-key interval [lo, hi) of query row i of `stream` (0 clean,
+// 1 corrupted); empty when hi <= lo.
+BDLM_HD void clean_interval(const Geom& g, int stream, int64_t i, int64_t& lo, int64_t& hi) {
+  const int64_t b = i / g.B;
+  const int64_t lim = stream == 0 ? (b + 1) * g.B : b * g.B;
+  lo = g.kv_begin;
+  hi = imin64(g.kv_end, lim);
+}
+
+// Visible corrupted-key interval of query row i (only corrupted rows, only
+// with include_local).
+BDLM_HD void noisy_interval(const Geom& g, int stream, int64_t i, int64_t& lo, int64_t& hi) {
+  if (stream == 1 && g.include_local) {
+    const int64_t b = i / g.B;
+    lo = b * g.B;
+    hi = (b + 1) * g.B;
+  } else {
+    lo = 0;
+    hi = 0;
+  }
+}
+
+BDLM_HD bool visible(const Geom& g, int stream, int64_t i, int key_stream, int64_t j) {
+  int64_t lo, hi;
+  if (key_stream == 0) clean_interval(g, stream, i, lo, hi);
+  else noisy_interval(g, stream, i, lo, hi);
+  return j >= lo && j < hi;
+}
+
+// Key-tile ranges [c0, c1) (clean) and [n0, n1) (corrupted) in units of tk
+// keys that the query rows [r0, r1) of `stream` can see, and for each range
+// the key interval every row of the tile sees (to tell full tiles from
+// partial ones).
+struct QTileRanges {
+  int64_t c0, c1, n0, n1;          // tile ranges
+  int64_t c_all_lo, c_all_hi;      // clean keys seen by every row
+  int64_t n_all_lo, n_all_hi;      // corrupted keys seen by every row
+};
+
+BDLM_HD QTileRanges qtile_ranges(const Geom& g, int stream, int64_t r0, int64_t r1, int tk) {
+  QTileRanges q;
+  int64_t lo_first, hi_first, lo_last, hi_last;
+  clean_interval(g, stream, r0, lo_first, hi_first);
+  clean_interval(g, stream, r1 - 1, lo_last, hi_last);
+  // union over rows: [kv_begin, hi of the last row); intersection: [kv_begin, hi of the first row)
+  if (hi_last > lo_last) {
+    q.c0 = lo_last / tk;
+    q.c1 = cdiv64(hi_last, tk);
+  } else {
+    q.c0 = q.c1 = 0;
+  }
+  q.c_all_lo = lo_first;
+  q.c_all_hi = hi_first;
+  int64_t nlo_first, nhi_first, nlo_last, nhi_last;
+  noisy_interval(g, stream, r0, nlo_first, nhi_first);
+  noisy_interval(g, stream, r1 - 1, nlo_last, nhi_last);
+  if (nhi_last > nlo_first) {
+    q.n0 = nlo_first / tk;
+    q.n1 = cdiv64(nhi_last, tk);
+  } else {
+    q.n0 = q.n1 = 0;
+  }
+  q.n_all_lo = nlo_last;   // largest lower bound
+  q.n_all_hi = nhi_first;  // smallest upper bound
+  return q;
+}
+
+// True when every (row, key) pair of the key tile [j0, j0 + tk) is visible to
+// every row of the query tile and the tile lies inside the sequence.
+BDLM_HD bool tile_full(int64_t j0, int tk, int64_t all_lo, int64_t all_hi, int64_t L) {
+  return j0 >= all_lo && j0 + tk <= all_hi && j0 + tk <= L;
+}
+
+// Forward / dQ work items: (query tile, head, stream), ordered by
+// non-increasing visible-key count.  For a fixed shard the visible key count
+// of a query tile never decreases with its position, so walking query tiles
+// from the last to the first is longest-first.  Inside one query-tile index
+// the two streams of one head are adjacent, then the heads of one GQA group,
+// so items running at the same time read the same key/value tiles.
+struct QItem {
+  int stream, head;
+  int64_t qtile;
+};
+
+BDLM_HD int64_t q_items(const Geom& g, int tq) { return cdiv64(g.L, tq) * g.Hq * 2; }
+
+BDLM_HD QItem q_item(const Geom& g, int tq, int64_t idx) {
+  const int64_t nqt = cdiv64(g.L, tq);
+  const int64_t per = (int64_t)g.Hq * 2;
+  QItem it;
+  it.qtile = nqt - 1 - idx / per;
+  const int64_t rem = idx % per;
+  it.stream = (int)(rem % 2);
+  it.head = (int)(rem / 2);
+  return it;
+}
+
+// Persistent-grid assignment: CTA `cta` of `grid` takes, in round r, the item
+// r*grid + cta on even rounds and r*grid + (grid-1-cta) on odd rounds.  Over
+// a longest-first list this boustrophedon order evens the CTAs' totals.
+BDLM_HD int64_t snake_item(int64_t round, int cta, int grid) {
+  const int pos = (round & 1) ? (grid - 1 - cta) : cta;
+  return round * grid + pos;
+}
+
+// dK/dV work items: (key stream, key/value head, key tile).  Clean key tiles
+// first in increasing position (a clean key is read by every later row, so
+// earlier tiles carry more work), then corrupted key tiles (each read only by
+// its own block's rows).  Only tiles that intersect this call's keys count.
+struct KVItem {
+  int key_stream, kv_head;
+  int64_t ktile;
+};
+
+BDLM_HD void kv_tile_span(const Geom& g, int tk, int64_t& c_first, int64_t& c_count, int64_t& n_count) {
+  if (g.kv_end > g.kv_begin) {
+    c_first = g.kv_begin / tk;
+    c_count = cdiv64(g.kv_end, tk) - c_first;
+  } else {
+    c_first = 0;
+    c_count = 0;
+  }
+  n_count = g.include_local ? cdiv64(g.L, tk) : 0;
+}
+
+BDLM_HD int64_t kv_items(const Geom& g, int tk) {
+  int64_t cf, cc, nc;
+  kv_tile_span(g, tk, cf, cc, nc);
+  return (cc + nc) * g.Hkv;
+}
+
+BDLM_HD KVItem kv_item(const Geom& g, int tk, int64_t idx) {
+  int64_t cf, cc, nc;
+  kv_tile_span(g, tk, cf, cc, nc);
+  KVItem it;
+  const int64_t t = idx / g.Hkv;
+  it.kv_head = (int)(idx % g.Hkv);
+  if (t < cc) {
+    it.key_stream = 0;
+    it.ktile = cf + t;
+  } else {
+    it.key_stream = 1;
+    it.ktile = t - cc;
+  }
+  return it;
+}
+
+// Query rows that can see some key of the key tile [j0, j1) of `key_stream`:
+// [c_lo, L) of clean rows and [n_lo, n_hi) of corrupted rows (empty if
+// hi <= lo).  A clean key of block b is read by clean rows of blocks >= b and
+// corrupted rows of blocks > b; a corrupted key only by its own block's
+// corrupted rows.  Keys outside this call's key set see no rows.
+BDLM_HD void kv_tile_rows(const Geom& g, int key_stream, int64_t j0, int64_t j1,
+                          int64_t& c_lo, int64_t& c_hi, int64_t& n_lo, int64_t& n_hi) {
+  if (key_stream == 0) {
+    const int64_t a = imax64(j0, g.kv_begin), z = imin64(j1, g.kv_end);
+    if (z <= a) { c_lo = c_hi = n_lo = n_hi = 0; return; }
+    const int64_t b = a / g.B;
+    c_lo = b * g.B; c_hi = g.L;
+    n_lo = (b + 1) * g.B; n_hi = g.L;
+  } else {
+    c_lo = c_hi = 0;
+    if (!g.include_local) { n_lo = n_hi = 0; return; }
+    n_lo = (j0 / g.B) * g.B;
+    n_hi = imin64(g.L, ((j1 - 1) / g.B + 1) * g.B);
+  }
+}
+
+}  // namespace bdlm

@@ -1,0 +1,75 @@
+// kernels.h -- launch interfaces of the device kernels (host side).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "geometry.cuh"
+
+namespace bdlm {
+
+// ------------------------------------------------------------- forward
+struct FwdParams {
+  Geom g;
+  float scale_log2;  // softmax scale * log2(e)
+  void* Oc;
+  void* On;
+  int o_f32;  // outputs fp32 (else bf16)
+  float* LSEc;
+  float* LSEn;
+  int64_t n_items;
+  uint32_t* status;
+  uint64_t limit_ns;
+};
+
+struct FwdMaps {
+  CUtensorMap Qc, Qn, Kc, Kn, Vc, Vn;
+};
+
+// Tile sizes of the tensor-core forward: 128 query rows x 128 keys.
+constexpr int kFwdTileQ = 128;
+constexpr int kFwdTileK = 128;
+
+cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, int d, int num_sms, cudaStream_t stream,
+                       int* launches);
+
+// ------------------------------------------------------------- backward
+struct BwdParams {
+  Geom g;
+  int d;
+  float scale;       // softmax scale (for dQ, dK)
+  float scale_log2;  // scale * log2(e)
+  const void *Qc, *Kc, *Vc, *Qn, *Kn, *Vn, *dOc, *dOn;  // bf16
+  const float *LSEc, *LSEn, *Dc, *Dn;                  // [Hq, L]
+  void *dQc, *dQn, *dKc, *dVc, *dKn, *dVn;
+  int g_f32;         // gradient outputs fp32 (else bf16)
+  int dq_accumulate; // dQ += contribution (fp32 only)
+};
+
+constexpr int kDkvTileK = 64;   // keys per dK/dV item
+constexpr int kDkvTileQ = 32;   // query rows per inner step
+constexpr int kDqTileQ = 64;    // query rows per dQ item
+constexpr int kDqTileK = 32;    // keys per inner step
+
+cudaError_t launch_bwd_dkv(const BwdParams& p, cudaStream_t stream, int* launches);
+cudaError_t launch_bwd_dq(const BwdParams& p, cudaStream_t stream, int* launches);
+
+// ------------------------------------------------------------- small kernels
+constexpr int kMaxParts = 32;
+struct MergeParams {
+  const float* O[kMaxParts];
+  const float* LSE[kMaxParts];
+  int n;
+  int64_t rows;
+  int H, d;
+  void* out;
+  int out_f32;
+  float* lse_out;
+};
+
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, int* launches);
+cudaError_t launch_preprocess(const void* O, int o_f32, const void* dO, int64_t rows, int H, int d, float* D,
+                              cudaStream_t stream, int* launches);
+cudaError_t launch_watchdog(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace bdlm

@@ -1,0 +1,144 @@
+// small_kernels.cu -- HBM-bound kernels: the exact LSE merge of partial
+// attention results, the backward row statistic D, and the watchdog
+// self-test.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace bdlm {
+namespace {
+
+// Merge of partial softmax-attention results over disjoint key sets (CSBP's
+// per-shard partials; Proposition 1, evolve.pub FAQ "Does CSBP change
+// training results?": equal to the unsharded result up to reduction order):
+//   M = max_p LSE_p, LSE = M + ln sum_p exp(LSE_p - M),
+//   O = sum_p exp(LSE_p - LSE) O_p, skipping LSE_p = -inf.
+// One warp per (head, row): lane p reads LSE_p; the warp then streams the
+// non-empty partials' O rows (HD fp32, 16 bytes per lane) in partial order.
+template <int HD>
+__global__ void __launch_bounds__(256) bdlm_merge_kernel(const MergeParams p) {
+  const int64_t wid = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= p.rows * p.H) return;
+  const int h = (int)(wid / p.rows);
+  const int64_t r = wid % p.rows;
+  const float lp = lane < p.n ? p.LSE[lane][(int64_t)h * p.rows + r] : -INFINITY;
+  float M = lp;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const bool any = M != -INFINITY;
+  const float w = (any && lp != -INFINITY) ? __expf(lp - M) : 0.f;
+  float tot = w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  const float inv = any ? 1.f / tot : 0.f;
+  constexpr int PER = HD / 32;  // floats per lane
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  const int64_t off = (r * p.H + h) * HD + lane * PER;
+  for (int q = 0; q < p.n; ++q) {
+    const float c = __shfl_sync(0xffffffffu, w, q) * inv;
+    if (c == 0.f) continue;
+    if (PER == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(p.O[q] + off);
+      acc[0] = fmaf(c, v.x, acc[0]);
+      acc[1] = fmaf(c, v.y, acc[1]);
+      acc[2] = fmaf(c, v.z, acc[2]);
+      acc[3] = fmaf(c, v.w, acc[3]);
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(p.O[q] + off);
+      acc[0] = fmaf(c, v.x, acc[0]);
+      acc[1] = fmaf(c, v.y, acc[1]);
+    }
+  }
+  if (p.out_f32) {
+    float* o = static_cast<float*>(p.out) + off;
+    if (PER == 4) *reinterpret_cast<float4*>(o) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    else *reinterpret_cast<float2*>(o) = make_float2(acc[0], acc[1]);
+  } else {
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + off;
+    if (PER == 4) *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]));
+    else *reinterpret_cast<uint32_t*>(o) = pack_bf16x2(acc[0], acc[1]);
+  }
+  if (p.lse_out && lane == 0) p.lse_out[(int64_t)h * p.rows + r] = any ? M + __logf(tot) : -INFINITY;
+}
+
+// D_i = sum_d dO_i * O_i, [H, rows] fp32 (the row statistic of the
+// softmax-attention backward).  One warp per (head, row).
+template <int HD>
+__global__ void __launch_bounds__(256) bdlm_preprocess_kernel(const void* O, int o_f32, const __nv_bfloat16* dO,
+                                                              int64_t rows, int H, float* D) {
+  const int64_t wid = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= rows * H) return;
+  const int h = (int)(wid / rows);
+  const int64_t r = wid % rows;
+  constexpr int PER = HD / 32;
+  const int64_t off = (r * H + h) * HD + lane * PER;
+  float o[PER], g[PER];
+  if (o_f32) {
+    const float* src = static_cast<const float*>(O) + off;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) o[i] = src[i];
+  } else {
+    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(O) + off;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) o[i] = __bfloat162float(src[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < PER; ++i) g[i] = __bfloat162float(dO[off + i]);
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc = fmaf(o[i], g[i], acc);
+#pragma unroll
+  for (int k = 16; k > 0; k >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, k);
+  if (lane == 0) D[(int64_t)h * rows + r] = acc;
+}
+
+// Waits on an mbarrier that nobody arrives on, through the same bounded wait
+// the attention kernels use; no asynchronous copy or MMA is in flight.
+__global__ void bdlm_watchdog_kernel(uint32_t* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const Watchdog wd{status, limit_ns, &abort_flag};
+  (void)mbar_wait(smem_u32(&bar), 0, wd, 0x7f);
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, int* launches) {
+  const int64_t warps = p.rows * p.H;
+  if (warps == 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((warps + 7) / 8);
+  if (p.d == 128) bdlm_merge_kernel<128><<<blocks, 256, 0, stream>>>(p);
+  else bdlm_merge_kernel<64><<<blocks, 256, 0, stream>>>(p);
+  if (launches) ++*launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_preprocess(const void* O, int o_f32, const void* dO, int64_t rows, int H, int d, float* D,
+                              cudaStream_t stream, int* launches) {
+  const int64_t warps = rows * H;
+  if (warps == 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((warps + 7) / 8);
+  const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(dO);
+  if (d == 128) bdlm_preprocess_kernel<128><<<blocks, 256, 0, stream>>>(O, o_f32, g, rows, H, D);
+  else bdlm_preprocess_kernel<64><<<blocks, 256, 0, stream>>>(O, o_f32, g, rows, H, D);
+  if (launches) ++*launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_watchdog(uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {
+  bdlm_watchdog_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace bdlm

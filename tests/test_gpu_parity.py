@@ -1,0 +1,194 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded bf16 inputs, at sizes the oracle finishes in seconds, covering
+several tiles, ragged tails and the degenerate block sizes."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle.bdlm_oracle as orc
+from structured_mask_attention_gb300.inputs import WORKLOADS, make_numpy
+from tests.parity_util import check_lse, check_rel, to_dev, to_np
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+NAMES = ("Qc", "Kc", "Vc", "Qn", "Kn", "Vn", "dOc", "dOn")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import structured_mask_attention_gb300 as m
+    m.load_library()
+    return m
+
+
+def _run_case(m, L, B, Hq, Hkv, d, seed=0, lognormal=0.0, bwd=True, o_dtype=None, brute=False):
+    X = make_numpy(L, Hq, Hkv, d, seed=seed, lognormal_sigma=lognormal)
+    dev = {k: to_dev(v, torch) for k, v in X.items()}
+    X64 = {k: v.astype(np.float64) for k, v in X.items()}
+    sc = 1.0 / math.sqrt(d)
+    ins = [dev[k] for k in NAMES[:6]]
+    Oc, On, LSEc, LSEn = m.bdlm_attn_fwd(*ins, B, sc, o_dtype=o_dtype)
+    fwd_ref = (orc.fwd_brute if brute else orc.fwd_blockwise)(*[X64[k] for k in NAMES[:6]], B, sc)
+    check_rel("Oc", to_np(Oc), fwd_ref[0])
+    check_rel("On", to_np(On), fwd_ref[1])
+    check_lse("LSEc", to_np(LSEc), fwd_ref[2])
+    check_lse("LSEn", to_np(LSEn), fwd_ref[3])
+    if not bwd:
+        return
+    # the GPU backward reads its own (bf16) O; the oracle uses its own O
+    if Oc.dtype != torch.bfloat16:
+        Oc, On = Oc.to(torch.bfloat16), On.to(torch.bfloat16)
+    grads = m.bdlm_attn_bwd(*ins, Oc, On, dev["dOc"], dev["dOn"], LSEc, LSEn, B, sc, g_dtype=torch.float32)
+    gref = (orc.bwd_brute if brute else orc.bwd_blockwise)(*[X64[k] for k in NAMES], B, sc)
+    for name, g, r in zip(("dQc", "dKc", "dVc", "dQn", "dKn", "dVn"), grads, gref):
+        check_rel(name, to_np(g), r)
+
+
+def test_tiny_workload_brute(lib):
+    w = WORKLOADS["tiny"]
+    _run_case(lib, w["L"], w["B"], w["Hq"], w["Hkv"], w["d"], seed=0, brute=True)
+
+
+@pytest.mark.parametrize("L,B,Hq,Hkv,d", [
+    (200, 40, 3, 1, 128),    # ragged q/k tail, blocks straddle tiles
+    (384, 128, 4, 2, 128),   # tile-aligned blocks, GQA 2
+    (160, 1, 2, 1, 64),      # token-causal clean stream
+    (192, 192, 2, 2, 128),   # one block: full attention per stream
+    (512, 256, 2, 1, 128),   # blocks larger than a tile
+    (640, 160, 5, 1, 64),    # GQA 5, blocks not a multiple of the tile
+    (96, 32, 1, 1, 128),     # shorter than one tile
+])
+def test_shapes(lib, L, B, Hq, Hkv, d):
+    _run_case(lib, L, B, Hq, Hkv, d, seed=L + B)
+
+
+def test_fp32_output(lib):
+    _run_case(lib, 256, 64, 2, 1, 128, seed=3, o_dtype=torch.float32, bwd=False)
+
+
+def test_lognormal_rows(lib):
+    _run_case(lib, 1024, 128, 4, 1, 128, seed=4, lognormal=0.5)
+
+
+def test_gqa_8k_workload_full(lib):
+    w = WORKLOADS["gqa-8k"]
+    _run_case(lib, w["L"], w["B"], w["Hq"], w["Hkv"], w["d"], seed=0)
+
+
+def _sharded(m, X, L, B, Hq, Hkv, d, P, sc):
+    dev = {k: to_dev(v, torch) for k, v in X.items()}
+    ins = [dev[k] for k in NAMES[:6]]
+    bounds = orc.shard_bounds(L, P)
+    parts = [m.bdlm_attn_fwd_shard(*ins, B, lo, hi, False, sc) for (lo, hi) in bounds]
+    parts.append(m.bdlm_attn_fwd_shard(*ins, B, 0, 0, True, sc))
+    Oc, LSEc = m.bdlm_lse_merge([p[0] for p in parts], [p[2] for p in parts], o_dtype=torch.float32)
+    On, LSEn = m.bdlm_lse_merge([p[1] for p in parts], [p[3] for p in parts], o_dtype=torch.float32)
+    return dev, ins, parts, (Oc, On, LSEc, LSEn), bounds
+
+
+@pytest.mark.parametrize("L,B,P", [(256, 32, 8), (4096, 128, 8), (4096, 1024, 8), (4096, 512, 8), (4096, 256, 8)])
+def test_shard_and_merge(lib, L, B, P):
+    """CSBP on one GPU: per-shard partials (each checked against the oracle's
+    partial), their LSE merge, and the sharded backward."""
+    m = lib
+    Hq, Hkv, d = (8, 4, 128) if L >= 4096 else (2, 1, 64)
+    X = make_numpy(L, Hq, Hkv, d, seed=P + B)
+    X64 = {k: v.astype(np.float64) for k, v in X.items()}
+    sc = 1.0 / math.sqrt(d)
+    dev, ins, parts, merged, bounds = _sharded(m, X, L, B, Hq, Hkv, d, P, sc)
+    (ref_fwd, ref_parts) = orc.fwd_sharded(*[X64[k] for k in NAMES[:6]], B, sc, P)
+    for k, (gp, rp) in enumerate(zip(parts, ref_parts)):
+        check_lse(f"LSEp_c[{k}]", to_np(gp[2]), rp[2])
+        check_lse(f"LSEp_n[{k}]", to_np(gp[3]), rp[3])
+        check_rel(f"Op_c[{k}]", to_np(gp[0]), rp[0])
+        check_rel(f"Op_n[{k}]", to_np(gp[1]), rp[1])
+    for name, g, r in zip(("Oc", "On"), merged[:2], ref_fwd[:2]):
+        check_rel(name, to_np(g), r)
+    check_lse("LSEc", to_np(merged[2]), ref_fwd[2])
+    check_lse("LSEn", to_np(merged[3]), ref_fwd[3])
+    # sharded backward with the merged statistics
+    Oc_b, On_b = merged[0].to(torch.bfloat16), merged[1].to(torch.bfloat16)
+    Dc = m.bdlm_bwd_preprocess(Oc_b, dev["dOc"])
+    Dn = m.bdlm_bwd_preprocess(On_b, dev["dOn"])
+    z = lambda H: torch.zeros((L, H, d), dtype=torch.float32, device="cuda")
+    dQc, dQn = z(Hq), z(Hq)
+    dKc, dVc, dKn, dVn = z(Hkv), z(Hkv), z(Hkv), z(Hkv)
+    for (lo, hi) in bounds:
+        m.bdlm_attn_bwd_shard(*ins, dev["dOc"], dev["dOn"], merged[2], merged[3], Dc, Dn, B, lo, hi, False,
+                              dQc, dQn, dKc, dVc, dKn, dVn, sc)
+    m.bdlm_attn_bwd_shard(*ins, dev["dOc"], dev["dOn"], merged[2], merged[3], Dc, Dn, B, 0, 0, True,
+                          dQc, dQn, dKc, dVc, dKn, dVn, sc)
+    gref = orc.bwd_blockwise(*[X64[k] for k in NAMES], B, sc)
+    for name, g, r in zip(("dQc", "dKc", "dVc", "dQn", "dKn", "dVn"), (dQc, dKc, dVc, dQn, dKn, dVn), gref):
+        check_rel(name, to_np(g), r)
+
+
+def test_sharded_matches_unsharded_fp32(lib):
+    """Shard-and-merge vs the unsharded kernel, both fp32 outputs, same
+    inputs: equal up to reduction order and bf16 rounding of P."""
+    m = lib
+    L, B, Hq, Hkv, d, P = 4096, 256, 8, 4, 128, 8
+    X = make_numpy(L, Hq, Hkv, d, seed=21)
+    sc = 1.0 / math.sqrt(d)
+    dev, ins, parts, merged, _ = _sharded(m, X, L, B, Hq, Hkv, d, P, sc)
+    Oc, On, LSEc, LSEn = m.bdlm_attn_fwd(*ins, B, sc, o_dtype=torch.float32)
+    dO = max((merged[0] - Oc).abs().max().item(), (merged[1] - On).abs().max().item())
+    dL = max((merged[2] - LSEc).abs().max().item(), (merged[3] - LSEn).abs().max().item())
+    print(f"sharded vs unsharded: max|dO| = {dO:.3e}, max|dLSE| = {dL:.3e}")
+    assert dL <= 1e-4
+    assert dO <= 2e-3
+
+
+def test_deterministic(lib):
+    m = lib
+    L, B, Hq, Hkv, d = 1024, 128, 4, 2, 128
+    X = make_numpy(L, Hq, Hkv, d, seed=9)
+    dev = {k: to_dev(v, torch) for k, v in X.items()}
+    ins = [dev[k] for k in NAMES[:6]]
+    outs = []
+    for _ in range(2):
+        f = m.bdlm_attn_fwd(*ins, B)
+        g = m.bdlm_attn_bwd(*ins, f[0], f[1], dev["dOc"], dev["dOn"], f[2], f[3], B)
+        outs.append([t.clone() for t in (*f, *g)])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
+def test_watchdog_reports_timeout(lib):
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    assert lib.bdlm_watchdog_selftest(ws, 20000) == 7
+    # the context is still usable afterwards
+    _run_case(lib, 128, 32, 1, 1, 64, seed=1, bwd=False)
+
+
+def test_abi_rejects_bad_arguments_on_gpu(lib):
+    m = lib
+    X = make_numpy(128, 2, 1, 64, seed=2)
+    dev = {k: to_dev(v, torch) for k, v in X.items()}
+    ins = [dev[k] for k in NAMES[:6]]
+    with pytest.raises(m.BdlmError) as e:
+        m.bdlm_attn_fwd(*ins, 48)  # 128 % 48 != 0
+    assert e.value.status == 2
+    ws = torch.zeros(8, dtype=torch.uint8, device="cuda")
+    with pytest.raises(m.BdlmError) as e:
+        m.bdlm_attn_bwd(*ins, dev["dOc"], dev["dOn"], dev["dOc"], dev["dOn"],
+                        torch.zeros(2, 128, device="cuda"), torch.zeros(2, 128, device="cuda"), 32, workspace=ws)
+    assert e.value.status == 4
+
+
+def test_launch_counter_counts_kernels(lib):
+    m = lib
+    X = make_numpy(256, 2, 1, 64, seed=2)
+    dev = {k: to_dev(v, torch) for k, v in X.items()}
+    ins = [dev[k] for k in NAMES[:6]]
+    n0 = m.bdlm_kernel_launches()
+    f = m.bdlm_attn_fwd(*ins, 32)
+    m.bdlm_attn_bwd(*ins, f[0], f[1], dev["dOc"], dev["dOn"], f[2], f[3], 32)
+    torch.cuda.synchronize()
+    assert m.bdlm_kernel_launches() - n0 == 1 + 4  # fwd; 2 preprocess + dK/dV + dQ
