@@ -183,7 +183,7 @@ def run_native(args, rank, world, local_rank):
     from structured_mask_attention_gb300.inputs import WORKLOADS, make_torch
 
     m.load_library()
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[args.workload]
     L, B, Hq, Hkv, d = w["L"], w["B"], w["Hq"], w["Hkv"], w["d"]
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -305,8 +305,8 @@ def run_native(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), bf16)",
-        "config": {"workload": WORKLOAD, "L": L, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d, "batch": 1,
-                   "tokens_per_step": 2 * L, "l2": "inputs larger than L2 (3 GiB per step)",
+        "config": {"workload": args.workload, "L": L, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d, "batch": 1,
+                   "tokens_per_step": 2 * L, "l2": "inputs larger than L2 (129 MB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "tokens_per_s": round(world * 2 * L / (ms_step * 1e-3), 1),
         "strict_tflops": round(world * strict_flops(L, B, Hq, d) / (ms_step * 1e-3) / 1e12, 3),
@@ -319,14 +319,14 @@ def run_native(args, rank, world, local_rank):
         line["cpu_baseline"] = {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": thr,
                                 "kind": "oracle",
                                 "sample": f"fp64 oracle fwd+bwd of the last {blocks} block(s) of one query head "
-                                          f"of {WORKLOAD} (both streams), {dt:.1f} s"}
+                                          f"of {args.workload} (both streams), {dt:.1f} s"}
     return line
 
 
 # ------------------------------------------------------------------ reference arm
 def run_reference(args):
     from structured_mask_attention_gb300.inputs import WORKLOADS
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[args.workload]
     L, B, Hq, Hkv, d = w["L"], w["B"], w["Hq"], w["Hkv"], w["d"]
     budget = max(1.0, min(args.cpu_budget, 240.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
@@ -336,13 +336,13 @@ def run_reference(args):
         f, t, nb, thr = oracle_sample(L, B, Hq, Hkv, d, budget)
         tot_f += f; tot_t += t; blocks += nb
     value = tot_f / tot_t / 1e12
-    sample = (f"fp64 oracle fwd+bwd of the last blocks of one query head of {WORKLOAD} (both streams), "
+    sample = (f"fp64 oracle fwd+bwd of the last blocks of one query head of {args.workload} (both streams), "
               f"{blocks} blocks over {args.steps} steps")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / args.steps, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1), bf16-rounded)",
-            "config": {"workload": WORKLOAD, "L": L, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d},
+            "config": {"workload": args.workload, "L": L, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -354,6 +354,8 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("native", "reference"), default="native")
+    ap.add_argument("--workload", choices=(WORKLOAD, "profile-16k"), default=WORKLOAD,
+                    help="profile-16k: the same head layout at 1/8 length, for profiler captures")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for the CPU baseline")

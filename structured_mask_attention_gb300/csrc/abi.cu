@@ -192,12 +192,13 @@ bdlm_status get_encoder(EncodeTiledFn& fn) {
   return BDLM_OK;
 }
 
-// [L, H, d] bf16 tensor as a 3-D TMA map (d innermost), box 64 x 1 x 128,
+// [L, H, d] bf16 tensor as a 3-D TMA map (d innermost), box 64 x 1 x box_rows,
 // 128-byte swizzle; out-of-range rows read as zero.
-bdlm_status encode_lhd(EncodeTiledFn fn, CUtensorMap* m, const void* ptr, int64_t L, int H, int d) {
+bdlm_status encode_lhd(EncodeTiledFn fn, CUtensorMap* m, const void* ptr, int64_t L, int H, int d,
+                       int box_rows = 128) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)L};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
-  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -278,6 +279,37 @@ BwdParams bwd_params(const void* Qc, const void* Kc, const void* Vc, const void*
   p.g_f32 = 0;
   p.dq_accumulate = 0;
   return p;
+}
+
+// Launches the dK/dV pass then the dQ pass for the key set of p.
+cudaError_t launch_backward_passes(const BwdParams& p, const DeviceInfo& info, void* ws, cudaStream_t st,
+                                   int* launches, bdlm_status* vstatus) {
+  *vstatus = BDLM_OK;
+  EncodeTiledFn enc;
+  if ((*vstatus = get_encoder(enc)) != BDLM_OK) return cudaSuccess;
+  BwdMaps m;
+  const int64_t L = p.g.L;
+  const int Hq = p.g.Hq, Hkv = p.g.Hkv, d = p.d;
+  struct E { CUtensorMap* map; const void* ptr; int H; int rows; };
+  const E list[16] = {{&m.Qc128, p.Qc, Hq, 128}, {&m.Qn128, p.Qn, Hq, 128}, {&m.dOc128, p.dOc, Hq, 128},
+                      {&m.dOn128, p.dOn, Hq, 128}, {&m.Kc64, p.Kc, Hkv, 64},   {&m.Kn64, p.Kn, Hkv, 64},
+                      {&m.Vc64, p.Vc, Hkv, 64},    {&m.Vn64, p.Vn, Hkv, 64},   {&m.Qc64, p.Qc, Hq, 64},
+                      {&m.Qn64, p.Qn, Hq, 64},     {&m.dOc64, p.dOc, Hq, 64},  {&m.dOn64, p.dOn, Hq, 64},
+                      {&m.Kc128, p.Kc, Hkv, 128},  {&m.Kn128, p.Kn, Hkv, 128}, {&m.Vc128, p.Vc, Hkv, 128},
+                      {&m.Vn128, p.Vn, Hkv, 128}};
+  for (const E& x : list)
+    if ((*vstatus = encode_lhd(enc, x.map, x.ptr, L, x.H, d, x.rows)) != BDLM_OK) return cudaSuccess;
+  uint32_t* status = static_cast<uint32_t*>(ws);
+  cudaError_t e;
+  {
+    ScopedKernelTimer tm(K_DKV, st);
+    e = launch_bwd_dkv_tc(m, p, info.sms, status, wait_limit_ns(), st, launches);
+  }
+  if (e == cudaSuccess) {
+    ScopedKernelTimer tm(K_DQ, st);
+    e = launch_bwd_dq_tc(m, p, info.sms, status, wait_limit_ns(), st, launches);
+  }
+  return e;
 }
 
 template <typename F>
@@ -429,14 +461,9 @@ bdlm_status bdlm_attn_bwd(const void* Qc, const void* Kc, const void* Vc, const 
     BwdParams p = bwd_params(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn, L, B, Hq, Hkv, d, scale, 0, L, 1);
     p.dQc = dQc; p.dQn = dQn; p.dKc = dKc; p.dVc = dVc; p.dKn = dKn; p.dVn = dVn;
     p.g_f32 = g_dtype == BDLM_F32;
-    if (e == cudaSuccess) {
-      ScopedKernelTimer tm(K_DKV, st);
-      e = launch_bwd_dkv(p, st, &launches);
-    }
-    if (e == cudaSuccess) {
-      ScopedKernelTimer tm(K_DQ, st);
-      e = launch_bwd_dq(p, st, &launches);
-    }
+    bdlm_status vs = BDLM_OK;
+    if (e == cudaSuccess) e = launch_backward_passes(p, info, workspace, st, &launches, &vs);
+    if (vs != BDLM_OK) return vs;
     return finish(e, launches, "backward launch");
   });
 }
@@ -468,15 +495,9 @@ bdlm_status bdlm_attn_bwd_shard(const void* Qc, const void* Kc, const void* Vc, 
     p.g_f32 = 1;
     p.dq_accumulate = 1;
     int launches = 0;
-    cudaError_t e;
-    {
-      ScopedKernelTimer tm(K_DKV, st);
-      e = launch_bwd_dkv(p, st, &launches);
-    }
-    if (e == cudaSuccess) {
-      ScopedKernelTimer tm(K_DQ, st);
-      e = launch_bwd_dq(p, st, &launches);
-    }
+    bdlm_status vs = BDLM_OK;
+    cudaError_t e = launch_backward_passes(p, info, workspace, st, &launches, &vs);
+    if (vs != BDLM_OK) return vs;
     return finish(e, launches, "sharded backward launch");
   });
 }

@@ -46,13 +46,15 @@ struct BwdParams {
   int dq_accumulate; // dQ += contribution (fp32 only)
 };
 
-constexpr int kDkvTileK = 64;   // keys per dK/dV item
-constexpr int kDkvTileQ = 32;   // query rows per inner step
-constexpr int kDqTileQ = 64;    // query rows per dQ item
-constexpr int kDqTileK = 32;    // keys per inner step
-
-cudaError_t launch_bwd_dkv(const BwdParams& p, cudaStream_t stream, int* launches);
-cudaError_t launch_bwd_dq(const BwdParams& p, cudaStream_t stream, int* launches);
+// Tensor maps of the tensor-core backward: 128-row and 64-row boxes.
+struct BwdMaps {
+  CUtensorMap Qc128, Qn128, dOc128, dOn128, Kc64, Kn64, Vc64, Vn64;  // dQ pass
+  CUtensorMap Qc64, Qn64, dOc64, dOn64, Kc128, Kn128, Vc128, Vn128;  // dK/dV pass
+};
+cudaError_t launch_bwd_dq_tc(const BwdMaps& m, const BwdParams& p, int num_sms, uint32_t* status,
+                             uint64_t limit_ns, cudaStream_t stream, int* launches);
+cudaError_t launch_bwd_dkv_tc(const BwdMaps& m, const BwdParams& p, int num_sms, uint32_t* status,
+                              uint64_t limit_ns, cudaStream_t stream, int* launches);
 
 // ------------------------------------------------------------- small kernels
 constexpr int kMaxParts = 32;

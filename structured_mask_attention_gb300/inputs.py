@@ -13,6 +13,7 @@ block size B, GQA with Hq query heads and Hkv key/value heads, head dim d):
 * ``gqa-32k``     L=32768,  B=256, Hq=40, Hkv=8, d=128  (+ LogNormal(0,0.5) Q/K rows)
 * ``long-128k``   L=131072, B=512, Hq=16, Hkv=8, d=128
 * ``sharded-256k`` L=262144, B in {128,256,512,1024}, Hq=8, Hkv=4, d=128, P=8
+* ``profile-16k`` L=16384, B=512, Hq=16, Hkv=8, d=128 (profiler captures)
 
 Draw order: Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn (each N(0,1) in fp32), then, when
 requested, one LogNormal(0, sigma) factor per token for each of Qc, Kc, Qn, Kn,
@@ -29,6 +30,9 @@ WORKLOADS = {
     "gqa-32k": dict(L=32768, B=256, Hq=40, Hkv=8, d=128),
     "long-128k": dict(L=131072, B=512, Hq=16, Hkv=8, d=128),
     "sharded-256k": dict(L=262144, B=1024, Hq=8, Hkv=4, d=128, P=8),
+    # same head layout and block size as long-128k at 1/8 of the length, for
+    # profiler captures (inputs ~0.4 GB, still larger than L2)
+    "profile-16k": dict(L=16384, B=512, Hq=16, Hkv=8, d=128),
 }
 SHARDED_BLOCK_SIZES = (128, 256, 512, 1024)
 
