@@ -29,6 +29,7 @@ def check_rel(name, got, ref, tol=REL_TOL):
     assert np.isfinite(got).all(), f"{name}: non-finite values"
     scale = np.abs(ref).max()
     err = np.abs(got - ref).max() if ref.size else 0.0
+    print(f"  {name}: max|err| / max|ref| = {err / max(scale, 1e-30):.3e}")
     assert err <= tol * max(scale, 1e-30), f"{name}: max err {err:.3e} > {tol} * {scale:.3e}"
     return err / max(scale, 1e-30)
 
@@ -39,5 +40,6 @@ def check_lse(name, got, ref, tol=LSE_TOL):
     fin = np.isfinite(ref)
     assert (np.isneginf(got) == ~fin).all(), f"{name}: -inf pattern differs"
     err = np.abs(got[fin] - ref[fin]).max() if fin.any() else 0.0
+    print(f"  {name}: max|err| = {err:.3e}")
     assert err <= tol, f"{name}: max err {err:.3e} > {tol}"
     return err
