@@ -141,6 +141,40 @@ bdlm_status bdlm_attn_bwd(const void* Qc, const void* Kc, const void* Vc,
                           void* dQc, void* dKc, void* dVc, void* dQn, void* dKn, void* dVn,
                           bdlm_dtype g_dtype, void* workspace, size_t ws_bytes, bdlm_stream stream);
 
+/* bdlm_attn_bwd for callers that cannot allocate device memory.  (The paper
+ * has no counterpart: this is a deployment variant of the backward.)
+ * Plugin hosts that hand a library only its input and output buffers,
+ * runtimes that reserve all device memory up front, and latency-critical
+ * code that avoids cudaMalloc (it may synchronize the device) cannot supply
+ * a workspace.  This call takes the same arguments as bdlm_attn_bwd minus
+ * the workspace and runs the same kernels with their workspace placed in a
+ * fixed 32 MiB array of device global memory declared by the library.
+ *  - Limit: the workspace (256 + 8 * Hq * L bytes) must fit the array, i.e.
+ *    Hq * L <= 4194272; larger shapes return BDLM_ERR_WORKSPACE, enqueue
+ *    nothing, and bdlm_last_error() names the limit.
+ *  - The array is created when the library's module is loaded on a device
+ *    and every GPU that loads it holds it until the process exits.  The first
+ *    call on a device also looks up the array's device address (once per
+ *    device, with that device current); make that first call before any
+ *    stream capture.
+ *  - Every call shares the one array per device and leaves its contents
+ *    behind; each call clears the status word and rewrites D before use.
+ *    Calls that overlap on the GPU (different streams, no ordering) race on
+ *    the array and must not be issued.
+ *  - No cudaMalloc, cudaFree or allocating library routine is called.  With
+ *    per-kernel timing enabled (bdlm_timing_enable), launches also record
+ *    CUDA events from a pool the library creates on first use: keep timing
+ *    off when no allocation at all is allowed.
+ * Kernel status (watchdog) is not reported through this call's return value;
+ * errors of the launches themselves are. */
+bdlm_status bdlm_attn_bwd_noalloc(const void* Qc, const void* Kc, const void* Vc,
+                                  const void* Qn, const void* Kn, const void* Vn,
+                                  const void* Oc, const void* On, const void* dOc, const void* dOn,
+                                  const float* LSEc, const float* LSEn,
+                                  int64_t L, int64_t B, int Hq, int Hkv, int d, float scale,
+                                  void* dQc, void* dKc, void* dVc, void* dQn, void* dKn, void* dVn,
+                                  bdlm_dtype g_dtype, bdlm_stream stream);
+
 /* Gradient contribution of one context shard, given the MERGED forward
  * statistics LSEc/LSEn and D (from bdlm_bwd_preprocess on the merged O):
  * keys are clean [kv_begin, kv_end) plus, if include_local, the corrupted own

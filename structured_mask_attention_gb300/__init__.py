@@ -18,7 +18,8 @@ import re
 
 __all__ = [
     "BdlmError", "load_library", "bdlm_workspace_size", "bdlm_attn_fwd", "bdlm_attn_fwd_shard",
-    "bdlm_lse_merge", "bdlm_bwd_preprocess", "bdlm_attn_bwd", "bdlm_attn_bwd_shard", "bdlm_worklist",
+    "bdlm_lse_merge", "bdlm_bwd_preprocess", "bdlm_attn_bwd", "bdlm_attn_bwd_noalloc", "bdlm_attn_bwd_shard",
+    "bdlm_worklist",
     "bdlm_sync_status", "bdlm_watchdog_selftest", "bdlm_kernel_launches", "bdlm_last_error",
     "bdlm_version", "bdlm_timing_enable", "bdlm_timing_report", "header_functions", "LIB_PATH",
     "HEADER_PATH",
@@ -58,6 +59,7 @@ _SIGS = {
     "bdlm_attn_bwd": (_I, [_P] * 12 + [_I64, _I64, _I, _I, _I, _F] + [_P] * 6 + [_I, _P, _SZ, _P]),
     "bdlm_attn_bwd_shard": (_I, [_P] * 12 + [_I64, _I64, _I, _I, _I, _F, _I64, _I64, _I] + [_P] * 6
                             + [_P, _SZ, _P]),
+    "bdlm_attn_bwd_noalloc": (_I, [_P] * 12 + [_I64, _I64, _I, _I, _I, _F] + [_P] * 6 + [_I, _P]),
     "bdlm_worklist": (_I64, [_I64, _I64, _I, _I, _I, _I, _I64, _I64, _I, _P, _I64]),
     "bdlm_sync_status": (_I, [_P, _P]),
     "bdlm_watchdog_selftest": (_I, [_P, _SZ, ctypes.c_uint32, _P]),
@@ -265,6 +267,27 @@ def bdlm_attn_bwd(Qc, Kc, Vc, Qn, Kn, Vn, Oc, On, dOc, dOn, LSEc, LSEn, B: int, 
         _ptr(Qc), _ptr(Kc), _ptr(Vc), _ptr(Qn), _ptr(Kn), _ptr(Vn), _ptr(Oc), _ptr(On), _ptr(dOc), _ptr(dOn),
         _ptr(LSEc), _ptr(LSEn), L, B, Hq, Hkv, d, scale, _ptr(dQc), _ptr(dKc), _ptr(dVc), _ptr(dQn), _ptr(dKn),
         _ptr(dVn), _dt(g_dtype), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def bdlm_attn_bwd_noalloc(Qc, Kc, Vc, Qn, Kn, Vn, Oc, On, dOc, dOn, LSEc, LSEn, B: int,
+                          scale: float | None = None, g_dtype=None, out=None, stream=None):
+    """bdlm_attn_bwd without a workspace argument, for callers that cannot
+    allocate device memory: the library uses its own fixed-size device array
+    (Hq * L <= 4194272).  Returns (dQc, dKc, dVc, dQn, dKn, dVn)."""
+    torch = _torch()
+    _check_inputs(Qc, Kc, Vc, Qn, Kn, Vn, Oc, On, dOc, dOn)
+    L, Hq, Hkv, d = _shape(Qc, Kc)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    g_dtype = torch.bfloat16 if g_dtype is None else g_dtype
+    if out is None:
+        mk = lambda H: torch.empty((L, H, d), dtype=g_dtype, device=Qc.device)
+        out = (mk(Hq), mk(Hkv), mk(Hkv), mk(Hq), mk(Hkv), mk(Hkv))
+    dQc, dKc, dVc, dQn, dKn, dVn = out
+    _check(load_library().bdlm_attn_bwd_noalloc(
+        _ptr(Qc), _ptr(Kc), _ptr(Vc), _ptr(Qn), _ptr(Kn), _ptr(Vn), _ptr(Oc), _ptr(On), _ptr(dOc), _ptr(dOn),
+        _ptr(LSEc), _ptr(LSEn), L, B, Hq, Hkv, d, scale, _ptr(dQc), _ptr(dKc), _ptr(dVc), _ptr(dQn), _ptr(dKn),
+        _ptr(dVn), _dt(g_dtype), _stream(stream)))
     return out
 
 

@@ -325,6 +325,8 @@ bdlm_status guarded(F&& f) {
 
 }  // namespace
 
+void bdlm::set_last_error(const std::string& msg) { g_last_error = msg; }
+
 extern "C" {
 
 size_t bdlm_workspace_size(int op, int64_t L, int64_t B, int Hq, int Hkv, int d, int P) {

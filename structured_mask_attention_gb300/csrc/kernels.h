@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <string>
+
 #include "geometry.cuh"
 
 namespace bdlm {
@@ -73,5 +75,8 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, int* launche
 cudaError_t launch_preprocess(const void* O, int o_f32, const void* dO, int64_t rows, int H, int d, float* D,
                               cudaStream_t stream, int* launches);
 cudaError_t launch_watchdog(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
+
+// Records the message bdlm_last_error() returns on this thread.
+void set_last_error(const std::string& msg);
 
 }  // namespace bdlm
