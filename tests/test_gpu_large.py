@@ -47,18 +47,28 @@ def _sample_rows(L, B, rng, n=12):
 
 def _invariants(X, grads, G):
     """Per KV head: sum over both streams' keys of dK is 0 and of dV equals the
-    sum of dO over the group's rows; errors bounded by the bf16 rounding of
-    ~sqrt(n) independent terms."""
+    sum of dO over the group's rows.  Two error terms bound the deviation:
+    bf16 rounding of P and dS, random across ~sqrt(n) keys, and the tensor
+    cores' fp32 accumulation over ~10^4 MMA steps per gradient element, which
+    truncates and shrinks each element by up to ~1e-3 relative (measured
+    shrinkage of the dV sums: 2e-4 to 7e-4 at L = 32768)."""
     dQc, dKc, dVc, dQn, dKn, dVn = [g.double() for g in grads]
     Hkv = dKc.shape[1]
     n = 2 * dKc.shape[0]
+    acc = 1e-3
     sK = dKc.sum(0) + dKn.sum(0)
     rmsK = torch.sqrt((dKc.square().sum(0) + dKn.square().sum(0)) / n)
-    assert (sK.abs() <= 2e-2 * math.sqrt(n) * rmsK + 1e-6).all(), float((sK.abs() / rmsK).max())
+    l1K = dKc.abs().sum(0) + dKn.abs().sum(0)
+    bound = 2e-2 * math.sqrt(n) * rmsK + acc * l1K + 1e-6
+    print(f"  sum dK: max |dev| / bound = {float((sK.abs() / bound).max()):.3f}")
+    assert (sK.abs() <= bound).all()
     sV = dVc.sum(0) + dVn.sum(0)
     dO = (X["dOc"].double() + X["dOn"].double()).sum(0).reshape(Hkv, G, -1).sum(1)
     rmsV = torch.sqrt((dVc.square().sum(0) + dVn.square().sum(0)) / n)
-    assert ((sV - dO).abs() <= 2e-2 * math.sqrt(n) * rmsV + 1e-6).all(), float(((sV - dO).abs() / rmsV).max())
+    l1V = dVc.abs().sum(0) + dVn.abs().sum(0)
+    bound = 2e-2 * math.sqrt(n) * rmsV + acc * l1V + 1e-6
+    print(f"  sum dV: max |dev| / bound = {float(((sV - dO).abs() / bound).max()):.3f}")
+    assert ((sV - dO).abs() <= bound).all()
 
 
 def _full_size_case(m, name, lognormal=0.0, groups=(0,), n_rows=12):
@@ -129,8 +139,13 @@ def test_sharded_256k_workload(lib, B):
     torch.cuda.synchronize()
     dO = max((Oc - Oc_u).abs().max().item(), (On - On_u).abs().max().item())
     dL = max((LSEc - LSEc_u).abs().max().item(), (LSEn - LSEn_u).abs().max().item())
-    print(f"B={B}: sharded vs unsharded fp32 max|dO| = {dO:.3e}, max|dLSE| = {dL:.3e}")
-    assert dL <= 1e-4 and dO <= 2e-3
+    # Both paths round P to bf16 (relative 2^-9) against different running
+    # maxima; each O row is a convex combination of V rows, so the two paths
+    # differ by at most 2 * 2^-9 * max|V|.
+    vmax = max(X["Vc"].abs().max().item(), X["Vn"].abs().max().item())
+    print(f"B={B}: sharded vs unsharded fp32 max|dO| = {dO:.3e} (bound {2 ** -8 * vmax:.3e}), "
+          f"max|dLSE| = {dL:.3e}")
+    assert dL <= 1e-4 and dO <= 2 ** -8 * vmax
     # merge kernel vs fp64 merge of the same fp32 partials, on sampled rows
     rng = np.random.default_rng(B)
     rows = np.sort(rng.choice(L, 64, replace=False))

@@ -140,9 +140,10 @@ def test_sharded_matches_unsharded_fp32(lib):
     Oc, On, LSEc, LSEn = m.bdlm_attn_fwd(*ins, B, sc, o_dtype=torch.float32)
     dO = max((merged[0] - Oc).abs().max().item(), (merged[1] - On).abs().max().item())
     dL = max((merged[2] - LSEc).abs().max().item(), (merged[3] - LSEn).abs().max().item())
-    print(f"sharded vs unsharded: max|dO| = {dO:.3e}, max|dLSE| = {dL:.3e}")
+    vmax = max(abs(X["Vc"]).max(), abs(X["Vn"]).max())
+    print(f"sharded vs unsharded: max|dO| = {dO:.3e} (bound {2 ** -8 * vmax:.3e}), max|dLSE| = {dL:.3e}")
     assert dL <= 1e-4
-    assert dO <= 2e-3
+    assert dO <= 2 ** -8 * vmax  # bf16 rounding of P in both paths, see test_gpu_large
 
 
 def test_deterministic(lib):
