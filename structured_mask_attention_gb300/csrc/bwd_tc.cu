@@ -7,25 +7,31 @@
 // evolve.pub FAQ on CSBP):
 //   P = exp(scale Q K^T - LSE), dP = dO V^T, dS = P o (dP - D),
 //   dV = sum_group P^T dO, dK = scale sum_group dS^T Q, dQ = scale dS K.
-// Two deterministic passes; every output element is written once:
+// Two deterministic passes; every output element is written once.
 //
-// dQ pass (bdlm_bwd_dq_tc): persistent, one item per (128-row query tile,
-//   head, stream) in the forward's longest-first order.  Q and dO stay in
-//   shared memory; 64-key K/V tiles stream through a 3-stage TMA ring.
-//   MMA warp: S = Q K^T and dP = dO V^T into one of two TMEM buffer pairs,
-//   then dQ += dS K (K read as an MN-major operand from the same tile).
-//   Elementwise warpgroup (thread = query row): P = exp2(S c - LSE2),
-//   dS = P (dP - D) -> bf16 swizzled shared tile (double-buffered).
+// Both kernels are persistent (one CTA per SM) with 10 warps:
+//   warp 0     producer: TMA tiles into shared-memory rings (and, for dK/dV,
+//              the LSE/D slices of each query tile through cp.async);
+//   warp 1     owns TMEM; one lane issues tcgen05.mma;
+//   warps 2-9  two elementwise warpgroups.  A thread owns one TMEM lane (a
+//              query row for dQ, a key row for dK/dV); the two warpgroups
+//              split the 64 columns of each step, 32 each, so every SM
+//              sub-partition runs two of these warps.  Tiles that every row
+//              sees completely take a branch-free path.
 //
-// dK/dV pass (bdlm_bwd_dkv_tc): persistent, one item per (key stream, KV
-//   head, 128-key tile): clean tiles first (they are read by every later
-//   row), then corrupted tiles.  K and V stay in shared memory; 64-row Q/dO
-//   tiles of every query head of the GQA group and both streams that can see
-//   the keys stream through a 2-stage ring (with their LSE and D slices).
-//   MMA warp: S^T = K Q^T, dP^T = V dO^T, then dV += P^T dO and
-//   dK += dS^T Q with Q/dO read as MN-major operands.  Elementwise warpgroup
-//   (thread = key row) forms P^T and dS^T.  dK and dV accumulate in TMEM
-//   across the whole group and are written once.
+// dQ pass (bdlm_bwd_dq_tc): item = (128-row query tile, head, stream), in the
+//   forward's longest-first order.  Q and dO stay in shared memory; 64-key K/V
+//   tiles stream through a 3-stage ring.  MMA: S = Q K^T and dP = dO V^T into
+//   one of two TMEM buffer pairs, then dQ += dS K (K read as an MN-major
+//   operand from the same tile).  dS goes to a swizzled bf16 shared tile.
+//
+// dK/dV pass (bdlm_bwd_dkv_tc): item = (key stream, KV head, 128-key tile):
+//   clean tiles first (read by every later row), then corrupted tiles.  K and
+//   V stay in shared memory; 64-row Q/dO tiles of every query head of the GQA
+//   group and both streams that see the keys stream through a 2-stage ring.
+//   MMA: S^T = K Q^T, dP^T = V dO^T, then dV += P^T dO and dK += dS^T Q with
+//   Q/dO read as MN-major operands.  dK and dV accumulate in TMEM across the
+//   whole group and are written once.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -34,8 +40,60 @@
 namespace bdlm {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kEwThreads = 256;  // elementwise threads (barrier arrival counts)
 constexpr float kLog2e = 1.4426950408889634f;
+
+// thread roles
+struct Role {
+  int warp, lane, quarter, half, row;
+  uint32_t tl;  // TMEM lane offset of this warp
+};
+__device__ __forceinline__ Role role() {
+  Role r;
+  r.warp = threadIdx.x >> 5;
+  r.lane = threadIdx.x & 31;
+  r.quarter = r.warp & 3;
+  r.half = (r.warp - 2) >> 2;  // valid for warps 2..9
+  r.row = r.quarter * 32 + r.lane;
+  r.tl = (uint32_t)(r.quarter * 32) << 16;
+  return r;
+}
+
+__device__ __forceinline__ void store_row32(void* base, int64_t off, const uint32_t (&u)[32], float mul, int f32,
+                                            int accumulate) {
+  if (f32) {
+    float4* o = reinterpret_cast<float4*>(static_cast<float*>(base) + off);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      float4 v = make_float4(__uint_as_float(u[4 * c]) * mul, __uint_as_float(u[4 * c + 1]) * mul,
+                             __uint_as_float(u[4 * c + 2]) * mul, __uint_as_float(u[4 * c + 3]) * mul);
+      if (accumulate) {
+        const float4 old = o[c];
+        v.x += old.x; v.y += old.y; v.z += old.z; v.w += old.w;
+      }
+      o[c] = v;
+    }
+  } else {
+    uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + off);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      o[c] = make_uint4(pack_bf16x2(__uint_as_float(u[8 * c + 0]) * mul, __uint_as_float(u[8 * c + 1]) * mul),
+                        pack_bf16x2(__uint_as_float(u[8 * c + 2]) * mul, __uint_as_float(u[8 * c + 3]) * mul),
+                        pack_bf16x2(__uint_as_float(u[8 * c + 4]) * mul, __uint_as_float(u[8 * c + 5]) * mul),
+                        pack_bf16x2(__uint_as_float(u[8 * c + 6]) * mul, __uint_as_float(u[8 * c + 7]) * mul));
+  }
+}
+
+// 32 bf16 pairs of one row half -> 4 swizzled 16-byte chunks of a 128-byte row
+__device__ __forceinline__ void store_half_row(uint32_t tile, int row, int half, const uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int ch = half * 4 + i;
+    st_shared_v4(tile + row * 128 + ((ch ^ (row & 7)) << 4), pk[4 * i + 0], pk[4 * i + 1], pk[4 * i + 2],
+                 pk[4 * i + 3]);
+  }
+}
 
 // ====================================================================== dQ
 constexpr int QBM = 128;  // query rows per item
@@ -101,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + LY::kBar + 8 * DQ_NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + LY::kBar + 8 * DQ_NBAR + 4);
   auto BAR = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Role R = role();
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(DQ_QFULL), 1);
@@ -112,16 +170,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(BAR(DQ_SFULL + s), 1);
-      mbar_init(BAR(DQ_SEMPTY + s), 128);
-      mbar_init(BAR(DQ_DSFULL + s), 128);
+      mbar_init(BAR(DQ_SEMPTY + s), kEwThreads);
+      mbar_init(BAR(DQ_DSFULL + s), kEwThreads);
       mbar_init(BAR(DQ_DSEMPTY + s), 1);
     }
     mbar_init(BAR(DQ_DONE), 1);
-    mbar_init(BAR(DQ_OEMPTY), 128);
+    mbar_init(BAR(DQ_OEMPTY), kEwThreads);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (R.warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -132,8 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Watchdog wd{status, limit_ns, abort_flag};
   const int grid = gridDim.x, cta = blockIdx.x;
   // TMEM columns: S[2] at 0/64, dP[2] at 128/192, dQ at 256
-  if (warp == 0) {
-    if (lane == 0) {
+  if (R.warp == 0) {
+    if (R.lane == 0) {
       uint32_t itn = 0, kvc = 0;
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
@@ -167,8 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++itn;
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0) {
+  } else if (R.warp == 1) {
+    if (R.lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(QBM, QBN, false, false);
       constexpr uint32_t kIdQ = idesc_bf16(QBM, HD, false, true);
       uint32_t itn = 0, kvc = 0, sc = 0, dc = 0;
@@ -224,9 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const uint32_t tl = (uint32_t)(quarter * 32) << 16;
+    // elementwise: thread = query row, warpgroup `half` = key columns [32 half, 32 half + 32)
+    const int row = R.row, half = R.half;
     uint32_t itn = 0, sc = 0, dc = 0;
     bool ok = true;
     for (int64_t rnd = 0; ok; ++rnd) {
@@ -236,17 +293,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t r = t.r0 + row;
       const bool valid = r < p.g.L;
       void* dqbase = t.stream ? p.dQn : p.dQc;
-      const int64_t oofs = (r * p.g.Hq + t.head) * HD;
+      const int64_t oofs = (r * p.g.Hq + t.head) * HD + half * (HD / 2);
       if (t.n == 0) {
         if (valid && !p.dq_accumulate) {
           if (p.g_f32) {
             float4* o = reinterpret_cast<float4*>(static_cast<float*>(dqbase) + oofs);
 #pragma unroll
-            for (int c = 0; c < HD / 4; ++c) o[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int c = 0; c < HD / 8; ++c) o[c] = make_float4(0.f, 0.f, 0.f, 0.f);
           } else {
             uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dqbase) + oofs);
 #pragma unroll
-            for (int c = 0; c < HD / 8; ++c) o[c] = make_uint4(0u, 0u, 0u, 0u);
+            for (int c = 0; c < HD / 16; ++c) o[c] = make_uint4(0u, 0u, 0u, 0u);
           }
         }
         continue;
@@ -255,8 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t clo, chi, nlo, nhi;
       clean_interval(p.g, t.stream, rr, clo, chi);
       noisy_interval(p.g, t.stream, rr, nlo, nhi);
-      const float lse2 = valid ? (t.stream ? p.LSEn : p.LSEc)[(int64_t)t.head * p.g.L + r] * kLog2e : 0.f;
+      const float nlse2 = valid ? -(t.stream ? p.LSEn : p.LSEc)[(int64_t)t.head * p.g.L + r] * kLog2e : 0.f;
       const float Dv = valid ? (t.stream ? p.Dn : p.Dc)[(int64_t)t.head * p.g.L + r] : 0.f;
+      const float sl2 = p.scale_log2;
       for (int j = 0; j < t.n; ++j, ++sc) {
         const bool cs = j < t.nc;
         const int64_t key0 = (cs ? t.q.c0 + j : t.q.n0 + (j - t.nc)) * QBN;
@@ -267,28 +325,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        float s[QBN], dp[QBN];
-#pragma unroll
-        for (int c4 = 0; c4 < QBN / 32; ++c4) {
-          uint32_t u[32];
-          tmem_ld32(tmem + tl + sb * QBN + c4 * 32, u);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) s[c4 * 32 + c] = __uint_as_float(u[c]);
-          tmem_ld32(tmem + tl + 128 + sb * QBN + c4 * 32, u);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) dp[c4 * 32 + c] = __uint_as_float(u[c]);
-        }
+        uint32_t us[32], ud[32];
+        tmem_ld32x2(tmem + R.tl + sb * QBN + half * 32, tmem + R.tl + 128 + sb * QBN + half * 32, us, ud);
         tc_fence_before();
         mbar_arrive(BAR(DQ_SEMPTY + sb));
-        const int64_t lo = (cs ? clo : nlo) - key0, hi = (cs ? chi : nhi) - key0;
-        uint32_t pk[QBN / 2];
+        uint32_t pk[16];
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < QBN; c += 2) {
-          float d0 = 0.f, d1 = 0.f;
-          if (full || (c >= lo && c < hi)) d0 = ex2_approx(fmaf(s[c], p.scale_log2, -lse2)) * (dp[c] - Dv);
-          if (full || (c + 1 >= lo && c + 1 < hi))
-            d1 = ex2_approx(fmaf(s[c + 1], p.scale_log2, -lse2)) * (dp[c + 1] - Dv);
-          pk[c / 2] = pack_bf16x2(d0, d1);
+          for (int c = 0; c < 32; c += 2) {
+            const float d0 = ex2_approx(fmaf(__uint_as_float(us[c]), sl2, nlse2)) * (__uint_as_float(ud[c]) - Dv);
+            const float d1 =
+                ex2_approx(fmaf(__uint_as_float(us[c + 1]), sl2, nlse2)) * (__uint_as_float(ud[c + 1]) - Dv);
+            pk[c / 2] = pack_bf16x2(d0, d1);
+          }
+        } else {
+          const int lo = (int)imax64(imin64((cs ? clo : nlo) - key0 - half * 32, 33), -1);
+          const int hi = (int)imax64(imin64((cs ? chi : nhi) - key0 - half * 32, 33), -1);
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float d0 = ex2_approx(fmaf(__uint_as_float(us[c]), sl2, nlse2)) * (__uint_as_float(ud[c]) - Dv);
+            float d1 = ex2_approx(fmaf(__uint_as_float(us[c + 1]), sl2, nlse2)) * (__uint_as_float(ud[c + 1]) - Dv);
+            d0 = (c >= lo && c < hi) ? d0 : 0.f;
+            d1 = (c + 1 >= lo && c + 1 < hi) ? d1 : 0.f;
+            pk[c / 2] = pack_bf16x2(d0, d1);
+          }
         }
         const int db = dc & 1;
         if (dc >= 2) {
@@ -296,11 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
         }
-#pragma unroll
-        for (int ch = 0; ch < QBN / 8; ++ch) {
-          const uint32_t addr = sDs + db * LY::kDsTile + row * 128 + ((ch ^ (row & 7)) << 4);
-          st_shared_v4(addr, pk[ch * 4 + 0], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-        }
+        store_half_row(sDs + db * LY::kDsTile, row, half, pk);
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(BAR(DQ_DSFULL + db));
@@ -312,34 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int c4 = 0; c4 < HD / 32; ++c4) {
+      for (int c4 = 0; c4 < HD / 64; ++c4) {
         uint32_t u[32];
-        tmem_ld32(tmem + tl + 256 + c4 * 32, u);
-        if (valid) {
-          if (p.g_f32) {
-            float4* o = reinterpret_cast<float4*>(static_cast<float*>(dqbase) + oofs + c4 * 32);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              float4 v = make_float4(__uint_as_float(u[4 * c]) * p.scale, __uint_as_float(u[4 * c + 1]) * p.scale,
-                                     __uint_as_float(u[4 * c + 2]) * p.scale,
-                                     __uint_as_float(u[4 * c + 3]) * p.scale);
-              if (p.dq_accumulate) {
-                const float4 old = o[c];
-                v.x += old.x; v.y += old.y; v.z += old.z; v.w += old.w;
-              }
-              o[c] = v;
-            }
-          } else {
-            uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dqbase) + oofs + c4 * 32);
-            const float sc2 = p.scale;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              o[c] = make_uint4(pack_bf16x2(__uint_as_float(u[8 * c + 0]) * sc2, __uint_as_float(u[8 * c + 1]) * sc2),
-                                pack_bf16x2(__uint_as_float(u[8 * c + 2]) * sc2, __uint_as_float(u[8 * c + 3]) * sc2),
-                                pack_bf16x2(__uint_as_float(u[8 * c + 4]) * sc2, __uint_as_float(u[8 * c + 5]) * sc2),
-                                pack_bf16x2(__uint_as_float(u[8 * c + 6]) * sc2, __uint_as_float(u[8 * c + 7]) * sc2));
-          }
-        }
+        tmem_ld32(tmem + R.tl + 256 + half * (HD / 2) + c4 * 32, u);
+        if (valid) store_row32(dqbase, oofs + c4 * 32, u, p.scale, p.g_f32, p.dq_accumulate);
       }
       tc_fence_before();
       mbar_arrive(BAR(DQ_OEMPTY));
@@ -348,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (*abort_flag) drain_after_abort(200);
-  if (warp == 1) {
+  if (R.warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -375,7 +407,7 @@ struct DkvLayout {
   static constexpr int kdO = kQ + KNS * kQTile;
   static constexpr int kPt = kdO + KNS * kQTile;
   static constexpr int kdSt = kPt + 2 * kPTile;
-  static constexpr int kStat = kdSt + 2 * kPTile;  // LSE2 and D per stage: KNS x 2 x 64 floats
+  static constexpr int kStat = kdSt + 2 * kPTile;  // per stage: LSE[64] then D[64], fp32
   static constexpr int kBar = kStat + KNS * 2 * KBN * 4;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
@@ -384,10 +416,10 @@ struct DkvLayout {
 struct DkvGeo {
   int ks, kvh;
   int64_t j0;
-  int64_t rlo[2], rhi[2];  // query rows of each stream that can see some key of the tile
-  int64_t t0[2];           // first query tile index of each stream
-  int nt[2];               // query tiles of each stream
-  int per_head, n;         // steps per head, total steps
+  int64_t rlo0, rhi0, rlo1, rhi1;  // query rows of each stream that can see some key of the tile
+  int64_t t00, t01;                // first query tile of each stream
+  int nt0, nt1;                    // query tiles of each stream
+  int per_head, n;                 // steps per head, total steps
 };
 
 __device__ __forceinline__ DkvGeo dkv_geo(const BwdParams& p, int64_t idx) {
@@ -397,18 +429,22 @@ __device__ __forceinline__ DkvGeo dkv_geo(const BwdParams& p, int64_t idx) {
   t.kvh = it.kv_head;
   t.j0 = it.ktile * KBM;
   const int64_t j1 = imin64(t.j0 + KBM, p.g.L);
-  kv_tile_rows(p.g, t.ks, t.j0, j1, t.rlo[0], t.rhi[0], t.rlo[1], t.rhi[1]);
-#pragma unroll
-  for (int s = 0; s < 2; ++s) {
-    if (t.rhi[s] > t.rlo[s]) {
-      t.t0[s] = t.rlo[s] / KBN;
-      t.nt[s] = (int)(cdiv64(t.rhi[s], KBN) - t.t0[s]);
-    } else {
-      t.t0[s] = 0;
-      t.nt[s] = 0;
-    }
+  kv_tile_rows(p.g, t.ks, t.j0, j1, t.rlo0, t.rhi0, t.rlo1, t.rhi1);
+  if (t.rhi0 > t.rlo0) {
+    t.t00 = t.rlo0 / KBN;
+    t.nt0 = (int)(cdiv64(t.rhi0, KBN) - t.t00);
+  } else {
+    t.t00 = 0;
+    t.nt0 = 0;
   }
-  t.per_head = t.nt[0] + t.nt[1];
+  if (t.rhi1 > t.rlo1) {
+    t.t01 = t.rlo1 / KBN;
+    t.nt1 = (int)(cdiv64(t.rhi1, KBN) - t.t01);
+  } else {
+    t.t01 = 0;
+    t.nt1 = 0;
+  }
+  t.per_head = t.nt0 + t.nt1;
   t.n = t.per_head * (p.g.Hq / p.g.Hkv);
   return t;
 }
@@ -416,13 +452,11 @@ __device__ __forceinline__ DkvGeo dkv_geo(const BwdParams& p, int64_t idx) {
 // step k of an item -> (query head, stream, first query row)
 __device__ __forceinline__ void dkv_step(const BwdParams& p, const DkvGeo& t, int k, int& head, int& s,
                                          int64_t& q0) {
-  const int G = p.g.Hq / p.g.Hkv;
-  (void)G;
   const int hh = k / t.per_head;
-  const int r = k % t.per_head;
+  const int r = k - hh * t.per_head;
   head = t.kvh * (p.g.Hq / p.g.Hkv) + hh;
-  s = r < t.nt[0] ? 0 : 1;
-  q0 = (s == 0 ? t.t0[0] + r : t.t0[1] + (r - t.nt[0])) * KBN;
+  s = r < t.nt0 ? 0 : 1;
+  q0 = (s == 0 ? t.t00 + r : t.t01 + (r - t.nt0)) * KBN;
 }
 
 // Query-row interval [lo, hi) of stream s that sees key j of key stream ks
@@ -456,33 +490,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw_u32);
   const uint32_t sK = base + LY::kK, sV = base + LY::kV, sQ = base + LY::kQ, sdO = base + LY::kdO,
-                 sPt = base + LY::kPt, sdSt = base + LY::kdSt;
-  float* sStat = reinterpret_cast<float*>(base_ptr + LY::kStat);  // [stage][lse2 | D][64]
+                 sPt = base + LY::kPt, sdSt = base + LY::kdSt, sStat = base + LY::kStat;
+  const float* stat_ptr = reinterpret_cast<const float*>(base_ptr + LY::kStat);
   const uint32_t bars = base + LY::kBar;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + LY::kBar + 8 * KV_NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + LY::kBar + 8 * KV_NBAR + 4);
   auto BAR = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Role R = role();
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(KV_KFULL), 1);
     mbar_init(BAR(KV_KEMPTY), 1);
     for (int s = 0; s < KNS; ++s) {
-      mbar_init(BAR(KV_QFULL + s), 1 + 32);  // expect_tx arrival + the warp's LSE/D stores
+      mbar_init(BAR(KV_QFULL + s), 1 + 32);  // expect_tx arrival + one cp.async arrival per producer lane
       mbar_init(BAR(KV_QEMPTY + s), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(BAR(KV_SFULL + s), 1);
-      mbar_init(BAR(KV_SEMPTY + s), 128);
-      mbar_init(BAR(KV_PFULL + s), 128);
+      mbar_init(BAR(KV_SEMPTY + s), kEwThreads);
+      mbar_init(BAR(KV_PFULL + s), kEwThreads);
       mbar_init(BAR(KV_PEMPTY + s), 1);
     }
     mbar_init(BAR(KV_ACCDONE), 1);
-    mbar_init(BAR(KV_ACCEMPTY), 128);
+    mbar_init(BAR(KV_ACCEMPTY), kEwThreads);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (R.warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -493,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Watchdog wd{status, limit_ns, abort_flag};
   const int grid = gridDim.x, cta = blockIdx.x;
   // TMEM columns: dK at 0, dV at 128, S^T[2] at 256/320, dP^T[2] at 384/448
-  if (warp == 0) {
+  if (R.warp == 0) {
     // ---------------------------------------------------------- producer (whole warp)
     uint32_t itn = 0, qc = 0;
     bool ok = true;
@@ -506,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(BAR(KV_KEMPTY), (itn - 1) & 1, wd, 41));
         if (!ok) break;
       }
-      if (lane == 0) {
+      if (R.lane == 0) {
         mbar_arrive_expect_tx(BAR(KV_KFULL), 2 * LY::kKTile);
         const CUtensorMap* mk = t.ks ? &tKn : &tKc;
         const CUtensorMap* mv = t.ks ? &tVn : &tVc;
@@ -525,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int head, s;
         int64_t q0;
         dkv_step(p, t, k, head, s, q0);
-        if (lane == 0) {
+        if (R.lane == 0) {
           mbar_arrive_expect_tx(BAR(KV_QFULL + st), 2 * LY::kQTile);
           const CUtensorMap* mq = s ? &tQn : &tQc;
           const CUtensorMap* mo = s ? &tdOn : &tdOc;
@@ -535,24 +569,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(sdO + st * LY::kQTile + pn * LY::kQPanel, mo, BAR(KV_QFULL + st), pn * 64, head, (int)q0);
           }
         }
+        // LSE and D of the tile's 64 rows, asynchronously (rows >= L read as 0)
         const float* LSE = (s ? p.LSEn : p.LSEc) + (int64_t)head * p.g.L;
         const float* Dr = (s ? p.Dn : p.Dc) + (int64_t)head * p.g.L;
-        float* stat = sStat + st * 2 * KBN;
+        const uint32_t stat = sStat + st * 2 * KBN * 4;
 #pragma unroll
-        for (int c = lane; c < KBN; c += 32) {
+        for (int c = R.lane; c < KBN; c += 32) {
           const int64_t r = q0 + c;
           const bool v = r < p.g.L;
-          stat[c] = v ? LSE[r] * kLog2e : 0.f;
-          stat[KBN + c] = v ? Dr[r] : 0.f;
+          cp_async4(stat + c * 4, LSE + (v ? r : 0), v);
+          cp_async4(stat + (KBN + c) * 4, Dr + (v ? r : 0), v);
         }
-        mbar_arrive(BAR(KV_QFULL + st));
+        cp_async_mbar_arrive(BAR(KV_QFULL + st));
       }
       if (!ok) break;
       ++itn;
     }
-  } else if (warp == 1) {
+  } else if (R.warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (R.lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(KBM, KBN, false, false);
       constexpr uint32_t kIdA = idesc_bf16(KBM, HD, false, true);
       uint32_t itn = 0, qc = 0, sc = 0, pc = 0;
@@ -611,70 +646,95 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- elementwise (thread = key row)
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const uint32_t tl = (uint32_t)(quarter * 32) << 16;
+    const int row = R.row, half = R.half;
     uint32_t itn = 0, qc = 0, sc = 0, pc = 0;
     bool ok = true;
+    const float sl2 = p.scale_log2;
     for (int64_t rnd = 0; ok; ++rnd) {
       const int64_t idx = snake_item(rnd, cta, grid);
       if (idx >= n_items) break;
       const DkvGeo t = dkv_geo(p, idx);
       if (t.n == 0) continue;
       const int64_t j = t.j0 + row;
-      int64_t klo[2], khi[2];
-      key_rows(p.g, t.ks, j, 0, klo[0], khi[0]);
-      key_rows(p.g, t.ks, j, 1, klo[1], khi[1]);
+      int64_t klo0, khi0, klo1, khi1;
+      key_rows(p.g, t.ks, j, 0, klo0, khi0);
+      key_rows(p.g, t.ks, j, 1, klo1, khi1);
       // rows every key of the tile sees (for the full-tile test)
-      int64_t alo[2], ahi[2];
+      int64_t alo0, ahi0, alo1, ahi1;
       {
         const int64_t jl = imin64(t.j0 + KBM, p.g.L) - 1;
         bool all_in = t.j0 + KBM <= p.g.L;
         if (t.ks == 0) all_in = all_in && t.j0 >= p.g.kv_begin && t.j0 + KBM <= p.g.kv_end;
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          int64_t a0, b0, a1, b1;
-          key_rows(p.g, t.ks, t.j0, s, a0, b0);
-          key_rows(p.g, t.ks, jl, s, a1, b1);
-          alo[s] = imax64(a0, a1);
-          ahi[s] = all_in ? imin64(b0, b1) : alo[s];
-        }
+        int64_t a0, b0, a1, b1;
+        key_rows(p.g, t.ks, t.j0, 0, a0, b0);
+        key_rows(p.g, t.ks, jl, 0, a1, b1);
+        alo0 = imax64(a0, a1);
+        ahi0 = all_in ? imin64(b0, b1) : alo0;
+        key_rows(p.g, t.ks, t.j0, 1, a0, b0);
+        key_rows(p.g, t.ks, jl, 1, a1, b1);
+        alo1 = imax64(a0, a1);
+        ahi1 = all_in ? imin64(b0, b1) : alo1;
       }
       for (int k = 0; k < t.n; ++k, ++qc, ++sc) {
         int head, s;
         int64_t q0;
         dkv_step(p, t, k, head, s, q0);
+        (void)head;
         const int st = qc % KNS;
         const int sb = sc & 1;
         ok = mbar_wait(BAR(KV_SFULL + sb), (sc >> 1) & 1, wd, 48);
-        if (ok) ok = mbar_wait(BAR(KV_QFULL + st), (qc / KNS) & 1, wd, 49);  // LSE/D visibility
+        if (ok) ok = mbar_wait(BAR(KV_QFULL + st), (qc / KNS) & 1, wd, 49);  // LSE/D landed
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        float sv[KBN], dpv[KBN];
-#pragma unroll
-        for (int c4 = 0; c4 < KBN / 32; ++c4) {
-          uint32_t u[32];
-          tmem_ld32(tmem + tl + 256 + sb * KBN + c4 * 32, u);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) sv[c4 * 32 + c] = __uint_as_float(u[c]);
-          tmem_ld32(tmem + tl + 384 + sb * KBN + c4 * 32, u);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) dpv[c4 * 32 + c] = __uint_as_float(u[c]);
-        }
+        uint32_t us[32], ud[32];
+        tmem_ld32x2(tmem + R.tl + 256 + sb * KBN + half * 32, tmem + R.tl + 384 + sb * KBN + half * 32, us, ud);
         tc_fence_before();
         mbar_arrive(BAR(KV_SEMPTY + sb));
-        const float* stat = sStat + st * 2 * KBN;
-        const bool full = q0 >= alo[s] && q0 + KBN <= ahi[s];
-        const int64_t lo = klo[s] - q0, hi = khi[s] - q0;
-        uint32_t pp[KBN / 2], dd[KBN / 2];
+        const float* stl = stat_ptr + st * 2 * KBN + half * 32;  // LSE of this half's 32 rows; D at +KBN
+        const bool full = s == 0 ? (q0 >= alo0 && q0 + KBN <= ahi0) : (q0 >= alo1 && q0 + KBN <= ahi1);
+        uint32_t pp[16], dd[16];
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < KBN; c += 2) {
-          float p0 = 0.f, p1 = 0.f;
-          if (full || (c >= lo && c < hi)) p0 = ex2_approx(fmaf(sv[c], p.scale_log2, -stat[c]));
-          if (full || (c + 1 >= lo && c + 1 < hi)) p1 = ex2_approx(fmaf(sv[c + 1], p.scale_log2, -stat[c + 1]));
-          pp[c / 2] = pack_bf16x2(p0, p1);
-          dd[c / 2] = pack_bf16x2(p0 * (dpv[c] - stat[KBN + c]), p1 * (dpv[c + 1] - stat[KBN + c + 1]));
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(stl + 4 * c4);
+            const float4 d4 = *reinterpret_cast<const float4*>(stl + KBN + 4 * c4);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pv[4], sv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = 4 * c4 + e;
+              pv[e] = ex2_approx(fmaf(__uint_as_float(us[c]), sl2, -lv[e] * kLog2e));
+              sv[e] = pv[e] * (__uint_as_float(ud[c]) - dv[e]);
+            }
+            pp[2 * c4] = pack_bf16x2(pv[0], pv[1]);
+            pp[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
+            dd[2 * c4] = pack_bf16x2(sv[0], sv[1]);
+            dd[2 * c4 + 1] = pack_bf16x2(sv[2], sv[3]);
+          }
+        } else {
+          const int64_t base_row = q0 + half * 32;
+          const int lo = (int)imax64(imin64((s == 0 ? klo0 : klo1) - base_row, 33), -1);
+          const int hi = (int)imax64(imin64((s == 0 ? khi0 : khi1) - base_row, 33), -1);
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(stl + 4 * c4);
+            const float4 d4 = *reinterpret_cast<const float4*>(stl + KBN + 4 * c4);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pv[4], sv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = 4 * c4 + e;
+              float pe = ex2_approx(fmaf(__uint_as_float(us[c]), sl2, -lv[e] * kLog2e));
+              pe = (c >= lo && c < hi) ? pe : 0.f;
+              pv[e] = pe;
+              sv[e] = pe * (__uint_as_float(ud[c]) - dv[e]);
+            }
+            pp[2 * c4] = pack_bf16x2(pv[0], pv[1]);
+            pp[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
+            dd[2 * c4] = pack_bf16x2(sv[0], sv[1]);
+            dd[2 * c4 + 1] = pack_bf16x2(sv[2], sv[3]);
+          }
         }
         const int pb = pc & 1;
         if (pc >= 2) {
@@ -682,12 +742,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
         }
-#pragma unroll
-        for (int ch = 0; ch < KBN / 8; ++ch) {
-          const uint32_t off = row * 128 + ((ch ^ (row & 7)) << 4);
-          st_shared_v4(sPt + pb * LY::kPTile + off, pp[ch * 4 + 0], pp[ch * 4 + 1], pp[ch * 4 + 2], pp[ch * 4 + 3]);
-          st_shared_v4(sdSt + pb * LY::kPTile + off, dd[ch * 4 + 0], dd[ch * 4 + 1], dd[ch * 4 + 2], dd[ch * 4 + 3]);
-        }
+        store_half_row(sPt + pb * LY::kPTile, row, half, pp);
+        store_half_row(sdSt + pb * LY::kPTile, row, half, dd);
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(BAR(KV_PFULL + pb));
@@ -702,32 +758,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool wr = j < p.g.L && (t.ks == 1 || (j >= p.g.kv_begin && j < p.g.kv_end));
       void* dKo = t.ks ? p.dKn : p.dKc;
       void* dVo = t.ks ? p.dVn : p.dVc;
-      const int64_t oofs = (j * p.g.Hkv + t.kvh) * HD;
+      const int64_t oofs = (j * p.g.Hkv + t.kvh) * HD + half * (HD / 2);
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        void* obase = which == 0 ? dKo : dVo;
-        const float mul = which == 0 ? p.scale : 1.f;
-#pragma unroll
-        for (int c4 = 0; c4 < HD / 32; ++c4) {
-          uint32_t u[32];
-          tmem_ld32(tmem + tl + which * 128 + c4 * 32, u);
-          if (wr) {
-            if (p.g_f32) {
-              float4* o = reinterpret_cast<float4*>(static_cast<float*>(obase) + oofs + c4 * 32);
-#pragma unroll
-              for (int c = 0; c < 8; ++c)
-                o[c] = make_float4(__uint_as_float(u[4 * c]) * mul, __uint_as_float(u[4 * c + 1]) * mul,
-                                   __uint_as_float(u[4 * c + 2]) * mul, __uint_as_float(u[4 * c + 3]) * mul);
-            } else {
-              uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(obase) + oofs + c4 * 32);
-#pragma unroll
-              for (int c = 0; c < 4; ++c)
-                o[c] = make_uint4(pack_bf16x2(__uint_as_float(u[8 * c + 0]) * mul, __uint_as_float(u[8 * c + 1]) * mul),
-                                  pack_bf16x2(__uint_as_float(u[8 * c + 2]) * mul, __uint_as_float(u[8 * c + 3]) * mul),
-                                  pack_bf16x2(__uint_as_float(u[8 * c + 4]) * mul, __uint_as_float(u[8 * c + 5]) * mul),
-                                  pack_bf16x2(__uint_as_float(u[8 * c + 6]) * mul, __uint_as_float(u[8 * c + 7]) * mul));
-            }
-          }
+      for (int c4 = 0; c4 < HD / 64; ++c4) {
+        uint32_t uk[32], uv[32];
+        tmem_ld32x2(tmem + R.tl + half * (HD / 2) + c4 * 32, tmem + R.tl + 128 + half * (HD / 2) + c4 * 32, uk, uv);
+        if (wr) {
+          store_row32(dKo, oofs + c4 * 32, uk, p.scale, p.g_f32, 0);
+          store_row32(dVo, oofs + c4 * 32, uv, 1.f, p.g_f32, 0);
         }
       }
       tc_fence_before();
@@ -737,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (*abort_flag) drain_after_abort(200);
-  if (warp == 1) {
+  if (R.warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

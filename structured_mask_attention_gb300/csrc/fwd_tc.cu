@@ -9,17 +9,20 @@
 // (clean keys restricted to [kv_begin, kv_end), corrupted own block optional:
 // CSBP, evolve.pub FAQ), writing O = 0, LSE = -inf for rows with no key.
 //
-// Design (one CTA per SM, persistent; 6 warps):
-//   warp 0      TMA producer: Q tile once per item, K and V tiles into a
-//               two-stage ring (128-byte swizzle, 64-column panels).
-//   warp 1      owns TMEM (512 columns); one lane issues tcgen05.mma:
-//               S = Q K^T into one of two TMEM S buffers, O += P V into TMEM.
-//   warps 2-5   softmax warpgroup, one query row per thread (TMEM lane):
-//               online softmax in the log2 domain with a lazy rescale (the
-//               running reference max only moves when the row max grows by
-//               more than 8, so O rarely needs a TMEM round trip), writes P as
-//               bf16 into a swizzled shared-memory tile, and runs the
-//               epilogue (O / l, LSE).
+// Design (one CTA per SM, persistent; 10 warps).  A CTA works on a PAIR of
+// 128-row query tiles at once: the clean and the corrupted tile of the same
+// head and position (equal work: both see (b+1)B keys per row).  Each tile
+// has its own Q, K and V shared-memory slots and its own TMEM S and O:
+//   warp 0      TMA producer (K of the next step as soon as the previous
+//               S MMA released the slot, V as soon as the previous PV did);
+//   warp 1      owns TMEM (512 columns); one lane issues tcgen05.mma, per
+//               tile and step: PV(j-1) then S(j) = Q K^T(j), alternating the
+//               two tiles so one tile's softmax overlaps the other's MMAs;
+//   warps 2-5   softmax warpgroup of tile 0, warps 6-9 of tile 1: one query
+//               row per thread, online softmax in the log2 domain with a lazy
+//               rescale (the reference max moves only when the row max grows
+//               by more than 8), P written back over S in TMEM as packed bf16
+//               and consumed from there by the PV MMA (A operand in TMEM).
 // Only key tiles some row of the query tile can see are visited; a per-row
 // interval test masks the tiles that are not fully visible.
 #include <cuda_bf16.h>
@@ -31,25 +34,21 @@ namespace bdlm {
 namespace {
 
 constexpr int BM = kFwdTileQ;   // query rows per tile
-constexpr int BN = kFwdTileK;   // keys per tile
-constexpr int NS = 2;           // K/V pipeline stages
-constexpr int kThreads = 192;
+constexpr int BN = kFwdTileK;   // keys per step
+constexpr int kThreads = 320;
 constexpr int kPanelBytes = 128 * 128;  // 128 rows x 128 bytes (64 bf16)
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// barrier slots
-enum { B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_VFULL = 4, B_KVEMPTY = 6, B_SFULL = 8, B_SEMPTY = 10,
-       B_PFULL = 12, B_PVDONE = 13, B_OEMPTY = 14, B_COUNT = 15 };
+// barrier slots, two of each (one per tile)
+enum { B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_SF = 12, B_PF = 14, B_PVD = 16, B_OE = 18,
+       B_COUNT = 20 };
 
 template <int HD>
 struct Layout {
   static constexpr int kTileBytes = 128 * HD * 2;  // 128 rows x HD bf16
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;
-  static constexpr int kV = kK + NS * kTileBytes;
-  static constexpr int kP = kV + NS * kTileBytes;
-  static constexpr int kBar = kP + BM * BN * 2;
+  // per tile t: Q at t * 3 * kTileBytes, K after it, V after K
+  static constexpr int kBar = 6 * kTileBytes;
   static constexpr int kBytes = kBar + 256;
   // 1024 bytes of slack for alignment; never below 120 KB so that a second
   // CTA cannot share the SM (each CTA holds all 512 TMEM columns).
@@ -92,29 +91,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw_u32);
-  const uint32_t sQ = base + LY::kQ, sK = base + LY::kK, sV = base + LY::kV, sP = base + LY::kP;
+  auto sQ = [&](int t) -> uint32_t { return base + (3 * t + 0) * LY::kTileBytes; };
+  auto sK = [&](int t) -> uint32_t { return base + (3 * t + 1) * LY::kTileBytes; };
+  auto sV = [&](int t) -> uint32_t { return base + (3 * t + 2) * LY::kTileBytes; };
   const uint32_t bars = base + LY::kBar;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + LY::kBar + 8 * B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + LY::kBar + 8 * B_COUNT + 4);
-  auto BAR = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+  auto BAR = [&](int i, int t) -> uint32_t { return bars + 8u * (uint32_t)(i + t); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(BAR(B_QFULL), 1);
-    mbar_init(BAR(B_QEMPTY), 1);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(BAR(B_KFULL + s), 1);
-      mbar_init(BAR(B_VFULL + s), 1);
-      mbar_init(BAR(B_KVEMPTY + s), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(BAR(B_QF, t), 1);
+      mbar_init(BAR(B_QE, t), 1);
+      mbar_init(BAR(B_KF, t), 1);
+      mbar_init(BAR(B_KE, t), 1);
+      mbar_init(BAR(B_VF, t), 1);
+      mbar_init(BAR(B_VE, t), 1);
+      mbar_init(BAR(B_SF, t), 1);
+      mbar_init(BAR(B_PF, t), 128);
+      mbar_init(BAR(B_PVD, t), 1);
+      mbar_init(BAR(B_OE, t), 128);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(BAR(B_SFULL + s), 1);
-      mbar_init(BAR(B_SEMPTY + s), 128);
-    }
-    mbar_init(BAR(B_PFULL), 128);
-    mbar_init(BAR(B_PVDONE), 1);
-    mbar_init(BAR(B_OEMPTY), 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -128,42 +127,62 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const Watchdog wd{p.status, p.limit_ns, abort_flag};
   const int grid = gridDim.x, cta = blockIdx.x;
+  const int64_t n_pairs = p.n_items / 2;  // items 2i, 2i+1: clean and corrupted tile of one head/position
+  // TMEM columns: S of tile t at 128 t (P over its first 64 columns), O of tile t at 256 + 128 t
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tQc); tma_prefetch_desc(&tQn); tma_prefetch_desc(&tKc);
       tma_prefetch_desc(&tKn); tma_prefetch_desc(&tVc); tma_prefetch_desc(&tVn);
-      uint32_t itn = 0, kvc = 0;
+      uint32_t qc[2] = {0, 0}, kc[2] = {0, 0}, vc[2] = {0, 0};
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
-        const int64_t idx = snake_item(rnd, cta, grid);
-        if (idx >= p.n_items) break;
-        const ItemGeo t = item_geo(p, idx);
-        if (t.n == 0) continue;
-        if (itn > 0 && !mbar_wait(BAR(B_QEMPTY), (itn - 1) & 1, wd, 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(BAR(B_QFULL), LY::kTileBytes);
-        const CUtensorMap* mq = t.stream ? &tQn : &tQc;
-#pragma unroll
-        for (int pn = 0; pn < HD / 64; ++pn)
-          tma_load_3d(sQ + pn * kPanelBytes, mq, BAR(B_QFULL), pn * 64, t.head, (int)t.r0);
-        for (int j = 0; j < t.n; ++j, ++kvc) {
-          const int st = kvc % NS;
-          if (kvc >= NS && !mbar_wait(BAR(B_KVEMPTY + st), ((kvc / NS) - 1) & 1, wd, 2)) { ok = false; break; }
-          const bool cs = j < t.nc;
-          const int key0 = (int)tile_key0(t, j);
-          const CUtensorMap* mk = cs ? &tKc : &tKn;
-          const CUtensorMap* mv = cs ? &tVc : &tVn;
-          mbar_arrive_expect_tx(BAR(B_KFULL + st), LY::kTileBytes);
+        const int64_t pi = snake_item(rnd, cta, grid);
+        if (pi >= n_pairs) break;
+        const ItemGeo g0 = item_geo(p, 2 * pi), g1 = item_geo(p, 2 * pi + 1);
+        const int nmax = g0.n > g1.n ? g0.n : g1.n;
+        #pragma unroll
+        for (int t = 0; t < 2 && ok; ++t) {
+          const ItemGeo& g = t ? g1 : g0;
+          if (g.n == 0) continue;
+          if (qc[t] > 0 && !mbar_wait(BAR(B_QE, t), (qc[t] - 1) & 1, wd, 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(BAR(B_QF, t), LY::kTileBytes);
+          const CUtensorMap* mq = g.stream ? &tQn : &tQc;
 #pragma unroll
           for (int pn = 0; pn < HD / 64; ++pn)
-            tma_load_3d(sK + st * LY::kTileBytes + pn * kPanelBytes, mk, BAR(B_KFULL + st), pn * 64, t.kvh, key0);
-          mbar_arrive_expect_tx(BAR(B_VFULL + st), LY::kTileBytes);
-#pragma unroll
-          for (int pn = 0; pn < HD / 64; ++pn)
-            tma_load_3d(sV + st * LY::kTileBytes + pn * kPanelBytes, mv, BAR(B_VFULL + st), pn * 64, t.kvh, key0);
+            tma_load_3d(sQ(t) + pn * kPanelBytes, mq, BAR(B_QF, t), pn * 64, g.head, (int)g.r0);
+          ++qc[t];
         }
-        ++itn;
+        for (int j = 0; j < nmax && ok; ++j) {
+          // K of both tiles first (their slots free up early), then V
+          #pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const ItemGeo& g = t ? g1 : g0;
+            if (j >= g.n) continue;
+            if (kc[t] > 0 && !mbar_wait(BAR(B_KE, t), (kc[t] - 1) & 1, wd, 2)) { ok = false; break; }
+            const CUtensorMap* mk = j < g.nc ? &tKc : &tKn;
+            const int key0 = (int)tile_key0(g, j);
+            mbar_arrive_expect_tx(BAR(B_KF, t), LY::kTileBytes);
+#pragma unroll
+            for (int pn = 0; pn < HD / 64; ++pn)
+              tma_load_3d(sK(t) + pn * kPanelBytes, mk, BAR(B_KF, t), pn * 64, g.kvh, key0);
+            ++kc[t];
+          }
+          #pragma unroll
+          for (int t = 0; t < 2 && ok; ++t) {
+            const ItemGeo& g = t ? g1 : g0;
+            if (j >= g.n) continue;
+            if (vc[t] > 0 && !mbar_wait(BAR(B_VE, t), (vc[t] - 1) & 1, wd, 3)) { ok = false; break; }
+            const CUtensorMap* mv = j < g.nc ? &tVc : &tVn;
+            const int key0 = (int)tile_key0(g, j);
+            mbar_arrive_expect_tx(BAR(B_VF, t), LY::kTileBytes);
+#pragma unroll
+            for (int pn = 0; pn < HD / 64; ++pn)
+              tma_load_3d(sV(t) + pn * kPanelBytes, mv, BAR(B_VF, t), pn * 64, g.kvh, key0);
+            ++vc[t];
+          }
+        }
       }
     }
   } else if (warp == 1) {
@@ -171,73 +190,80 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16(BM, BN, false, false);
       constexpr uint32_t kIdescO = idesc_bf16(BM, HD, false, true);
-      const uint32_t tS = tmem, tO = tmem + 256;
-      uint32_t itn = 0, kvc = 0, sc = 0, pc = 0;
+      uint32_t qc[2] = {0, 0}, kc[2] = {0, 0}, vc[2] = {0, 0}, pc[2] = {0, 0}, oc[2] = {0, 0};
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
-        const int64_t idx = snake_item(rnd, cta, grid);
-        if (idx >= p.n_items) break;
-        const ItemGeo t = item_geo(p, idx);
-        if (t.n == 0) continue;
-        if (!mbar_wait(BAR(B_QFULL), itn & 1, wd, 3)) { ok = false; break; }
-        const uint32_t kv_base = kvc;
-        auto do_pv = [&](int jj) -> bool {
-          const uint32_t kv = kv_base + jj;
-          const int st = kv % NS;
-          if (!mbar_wait(BAR(B_PFULL), pc & 1, wd, 4)) return false;
-          if (jj == 0 && itn > 0 && !mbar_wait(BAR(B_OEMPTY), (itn - 1) & 1, wd, 5)) return false;
-          if (!mbar_wait(BAR(B_VFULL + st), (kv / NS) & 1, wd, 6)) return false;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(sP + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(sV + st * LY::kTileBytes + kk * 2048, kPanelBytes, 1024);
-            tc_mma_ss(tO, ad, bd, kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc_commit(BAR(B_KVEMPTY + st));
-          tc_commit(BAR(B_PVDONE));
-          ++pc;
-          return true;
-        };
-        for (int j = 0; j < t.n && ok; ++j, ++kvc, ++sc) {
-          const int st = kvc % NS;
-          const int sb = sc & 1;
-          if (!mbar_wait(BAR(B_KFULL + st), (kvc / NS) & 1, wd, 7)) { ok = false; break; }
-          if (sc >= 2 && !mbar_wait(BAR(B_SEMPTY + sb), ((sc >> 1) - 1) & 1, wd, 8)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(sK + st * LY::kTileBytes + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
-            tc_mma_ss(tS + sb * BN, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
-          }
-          tc_commit(BAR(B_SFULL + sb));
-          if (j == t.n - 1) tc_commit(BAR(B_QEMPTY));
-          if (j >= 1 && !do_pv(j - 1)) { ok = false; break; }
+        const int64_t pi = snake_item(rnd, cta, grid);
+        if (pi >= n_pairs) break;
+        const ItemGeo g0 = item_geo(p, 2 * pi), g1 = item_geo(p, 2 * pi + 1);
+        const int nmax = g0.n > g1.n ? g0.n : g1.n;
+        #pragma unroll
+        for (int t = 0; t < 2 && ok; ++t) {
+          const ItemGeo& g = t ? g1 : g0;
+          if (g.n == 0) continue;
+          if (!mbar_wait(BAR(B_QF, t), qc[t] & 1, wd, 4)) { ok = false; break; }
+          ++qc[t];
         }
-        if (!ok) break;
-        if (!do_pv(t.n - 1)) { ok = false; break; }
-        ++itn;
+        for (int j = 0; j <= nmax && ok; ++j) {
+          #pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const ItemGeo& g = t ? g1 : g0;
+            const uint32_t tS = tmem + t * 128, tO = tmem + 256 + t * 128;
+            if (j >= 1 && j <= g.n) {
+              // PV(j-1): O += P V with P (bf16) in TMEM over S
+              if (!mbar_wait(BAR(B_PF, t), pc[t] & 1, wd, 5)) { ok = false; break; }
+              if (j == 1 && oc[t] > 0 && !mbar_wait(BAR(B_OE, t), (oc[t] - 1) & 1, wd, 6)) { ok = false; break; }
+              if (!mbar_wait(BAR(B_VF, t), vc[t] & 1, wd, 7)) { ok = false; break; }
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < BN / 16; ++kk) {
+                const uint64_t bd = sdesc_sw128(sV(t) + kk * 2048, kPanelBytes, 1024);
+                tc_mma_ts(tO, tS + kk * 8, bd, kIdescO, (j > 1 || kk > 0) ? 1u : 0u);
+              }
+              tc_commit(BAR(B_VE, t));
+              tc_commit(BAR(B_PVD, t));
+              ++pc[t];
+              ++vc[t];
+              if (j == g.n) ++oc[t];
+            }
+            if (j < g.n) {
+              // S(j) = Q K^T(j); issued after PV(j-1) so it never overwrites an unread P
+              if (!mbar_wait(BAR(B_KF, t), kc[t] & 1, wd, 8)) { ok = false; break; }
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < HD / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                tc_mma_ss(tS, sdesc_sw128(sQ(t) + off, 16, 1024), sdesc_sw128(sK(t) + off, 16, 1024), kIdescS,
+                          kk > 0 ? 1u : 0u);
+              }
+              tc_commit(BAR(B_SF, t));
+              tc_commit(BAR(B_KE, t));
+              if (j == g.n - 1) tc_commit(BAR(B_QE, t));
+              ++kc[t];
+            }
+          }
+        }
       }
     }
   } else {
-    // ------------------------------------------------------------ softmax
+    // ------------------------------------------------------------ softmax (thread = row of tile t)
+    const int t = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t tl = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tS = tmem + tl, tO = tmem + tl + 256;
+    const uint32_t tS = tmem + tl + t * 128, tO = tmem + tl + 256 + t * 128;
     uint32_t sc = 0, pc = 0;
     bool ok = true;
     for (int64_t rnd = 0; ok; ++rnd) {
-      const int64_t idx = snake_item(rnd, cta, grid);
-      if (idx >= p.n_items) break;
-      const ItemGeo t = item_geo(p, idx);
-      const int64_t r = t.r0 + row;
+      const int64_t pi = snake_item(rnd, cta, grid);
+      if (pi >= n_pairs) break;
+      const ItemGeo g = item_geo(p, 2 * pi + t);
+      const int64_t r = g.r0 + row;
       const bool valid = r < p.g.L;
-      float* lse_out = (t.stream ? p.LSEn : p.LSEc) + (int64_t)t.head * p.g.L;
-      void* obase = t.stream ? p.On : p.Oc;
-      const int64_t oofs = (r * p.g.Hq + t.head) * HD;
-      if (t.n == 0) {
+      float* lse_out = (g.stream ? p.LSEn : p.LSEc) + (int64_t)g.head * p.g.L;
+      void* obase = g.stream ? p.On : p.Oc;
+      const int64_t oofs = (r * p.g.Hq + g.head) * HD;
+      if (g.n == 0) {
         if (valid) {
           if (p.o_f32) {
             float4* o = reinterpret_cast<float4*>(static_cast<float*>(obase) + oofs);
@@ -254,39 +280,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int64_t rr = valid ? r : p.g.L - 1;
       int64_t clo, chi, nlo, nhi;
-      clean_interval(p.g, t.stream, rr, clo, chi);
-      noisy_interval(p.g, t.stream, rr, nlo, nhi);
+      clean_interval(p.g, g.stream, rr, clo, chi);
+      noisy_interval(p.g, g.stream, rr, nlo, nhi);
+      const float sl2 = p.scale_log2;
       float m_ref = -INFINITY, l = 0.f;
-      for (int j = 0; j < t.n; ++j, ++sc) {
-        const bool cs = j < t.nc;
-        const int64_t key0 = tile_key0(t, j);
-        const bool full = cs ? tile_full(key0, BN, t.q.c_all_lo, t.q.c_all_hi, p.g.L)
-                             : tile_full(key0, BN, t.q.n_all_lo, t.q.n_all_hi, p.g.L);
-        const int sb = sc & 1;
-        ok = mbar_wait(BAR(B_SFULL + sb), (sc >> 1) & 1, wd, 9);
+      for (int j = 0; j < g.n; ++j, ++sc) {
+        const bool cs = j < g.nc;
+        const int64_t key0 = tile_key0(g, j);
+        const bool full = cs ? tile_full(key0, BN, g.q.c_all_lo, g.q.c_all_hi, p.g.L)
+                             : tile_full(key0, BN, g.q.n_all_lo, g.q.n_all_hi, p.g.L);
+        ok = mbar_wait(BAR(B_SF, t), sc & 1, wd, 9);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        float s[BN];
+        const int lo = full ? -1 : (int)imax64(imin64((cs ? clo : nlo) - key0, BN + 1), -1);
+        const int hi = full ? BN + 1 : (int)imax64(imin64((cs ? chi : nhi) - key0, BN + 1), -1);
+        // pass 1: masked row max (64 columns at a time)
+        float mx = -INFINITY;
 #pragma unroll
-        for (int c4 = 0; c4 < BN / 32; ++c4) {
-          uint32_t u[32];
-          tmem_ld32(tS + sb * BN + c4 * 32, u);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t a[32], b[32];
+          tmem_ld32x2(tS + 64 * h2, tS + 64 * h2 + 32, a, b);
+          if (full) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) s[c4 * 32 + c] = __uint_as_float(u[c]);
+            for (int c = 0; c < 32; ++c) mx = fmaxf(mx, fmaxf(__uint_as_float(a[c]), __uint_as_float(b[c])));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int ca = 64 * h2 + c, cb = ca + 32;
+              if (ca >= lo && ca < hi) mx = fmaxf(mx, __uint_as_float(a[c]));
+              if (cb >= lo && cb < hi) mx = fmaxf(mx, __uint_as_float(b[c]));
+            }
+          }
         }
-        tc_fence_before();
-        mbar_arrive(BAR(B_SEMPTY + sb));
-        if (!full) {
-          const int64_t lo = (cs ? clo : nlo) - key0, hi = (cs ? chi : nhi) - key0;
-#pragma unroll
-          for (int c = 0; c < BN; ++c)
-            if (c < lo || c >= hi) s[c] = -INFINITY;
-        }
-        float mx = s[0];
-#pragma unroll
-        for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
-        const float mx2 = mx * p.scale_log2;
+        const float mx2 = mx * sl2;
         bool rescale = false;
         float alpha = 1.f, m_use = m_ref;
         if (m_ref == -INFINITY) {
@@ -296,76 +323,95 @@ __global__ void __launch_bounds__(kThreads, 1)
           alpha = ex2_approx(m_ref - m_use);
           rescale = true;
         }
-        const float msub = (m_use == -INFINITY) ? 0.f : m_use;
-        uint32_t pk[BN / 2];
+        const float nm = (m_use == -INFINITY) ? 0.f : -m_use;
+        // pass 2: P = exp2(s c - m), row sum, P as packed bf16 over the columns
+        // already read (the PV MMA's A operand)
         float rs = 0.f;
 #pragma unroll
-        for (int c = 0; c < BN; c += 2) {
-          const float p0 = ex2_approx(fmaf(s[c], p.scale_log2, -msub));
-          const float p1 = ex2_approx(fmaf(s[c + 1], p.scale_log2, -msub));
-          rs += p0 + p1;
-          pk[c / 2] = pack_bf16x2(p0, p1);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t a[32], b[32];
+          tmem_ld32x2(tS + 64 * h2, tS + 64 * h2 + 32, a, b);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const uint32_t (&x)[32] = q ? b : a;
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const int ca = 64 * h2 + 32 * q + c;
+              float p0 = ex2_approx(fmaf(__uint_as_float(x[c]), sl2, nm));
+              float p1 = ex2_approx(fmaf(__uint_as_float(x[c + 1]), sl2, nm));
+              if (!full) {
+                p0 = (ca >= lo && ca < hi) ? p0 : 0.f;
+                p1 = (ca + 1 >= lo && ca + 1 < hi) ? p1 : 0.f;
+              }
+              rs += p0 + p1;
+              pk[c / 2] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(tS + 32 * h2 + 16 * q, pk);
+          }
         }
         l = l * alpha + rs;
         m_ref = m_use;
         if (j > 0) {
-          ok = mbar_wait(BAR(B_PVDONE), (pc - 1) & 1, wd, 10);
+          // PV(j-1) must be complete before O is rescaled
+          ok = mbar_wait(BAR(B_PVD, t), (pc - 1) & 1, wd, 10);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after();
           if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
             for (int c4 = 0; c4 < HD / 32; ++c4) {
-              uint32_t u[32];
-              tmem_ld32(tO + c4 * 32, u);
+              uint32_t o[32];
+              tmem_ld32(tO + c4 * 32, o);
 #pragma unroll
-              for (int c = 0; c < 32; ++c) u[c] = __float_as_uint(__uint_as_float(u[c]) * alpha);
-              tmem_st32(tO + c4 * 32, u);
+              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+              tmem_st32(tO + c4 * 32, o);
             }
           }
         }
-        // P row -> swizzled K-major tile (two 64-key panels)
-#pragma unroll
-        for (int ch = 0; ch < BN / 8; ++ch) {
-          const int pn = ch >> 3, cw = ch & 7;
-          const uint32_t addr = sP + pn * kPanelBytes + row * 128 + ((cw ^ (row & 7)) << 4);
-          st_shared_v4(addr, pk[ch * 4 + 0], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-        }
-        fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(BAR(B_PFULL));
+        mbar_arrive(BAR(B_PF, t));
         ++pc;
       }
       if (!ok) break;
-      ok = mbar_wait(BAR(B_PVDONE), (pc - 1) & 1, wd, 11);
+      ok = mbar_wait(BAR(B_PVD, t), (pc - 1) & 1, wd, 11);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-      for (int c4 = 0; c4 < HD / 32; ++c4) {
-        uint32_t u[32];
-        tmem_ld32(tO + c4 * 32, u);
+      for (int c4 = 0; c4 < HD / 64; ++c4) {
+        uint32_t a[32], b[32];
+        tmem_ld32x2(tO + c4 * 64, tO + c4 * 64 + 32, a, b);
         if (valid) {
           if (p.o_f32) {
-            float4* o = reinterpret_cast<float4*>(static_cast<float*>(obase) + oofs + c4 * 32);
+            float4* o = reinterpret_cast<float4*>(static_cast<float*>(obase) + oofs + c4 * 64);
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              o[c] = make_float4(__uint_as_float(u[4 * c]) * inv, __uint_as_float(u[4 * c + 1]) * inv,
-                                 __uint_as_float(u[4 * c + 2]) * inv, __uint_as_float(u[4 * c + 3]) * inv);
+            for (int c = 0; c < 8; ++c) {
+              o[c] = make_float4(__uint_as_float(a[4 * c]) * inv, __uint_as_float(a[4 * c + 1]) * inv,
+                                 __uint_as_float(a[4 * c + 2]) * inv, __uint_as_float(a[4 * c + 3]) * inv);
+              o[8 + c] = make_float4(__uint_as_float(b[4 * c]) * inv, __uint_as_float(b[4 * c + 1]) * inv,
+                                     __uint_as_float(b[4 * c + 2]) * inv, __uint_as_float(b[4 * c + 3]) * inv);
+            }
           } else {
-            uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(obase) + oofs + c4 * 32);
+            uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(obase) + oofs + c4 * 64);
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-              o[c] = make_uint4(pack_bf16x2(__uint_as_float(u[8 * c + 0]) * inv, __uint_as_float(u[8 * c + 1]) * inv),
-                                pack_bf16x2(__uint_as_float(u[8 * c + 2]) * inv, __uint_as_float(u[8 * c + 3]) * inv),
-                                pack_bf16x2(__uint_as_float(u[8 * c + 4]) * inv, __uint_as_float(u[8 * c + 5]) * inv),
-                                pack_bf16x2(__uint_as_float(u[8 * c + 6]) * inv, __uint_as_float(u[8 * c + 7]) * inv));
+            for (int c = 0; c < 4; ++c) {
+              o[c] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * c + 0]) * inv, __uint_as_float(a[8 * c + 1]) * inv),
+                                pack_bf16x2(__uint_as_float(a[8 * c + 2]) * inv, __uint_as_float(a[8 * c + 3]) * inv),
+                                pack_bf16x2(__uint_as_float(a[8 * c + 4]) * inv, __uint_as_float(a[8 * c + 5]) * inv),
+                                pack_bf16x2(__uint_as_float(a[8 * c + 6]) * inv, __uint_as_float(a[8 * c + 7]) * inv));
+              o[4 + c] =
+                  make_uint4(pack_bf16x2(__uint_as_float(b[8 * c + 0]) * inv, __uint_as_float(b[8 * c + 1]) * inv),
+                             pack_bf16x2(__uint_as_float(b[8 * c + 2]) * inv, __uint_as_float(b[8 * c + 3]) * inv),
+                             pack_bf16x2(__uint_as_float(b[8 * c + 4]) * inv, __uint_as_float(b[8 * c + 5]) * inv),
+                             pack_bf16x2(__uint_as_float(b[8 * c + 6]) * inv, __uint_as_float(b[8 * c + 7]) * inv));
+            }
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(BAR(B_OEMPTY));
+      mbar_arrive(BAR(B_OE, t));
       if (valid) lse_out[r] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
@@ -382,7 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, int d, int num_sms, cudaStream_t stream,
                        int* launches) {
-  const int64_t grid64 = p.n_items < num_sms ? p.n_items : num_sms;
+  const int64_t n_pairs = p.n_items / 2;
+  const int64_t grid64 = n_pairs < num_sms ? n_pairs : num_sms;
   const int grid = (int)(grid64 > 0 ? grid64 : 1);
   cudaError_t e;
   if (d == 128) {
