@@ -17,21 +17,27 @@
 //              query row for dQ, a key row for dK/dV); the two warpgroups
 //              split the 64 columns of each step, 32 each, so every SM
 //              sub-partition runs two of these warps.  Tiles that every row
-//              sees completely take a branch-free path.
+//              sees completely take a branch-free path.  Each warpgroup
+//              writes its bf16 results (dS, or P^T and dS^T) back into the
+//              TMEM columns it has just read, where the next MMA takes them
+//              as its A operand; the MMA warp issues the MMA that overwrites
+//              those columns only after the one that reads them (the tensor
+//              pipe runs in issue order).
 //
 // dQ pass (bdlm_bwd_dq_tc): item = (128-row query tile, head, stream), in the
-//   forward's longest-first order.  Q and dO stay in shared memory; 64-key K/V
-//   tiles stream through a 3-stage ring.  MMA: S = Q K^T and dP = dO V^T into
-//   one of two TMEM buffer pairs, then dQ += dS K (K read as an MN-major
-//   operand from the same tile).  dS goes to a swizzled bf16 shared tile.
+//   forward's longest-first order.  Q and dO of the item are copied into TMEM
+//   by the elementwise threads (one row each) and stay there; 64-key K/V
+//   tiles stream through a 4-stage TMA ring.  MMA: S = Q K^T and dP = dO V^T
+//   (A operands in TMEM) into one of two TMEM buffer pairs, then
+//   dQ += dS K (dS in TMEM, K read as an MN-major operand of the same tile).
 //
 // dK/dV pass (bdlm_bwd_dkv_tc): item = (key stream, KV head, 128-key tile):
 //   clean tiles first (read by every later row), then corrupted tiles.  K and
 //   V stay in shared memory; 64-row Q/dO tiles of every query head of the GQA
-//   group and both streams that see the keys stream through a 2-stage ring.
+//   group and both streams that see the keys stream through a 4-stage ring.
 //   MMA: S^T = K Q^T, dP^T = V dO^T, then dV += P^T dO and dK += dS^T Q with
-//   Q/dO read as MN-major operands.  dK and dV accumulate in TMEM across the
-//   whole group and are written once.
+//   P^T and dS^T in TMEM and Q/dO read as MN-major operands.  dK and dV
+//   accumulate in TMEM across the whole group and are written once.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -85,37 +91,26 @@ __device__ __forceinline__ void store_row32(void* base, int64_t off, const uint3
   }
 }
 
-// 32 bf16 pairs of one row half -> 4 swizzled 16-byte chunks of a 128-byte row
-__device__ __forceinline__ void store_half_row(uint32_t tile, int row, int half, const uint32_t (&pk)[16]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int ch = half * 4 + i;
-    st_shared_v4(tile + row * 128 + ((ch ^ (row & 7)) << 4), pk[4 * i + 0], pk[4 * i + 1], pk[4 * i + 2],
-                 pk[4 * i + 3]);
-  }
-}
+// TMEM column of the packed bf16 A operand for 16-row (or 16-key) K-step kk
+// of a 64-wide step whose two 32-wide halves were written, 16 packed columns
+// each, at the start of the 32-column region the half had read.
+__device__ __forceinline__ uint32_t packed_col(int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); }
 
 // ====================================================================== dQ
 constexpr int QBM = 128;  // query rows per item
 constexpr int QBN = 64;   // keys per step
-constexpr int QNS = 3;    // K/V stages
+constexpr int QNS = 4;    // K/V stages
 
-enum { DQ_QFULL = 0, DQ_QEMPTY = 1, DQ_KVFULL = 2, DQ_KVEMPTY = 5, DQ_SFULL = 8, DQ_SEMPTY = 10, DQ_DSFULL = 12,
-       DQ_DSEMPTY = 14, DQ_DONE = 16, DQ_OEMPTY = 17, DQ_NBAR = 18 };
+enum { DQ_QL = 0, DQ_KVFULL = 1, DQ_KVEMPTY = 5, DQ_SFULL = 9, DQ_DSFULL = 11, DQ_DONE = 13, DQ_OEMPTY = 14,
+       DQ_NBAR = 15 };
 
 template <int HD>
 struct DqLayout {
-  static constexpr int kQTile = QBM * HD * 2;    // 128 rows
-  static constexpr int kKTile = QBN * HD * 2;    // 64 rows
-  static constexpr int kQPanel = QBM * 128;      // 16 KB
-  static constexpr int kKPanel = QBN * 128;      // 8 KB
-  static constexpr int kDsTile = QBM * QBN * 2;  // 16 KB
-  static constexpr int kQ = 0;
-  static constexpr int kdO = kQ + kQTile;
-  static constexpr int kK = kdO + kQTile;
+  static constexpr int kKTile = QBN * HD * 2;  // 64 rows
+  static constexpr int kKPanel = QBN * 128;    // 8 KB
+  static constexpr int kK = 0;
   static constexpr int kV = kK + QNS * kKTile;
-  static constexpr int kDs = kV + QNS * kKTile;
-  static constexpr int kBar = kDs + 2 * kDsTile;
+  static constexpr int kBar = kV + QNS * kKTile;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
 };
@@ -141,11 +136,31 @@ __device__ __forceinline__ DqGeo dq_geo(const BwdParams& p, int64_t idx) {
   return t;
 }
 
+// One row's half of a [L, H, HD] bf16 tensor row (HD/2 elements = HD/4
+// packed columns) -> TMEM, packed two bf16 per 32-bit column in memory order.
+template <int HD>
+__device__ __forceinline__ void row_half_to_tmem(uint32_t taddr, const __nv_bfloat16* src, bool valid) {
+  constexpr int NC = HD / 4;  // packed columns per half: 32 (HD=128) or 16 (HD=64)
+  uint32_t u[NC];
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < NC / 4; ++i) {
+    const uint4 v = valid ? s4[i] : make_uint4(0u, 0u, 0u, 0u);
+    u[4 * i + 0] = v.x;
+    u[4 * i + 1] = v.y;
+    u[4 * i + 2] = v.z;
+    u[4 * i + 3] = v.w;
+  }
+  if constexpr (NC == 32) {
+    tmem_st32(taddr, u);
+  } else {
+    tmem_st16(taddr, u);
+  }
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
-    bdlm_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tQc, const __grid_constant__ CUtensorMap tQn,
-                          const __grid_constant__ CUtensorMap tdOc, const __grid_constant__ CUtensorMap tdOn,
-                          const __grid_constant__ CUtensorMap tKc, const __grid_constant__ CUtensorMap tKn,
+    bdlm_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tKc, const __grid_constant__ CUtensorMap tKn,
                           const __grid_constant__ CUtensorMap tVc, const __grid_constant__ CUtensorMap tVn,
                           const BwdParams p, const int64_t n_items, uint32_t* status, const uint64_t limit_ns) {
   using LY = DqLayout<HD>;
@@ -153,8 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw_u32);
-  const uint32_t sQ = base + LY::kQ, sdO = base + LY::kdO, sK = base + LY::kK, sV = base + LY::kV,
-                 sDs = base + LY::kDs;
+  const uint32_t sK = base + LY::kK, sV = base + LY::kV;
   const uint32_t bars = base + LY::kBar;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + LY::kBar + 8 * DQ_NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + LY::kBar + 8 * DQ_NBAR + 4);
@@ -162,17 +176,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Role R = role();
 
   if (threadIdx.x == 0) {
-    mbar_init(BAR(DQ_QFULL), 1);
-    mbar_init(BAR(DQ_QEMPTY), 1);
+    mbar_init(BAR(DQ_QL), kEwThreads);
     for (int s = 0; s < QNS; ++s) {
       mbar_init(BAR(DQ_KVFULL + s), 1);
       mbar_init(BAR(DQ_KVEMPTY + s), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(BAR(DQ_SFULL + s), 1);
-      mbar_init(BAR(DQ_SEMPTY + s), kEwThreads);
       mbar_init(BAR(DQ_DSFULL + s), kEwThreads);
-      mbar_init(BAR(DQ_DSEMPTY + s), 1);
     }
     mbar_init(BAR(DQ_DONE), 1);
     mbar_init(BAR(DQ_OEMPTY), kEwThreads);
@@ -189,25 +200,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const Watchdog wd{status, limit_ns, abort_flag};
   const int grid = gridDim.x, cta = blockIdx.x;
-  // TMEM columns: S[2] at 0/64, dP[2] at 128/192, dQ at 256
+  // TMEM columns: S[2] at 0/64 (dS over them), dP[2] at 128/192, dQ at 256,
+  // Q at 384, dO at 384 + HD/2 (packed bf16)
+  constexpr uint32_t kColQ = 384, kColdO = 384 + HD / 2;
   if (R.warp == 0) {
     if (R.lane == 0) {
-      uint32_t itn = 0, kvc = 0;
+      uint32_t kvc = 0;
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
         const int64_t idx = snake_item(rnd, cta, grid);
         if (idx >= n_items) break;
         const DqGeo t = dq_geo(p, idx);
-        if (t.n == 0) continue;
-        if (itn > 0 && !mbar_wait(BAR(DQ_QEMPTY), (itn - 1) & 1, wd, 21)) { ok = false; break; }
-        mbar_arrive_expect_tx(BAR(DQ_QFULL), 2 * LY::kQTile);
-        const CUtensorMap* mq = t.stream ? &tQn : &tQc;
-        const CUtensorMap* mo = t.stream ? &tdOn : &tdOc;
-#pragma unroll
-        for (int pn = 0; pn < HD / 64; ++pn) {
-          tma_load_3d(sQ + pn * LY::kQPanel, mq, BAR(DQ_QFULL), pn * 64, t.head, (int)t.r0);
-          tma_load_3d(sdO + pn * LY::kQPanel, mo, BAR(DQ_QFULL), pn * 64, t.head, (int)t.r0);
-        }
         for (int j = 0; j < t.n; ++j, ++kvc) {
           const int st = kvc % QNS;
           if (kvc >= QNS && !mbar_wait(BAR(DQ_KVEMPTY + st), ((kvc / QNS) - 1) & 1, wd, 22)) { ok = false; break; }
@@ -222,7 +225,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(sV + st * LY::kKTile + pn * LY::kKPanel, mv, BAR(DQ_KVFULL + st), pn * 64, t.kvh, key0);
           }
         }
-        ++itn;
       }
     }
   } else if (R.warp == 1) {
@@ -236,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (idx >= n_items) break;
         const DqGeo t = dq_geo(p, idx);
         if (t.n == 0) continue;
-        if (!mbar_wait(BAR(DQ_QFULL), itn & 1, wd, 23)) { ok = false; break; }
+        if (!mbar_wait(BAR(DQ_QL), itn & 1, wd, 23)) { ok = false; break; }  // Q, dO in TMEM
         const uint32_t kv_base = kvc;
         auto do_dq = [&](int jj) -> bool {
           const uint32_t kv = kv_base + jj;
@@ -247,12 +249,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < QBN / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(sDs + db * LY::kDsTile + kk * 32, 16, 1024);
             const uint64_t bd = sdesc_sw128(sK + st * LY::kKTile + kk * 2048, LY::kKPanel, 1024);
-            tc_mma_ss(tmem + 256, ad, bd, kIdQ, (jj > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_ts(tmem + 256, tmem + db * QBN + packed_col(kk), bd, kIdQ, (jj > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(BAR(DQ_KVEMPTY + st));
-          tc_commit(BAR(DQ_DSEMPTY + db));
           ++dc;
           return true;
         };
@@ -260,19 +260,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int st = kvc % QNS;
           const int sb = sc & 1;
           if (!mbar_wait(BAR(DQ_KVFULL + st), (kvc / QNS) & 1, wd, 26)) { ok = false; break; }
-          if (sc >= 2 && !mbar_wait(BAR(DQ_SEMPTY + sb), ((sc >> 1) - 1) & 1, wd, 27)) { ok = false; break; }
           tc_fence_after();
+          // buffer sb was last read by dQ(j-2), issued before this point
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint32_t qo = (kk >> 2) * LY::kQPanel + (kk & 3) * 32;
             const uint32_t ko = st * LY::kKTile + (kk >> 2) * LY::kKPanel + (kk & 3) * 32;
-            tc_mma_ss(tmem + sb * QBN, sdesc_sw128(sQ + qo, 16, 1024), sdesc_sw128(sK + ko, 16, 1024), kIdS,
+            tc_mma_ts(tmem + sb * QBN, tmem + kColQ + kk * 8, sdesc_sw128(sK + ko, 16, 1024), kIdS,
                       kk > 0 ? 1u : 0u);
-            tc_mma_ss(tmem + 128 + sb * QBN, sdesc_sw128(sdO + qo, 16, 1024), sdesc_sw128(sV + ko, 16, 1024),
-                      kIdS, kk > 0 ? 1u : 0u);
+            tc_mma_ts(tmem + 128 + sb * QBN, tmem + kColdO + kk * 8, sdesc_sw128(sV + ko, 16, 1024), kIdS,
+                      kk > 0 ? 1u : 0u);
           }
           tc_commit(BAR(DQ_SFULL + sb));
-          if (j == t.n - 1) tc_commit(BAR(DQ_QEMPTY));
           if (j >= 1 && !do_dq(j - 1)) { ok = false; break; }
         }
         if (!ok) break;
@@ -284,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // elementwise: thread = query row, warpgroup `half` = key columns [32 half, 32 half + 32)
     const int row = R.row, half = R.half;
-    uint32_t itn = 0, sc = 0, dc = 0;
+    uint32_t itn = 0, sc = 0;
     bool ok = true;
     for (int64_t rnd = 0; ok; ++rnd) {
       const int64_t idx = snake_item(rnd, cta, grid);
@@ -308,6 +306,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
+      // Q and dO rows of this item into TMEM (the previous item's MMAs that
+      // read them are complete: its epilogue waited for DQ_DONE)
+      {
+        const int64_t rs = valid ? r : 0;
+        const __nv_bfloat16* qsrc = static_cast<const __nv_bfloat16*>(t.stream ? p.Qn : p.Qc) +
+                                    (rs * p.g.Hq + t.head) * HD + half * (HD / 2);
+        const __nv_bfloat16* osrc = static_cast<const __nv_bfloat16*>(t.stream ? p.dOn : p.dOc) +
+                                    (rs * p.g.Hq + t.head) * HD + half * (HD / 2);
+        row_half_to_tmem<HD>(tmem + R.tl + kColQ + half * (HD / 4), qsrc, valid);
+        row_half_to_tmem<HD>(tmem + R.tl + kColdO + half * (HD / 4), osrc, valid);
+        tc_fence_before();
+        mbar_arrive(BAR(DQ_QL));
+      }
       const int64_t rr = valid ? r : p.g.L - 1;
       int64_t clo, chi, nlo, nhi;
       clean_interval(p.g, t.stream, rr, clo, chi);
@@ -326,9 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         uint32_t us[32], ud[32];
-        tmem_ld32x2(tmem + R.tl + sb * QBN + half * 32, tmem + R.tl + 128 + sb * QBN + half * 32, us, ud);
-        tc_fence_before();
-        mbar_arrive(BAR(DQ_SEMPTY + sb));
+        const uint32_t tS = tmem + R.tl + sb * QBN + half * 32;
+        tmem_ld32x2(tS, tmem + R.tl + 128 + sb * QBN + half * 32, us, ud);
         uint32_t pk[16];
         if (full) {
 #pragma unroll
@@ -350,17 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[c / 2] = pack_bf16x2(d0, d1);
           }
         }
-        const int db = dc & 1;
-        if (dc >= 2) {
-          ok = mbar_wait(BAR(DQ_DSEMPTY + db), ((dc >> 1) - 1) & 1, wd, 29);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-        }
-        store_half_row(sDs + db * LY::kDsTile, row, half, pk);
-        fence_proxy_async_smem();
+        // dS (bf16) over the first 16 columns of the S columns this half read
+        tmem_st16(tS, pk);
         tc_fence_before();
-        mbar_arrive(BAR(DQ_DSFULL + db));
-        ++dc;
+        mbar_arrive(BAR(DQ_DSFULL + sb));
       }
       if (!ok) break;
       ok = mbar_wait(BAR(DQ_DONE), itn & 1, wd, 30);
@@ -389,25 +392,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 // =================================================================== dK / dV
 constexpr int KBM = 128;  // keys per item
 constexpr int KBN = 64;   // query rows per step
-constexpr int KNS = 2;    // Q/dO stages
+constexpr int KNS = 4;    // Q/dO stages
 
-enum { KV_KFULL = 0, KV_KEMPTY = 1, KV_QFULL = 2, KV_QEMPTY = 4, KV_SFULL = 6, KV_SEMPTY = 8, KV_PFULL = 10,
-       KV_PEMPTY = 12, KV_ACCDONE = 14, KV_ACCEMPTY = 15, KV_NBAR = 16 };
+enum { KV_KFULL = 0, KV_KEMPTY = 1, KV_QFULL = 2, KV_QEMPTY = 6, KV_SFULL = 10, KV_PFULL = 12, KV_ACCDONE = 14,
+       KV_ACCEMPTY = 15, KV_NBAR = 16 };
 
 template <int HD>
 struct DkvLayout {
-  static constexpr int kKTile = KBM * HD * 2;    // 128 key rows
-  static constexpr int kQTile = KBN * HD * 2;    // 64 query rows
-  static constexpr int kKPanel = KBM * 128;      // 16 KB
-  static constexpr int kQPanel = KBN * 128;      // 8 KB
-  static constexpr int kPTile = KBM * KBN * 2;   // 16 KB
+  static constexpr int kKTile = KBM * HD * 2;  // 128 key rows
+  static constexpr int kQTile = KBN * HD * 2;  // 64 query rows
+  static constexpr int kKPanel = KBM * 128;    // 16 KB
+  static constexpr int kQPanel = KBN * 128;    // 8 KB
   static constexpr int kK = 0;
   static constexpr int kV = kK + kKTile;
   static constexpr int kQ = kV + kKTile;
   static constexpr int kdO = kQ + KNS * kQTile;
-  static constexpr int kPt = kdO + KNS * kQTile;
-  static constexpr int kdSt = kPt + 2 * kPTile;
-  static constexpr int kStat = kdSt + 2 * kPTile;  // per stage: LSE[64] then D[64], fp32
+  static constexpr int kStat = kdO + KNS * kQTile;  // per stage: LSE[64] then D[64], fp32
   static constexpr int kBar = kStat + KNS * 2 * KBN * 4;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw_u32);
   const uint32_t sK = base + LY::kK, sV = base + LY::kV, sQ = base + LY::kQ, sdO = base + LY::kdO,
-                 sPt = base + LY::kPt, sdSt = base + LY::kdSt, sStat = base + LY::kStat;
+                 sStat = base + LY::kStat;
   const float* stat_ptr = reinterpret_cast<const float*>(base_ptr + LY::kStat);
   const uint32_t bars = base + LY::kBar;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + LY::kBar + 8 * KV_NBAR);
@@ -507,9 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(BAR(KV_SFULL + s), 1);
-      mbar_init(BAR(KV_SEMPTY + s), kEwThreads);
       mbar_init(BAR(KV_PFULL + s), kEwThreads);
-      mbar_init(BAR(KV_PEMPTY + s), 1);
     }
     mbar_init(BAR(KV_ACCDONE), 1);
     mbar_init(BAR(KV_ACCEMPTY), kEwThreads);
@@ -526,7 +524,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const Watchdog wd{status, limit_ns, abort_flag};
   const int grid = gridDim.x, cta = blockIdx.x;
-  // TMEM columns: dK at 0, dV at 128, S^T[2] at 256/320, dP^T[2] at 384/448
+  // TMEM columns: dK at 0, dV at 128, S^T[2] at 256/320 (P^T over them),
+  // dP^T[2] at 384/448 (dS^T over them)
   if (R.warp == 0) {
     // ---------------------------------------------------------- producer (whole warp)
     uint32_t itn = 0, qc = 0;
@@ -611,11 +610,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t acc = (kk > 0 || k4 > 0) ? 1u : 0u;
             const uint64_t bo = sdesc_sw128(sdO + st * LY::kQTile + k4 * 2048, LY::kQPanel, 1024);
             const uint64_t bq = sdesc_sw128(sQ + st * LY::kQTile + k4 * 2048, LY::kQPanel, 1024);
-            tc_mma_ss(tmem + 128, sdesc_sw128(sPt + pb * LY::kPTile + k4 * 32, 16, 1024), bo, kIdA, acc);
-            tc_mma_ss(tmem + 0, sdesc_sw128(sdSt + pb * LY::kPTile + k4 * 32, 16, 1024), bq, kIdA, acc);
+            tc_mma_ts(tmem + 128, tmem + 256 + pb * KBN + packed_col(k4), bo, kIdA, acc);
+            tc_mma_ts(tmem + 0, tmem + 384 + pb * KBN + packed_col(k4), bq, kIdA, acc);
           }
           tc_commit(BAR(KV_QEMPTY + st));
-          tc_commit(BAR(KV_PEMPTY + pb));
           ++pc;
           return true;
         };
@@ -623,8 +621,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int st = qc % KNS;
           const int sb = sc & 1;
           if (!mbar_wait(BAR(KV_QFULL + st), (qc / KNS) & 1, wd, 46)) { ok = false; break; }
-          if (sc >= 2 && !mbar_wait(BAR(KV_SEMPTY + sb), ((sc >> 1) - 1) & 1, wd, 47)) { ok = false; break; }
           tc_fence_after();
+          // buffer sb was last read by the dV/dK MMAs of step k-2, issued before this point
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
             const uint32_t ko = (kk >> 2) * LY::kKPanel + (kk & 3) * 32;
@@ -647,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------------------------------------------------- elementwise (thread = key row)
     const int row = R.row, half = R.half;
-    uint32_t itn = 0, qc = 0, sc = 0, pc = 0;
+    uint32_t itn = 0, qc = 0, sc = 0;
     bool ok = true;
     const float sl2 = p.scale_log2;
     for (int64_t rnd = 0; ok; ++rnd) {
@@ -688,66 +686,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         uint32_t us[32], ud[32];
-        tmem_ld32x2(tmem + R.tl + 256 + sb * KBN + half * 32, tmem + R.tl + 384 + sb * KBN + half * 32, us, ud);
-        tc_fence_before();
-        mbar_arrive(BAR(KV_SEMPTY + sb));
+        const uint32_t tS = tmem + R.tl + 256 + sb * KBN + half * 32;
+        const uint32_t tD = tmem + R.tl + 384 + sb * KBN + half * 32;
+        tmem_ld32x2(tS, tD, us, ud);
         const float* stl = stat_ptr + st * 2 * KBN + half * 32;  // LSE of this half's 32 rows; D at +KBN
         const bool full = s == 0 ? (q0 >= alo0 && q0 + KBN <= ahi0) : (q0 >= alo1 && q0 + KBN <= ahi1);
+        const int64_t base_row = q0 + half * 32;
+        const int lo = full ? -1 : (int)imax64(imin64((s == 0 ? klo0 : klo1) - base_row, 33), -1);
+        const int hi = full ? 33 : (int)imax64(imin64((s == 0 ? khi0 : khi1) - base_row, 33), -1);
         uint32_t pp[16], dd[16];
-        if (full) {
 #pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(stl + 4 * c4);
-            const float4 d4 = *reinterpret_cast<const float4*>(stl + KBN + 4 * c4);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pv[4], sv[4];
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(stl + 4 * c4);
+          const float4 d4 = *reinterpret_cast<const float4*>(stl + KBN + 4 * c4);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pv[4], sv[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = 4 * c4 + e;
-              pv[e] = ex2_approx(fmaf(__uint_as_float(us[c]), sl2, -lv[e] * kLog2e));
-              sv[e] = pv[e] * (__uint_as_float(ud[c]) - dv[e]);
-            }
-            pp[2 * c4] = pack_bf16x2(pv[0], pv[1]);
-            pp[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
-            dd[2 * c4] = pack_bf16x2(sv[0], sv[1]);
-            dd[2 * c4 + 1] = pack_bf16x2(sv[2], sv[3]);
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * c4 + e;
+            float pe = ex2_approx(fmaf(__uint_as_float(us[c]), sl2, -lv[e] * kLog2e));
+            if (!full) pe = (c >= lo && c < hi) ? pe : 0.f;
+            pv[e] = pe;
+            sv[e] = pe * (__uint_as_float(ud[c]) - dv[e]);
           }
-        } else {
-          const int64_t base_row = q0 + half * 32;
-          const int lo = (int)imax64(imin64((s == 0 ? klo0 : klo1) - base_row, 33), -1);
-          const int hi = (int)imax64(imin64((s == 0 ? khi0 : khi1) - base_row, 33), -1);
-#pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(stl + 4 * c4);
-            const float4 d4 = *reinterpret_cast<const float4*>(stl + KBN + 4 * c4);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pv[4], sv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = 4 * c4 + e;
-              float pe = ex2_approx(fmaf(__uint_as_float(us[c]), sl2, -lv[e] * kLog2e));
-              pe = (c >= lo && c < hi) ? pe : 0.f;
-              pv[e] = pe;
-              sv[e] = pe * (__uint_as_float(ud[c]) - dv[e]);
-            }
-            pp[2 * c4] = pack_bf16x2(pv[0], pv[1]);
-            pp[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
-            dd[2 * c4] = pack_bf16x2(sv[0], sv[1]);
-            dd[2 * c4 + 1] = pack_bf16x2(sv[2], sv[3]);
-          }
+          pp[2 * c4] = pack_bf16x2(pv[0], pv[1]);
+          pp[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
+          dd[2 * c4] = pack_bf16x2(sv[0], sv[1]);
+          dd[2 * c4 + 1] = pack_bf16x2(sv[2], sv[3]);
         }
-        const int pb = pc & 1;
-        if (pc >= 2) {
-          ok = mbar_wait(BAR(KV_PEMPTY + pb), ((pc >> 1) - 1) & 1, wd, 50);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-        }
-        store_half_row(sPt + pb * LY::kPTile, row, half, pp);
-        store_half_row(sdSt + pb * LY::kPTile, row, half, dd);
-        fence_proxy_async_smem();
+        // P^T and dS^T (bf16) over the first 16 columns of what this half read
+        tmem_st16(tS, pp);
+        tmem_st16(tD, dd);
         tc_fence_before();
-        mbar_arrive(BAR(KV_PFULL + pb));
-        ++pc;
+        mbar_arrive(BAR(KV_PFULL + sb));
       }
       if (!ok) break;
       ok = mbar_wait(BAR(KV_ACCDONE), itn & 1, wd, 51);
@@ -794,13 +765,13 @@ cudaError_t launch_bwd_dq_tc(const BwdMaps& m, const BwdParams& p, int num_sms, 
                              DqLayout<128>::kAlloc);
     if (e != cudaSuccess) return e;
     bdlm_bwd_dq_tc_kernel<128><<<grid, kThreads, DqLayout<128>::kAlloc, stream>>>(
-        m.Qc128, m.Qn128, m.dOc128, m.dOn128, m.Kc64, m.Kn64, m.Vc64, m.Vn64, p, n, status, limit_ns);
+        m.Kc64, m.Kn64, m.Vc64, m.Vn64, p, n, status, limit_ns);
   } else {
     e = cudaFuncSetAttribute(bdlm_bwd_dq_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DqLayout<64>::kAlloc);
     if (e != cudaSuccess) return e;
     bdlm_bwd_dq_tc_kernel<64><<<grid, kThreads, DqLayout<64>::kAlloc, stream>>>(
-        m.Qc128, m.Qn128, m.dOc128, m.dOn128, m.Kc64, m.Kn64, m.Vc64, m.Vn64, p, n, status, limit_ns);
+        m.Kc64, m.Kn64, m.Vc64, m.Vn64, p, n, status, limit_ns);
   }
   if (launches) ++*launches;
   return cudaGetLastError();
