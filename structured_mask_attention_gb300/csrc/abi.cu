@@ -194,8 +194,10 @@ bdlm_status get_encoder(EncodeTiledFn& fn) {
 
 // [L, H, d] bf16 tensor as a 3-D TMA map (d innermost), box 64 x 1 x box_rows,
 // 128-byte swizzle; out-of-range rows read as zero.
+// box_rows must equal the row count of the shared-memory slot the kernel
+// loads the box into (the kernel's expected transaction bytes assume it).
 bdlm_status encode_lhd(EncodeTiledFn fn, CUtensorMap* m, const void* ptr, int64_t L, int H, int d,
-                       int box_rows = 128) {
+                       int box_rows) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)L};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
   cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
@@ -238,12 +240,12 @@ bdlm_status fwd_common(const void* Qc, const void* Kc, const void* Vc, const voi
   EncodeTiledFn enc;
   BDLM_CHECK(get_encoder(enc));
   FwdMaps maps;
-  BDLM_CHECK(encode_lhd(enc, &maps.Qc, Qc, L, Hq, d));
-  BDLM_CHECK(encode_lhd(enc, &maps.Qn, Qn, L, Hq, d));
-  BDLM_CHECK(encode_lhd(enc, &maps.Kc, Kc, L, Hkv, d));
-  BDLM_CHECK(encode_lhd(enc, &maps.Kn, Kn, L, Hkv, d));
-  BDLM_CHECK(encode_lhd(enc, &maps.Vc, Vc, L, Hkv, d));
-  BDLM_CHECK(encode_lhd(enc, &maps.Vn, Vn, L, Hkv, d));
+  BDLM_CHECK(encode_lhd(enc, &maps.Qc, Qc, L, Hq, d, kFwdTileQ));
+  BDLM_CHECK(encode_lhd(enc, &maps.Qn, Qn, L, Hq, d, kFwdTileQ));
+  BDLM_CHECK(encode_lhd(enc, &maps.Kc, Kc, L, Hkv, d, kFwdTileK));
+  BDLM_CHECK(encode_lhd(enc, &maps.Kn, Kn, L, Hkv, d, kFwdTileK));
+  BDLM_CHECK(encode_lhd(enc, &maps.Vc, Vc, L, Hkv, d, kFwdTileK));
+  BDLM_CHECK(encode_lhd(enc, &maps.Vn, Vn, L, Hkv, d, kFwdTileK));
   FwdParams p;
   p.g = Geom{L, B, Hq, Hkv, kv_begin, kv_end, include_local ? 1 : 0};
   p.scale_log2 = scale * 1.4426950408889634f;

@@ -449,15 +449,20 @@ __device__ __forceinline__ DkvGeo dkv_geo(const BwdParams& p, int64_t idx) {
   return t;
 }
 
-// step k of an item -> (query head, stream, first query row)
-__device__ __forceinline__ void dkv_step(const BwdParams& p, const DkvGeo& t, int k, int& head, int& s,
-                                         int64_t& q0) {
-  const int hh = k / t.per_head;
-  const int r = k - hh * t.per_head;
-  head = t.kvh * (p.g.Hq / p.g.Hkv) + hh;
-  s = r < t.nt0 ? 0 : 1;
-  q0 = (s == 0 ? t.t00 + r : t.t01 + (r - t.nt0)) * KBN;
-}
+// Walks the steps of an item in order: query heads of the GQA group, and for
+// each head the query tiles of the clean rows, then of the corrupted rows.
+struct DkvCursor {
+  int hh, r;  // head within the group, tile index within the head's steps
+  __device__ __forceinline__ void reset() { hh = 0; r = 0; }
+  __device__ __forceinline__ void advance(const DkvGeo& t) {
+    if (++r == t.per_head) { r = 0; ++hh; }
+  }
+  __device__ __forceinline__ void get(const BwdParams& p, const DkvGeo& t, int& head, int& s, int64_t& q0) const {
+    head = t.kvh * (p.g.Hq / p.g.Hkv) + hh;
+    s = r < t.nt0 ? 0 : 1;
+    q0 = (s == 0 ? t.t00 + r : t.t01 + (r - t.nt0)) * KBN;
+  }
+};
 
 // Query-row interval [lo, hi) of stream s that sees key j of key stream ks
 // (empty if the key is not in this call's key set or j >= L).
@@ -549,7 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sV + pn * LY::kKPanel, mv, BAR(KV_KFULL), pn * 64, t.kvh, (int)t.j0);
         }
       }
-      for (int k = 0; k < t.n; ++k, ++qc) {
+      DkvCursor cur;
+      cur.reset();
+      for (int k = 0; k < t.n; ++k, ++qc, cur.advance(t)) {
         const int st = qc % KNS;
         if (qc >= KNS) {
           ok = __all_sync(0xffffffffu, mbar_wait(BAR(KV_QEMPTY + st), ((qc / KNS) - 1) & 1, wd, 42));
@@ -557,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         int head, s;
         int64_t q0;
-        dkv_step(p, t, k, head, s, q0);
+        cur.get(p, t, head, s, q0);
         if (R.lane == 0) {
           mbar_arrive_expect_tx(BAR(KV_QFULL + st), 2 * LY::kQTile);
           const CUtensorMap* mq = s ? &tQn : &tQc;
@@ -673,10 +680,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         alo1 = imax64(a0, a1);
         ahi1 = all_in ? imin64(b0, b1) : alo1;
       }
-      for (int k = 0; k < t.n; ++k, ++qc, ++sc) {
+      DkvCursor cur;
+      cur.reset();
+      for (int k = 0; k < t.n; ++k, ++qc, ++sc, cur.advance(t)) {
         int head, s;
         int64_t q0;
-        dkv_step(p, t, k, head, s, q0);
+        cur.get(p, t, head, s, q0);
         (void)head;
         const int st = qc % KNS;
         const int sb = sc & 1;

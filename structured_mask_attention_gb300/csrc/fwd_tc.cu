@@ -11,18 +11,23 @@
 //
 // Design (one CTA per SM, persistent; 10 warps).  A CTA works on a PAIR of
 // 128-row query tiles at once: the clean and the corrupted tile of the same
-// head and position (equal work: both see (b+1)B keys per row).  Each tile
-// has its own Q, K and V shared-memory slots and its own TMEM S and O:
-//   warp 0      TMA producer (K of the next step as soon as the previous
-//               S MMA released the slot, V as soon as the previous PV did);
-//   warp 1      owns TMEM (512 columns); one lane issues tcgen05.mma, per
-//               tile and step: PV(j-1) then S(j) = Q K^T(j), alternating the
-//               two tiles so one tile's softmax overlaps the other's MMAs;
+// head and position (equal work: both see (b+1)B keys per row).  Keys come in
+// steps of 64.  Each tile has its own Q slot, two K and two V slots in shared
+// memory, and in TMEM two 64-column S buffers and its O accumulator:
+//   warp 0      TMA producer (K of a step as soon as the S MMA two steps
+//               back released its slot, V likewise after the PV MMA);
+//   warp 1      owns TMEM (512 columns); one lane issues tcgen05.mma: per
+//               step, S(j) = Q K^T(j) of both tiles into the free S buffers,
+//               then PV(j-1) of both tiles, so every tile's softmax of step j
+//               overlaps its own S(j+1) and the other tile's MMAs;
 //   warps 2-5   softmax warpgroup of tile 0, warps 6-9 of tile 1: one query
 //               row per thread, online softmax in the log2 domain with a lazy
 //               rescale (the reference max moves only when the row max grows
-//               by more than 8), P written back over S in TMEM as packed bf16
-//               and consumed from there by the PV MMA (A operand in TMEM).
+//               by more than 8), P written back over the S buffer in TMEM as
+//               packed bf16 and consumed from there by the PV MMA (A operand
+//               in TMEM).  The S MMA that next reuses a buffer is issued after
+//               the PV MMA that reads its P (the tensor pipe runs in issue
+//               order).
 // Only key tiles some row of the query tile can see are visited; a per-row
 // interval test masks the tiles that are not fully visible.
 #include <cuda_bf16.h>
@@ -34,22 +39,25 @@ namespace bdlm {
 namespace {
 
 constexpr int BM = kFwdTileQ;   // query rows per tile
-constexpr int BN = kFwdTileK;   // keys per step
+constexpr int BN = kFwdTileK;   // keys per step (64)
 constexpr int kThreads = 320;
-constexpr int kPanelBytes = 128 * 128;  // 128 rows x 128 bytes (64 bf16)
+constexpr int kQPanel = BM * 128;  // 128 rows x 128 bytes (64 bf16)
+constexpr int kKPanel = BN * 128;  // 64 rows x 128 bytes
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// barrier slots, two of each (one per tile)
-enum { B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_SF = 12, B_PF = 14, B_PVD = 16, B_OE = 18,
-       B_COUNT = 20 };
+// barrier slots per tile (tile t adds t * B_PER_TILE)
+enum { B_QF = 0, B_QE = 1, B_KF = 2, B_KE = 4, B_VF = 6, B_VE = 8, B_SF = 10, B_PF = 12, B_PVD = 13, B_OE = 14,
+       B_PER_TILE = 15, B_COUNT = 30 };
 
 template <int HD>
 struct Layout {
-  static constexpr int kTileBytes = 128 * HD * 2;  // 128 rows x HD bf16
-  // per tile t: Q at t * 3 * kTileBytes, K after it, V after K
-  static constexpr int kBar = 6 * kTileBytes;
-  static constexpr int kBytes = kBar + 256;
+  static constexpr int kQBytes = BM * HD * 2;  // 128 rows x HD bf16
+  static constexpr int kKBytes = BN * HD * 2;  // 64 rows x HD bf16
+  // per tile t at t * kTile: Q, K[2], V[2]
+  static constexpr int kTile = kQBytes + 4 * kKBytes;
+  static constexpr int kBar = 2 * kTile;
+  static constexpr int kBytes = kBar + 512;
   // 1024 bytes of slack for alignment; never below 120 KB so that a second
   // CTA cannot share the SM (each CTA holds all 512 TMEM columns).
   static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
@@ -91,13 +99,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw_u32);
-  auto sQ = [&](int t) -> uint32_t { return base + (3 * t + 0) * LY::kTileBytes; };
-  auto sK = [&](int t) -> uint32_t { return base + (3 * t + 1) * LY::kTileBytes; };
-  auto sV = [&](int t) -> uint32_t { return base + (3 * t + 2) * LY::kTileBytes; };
+  auto sQ = [&](int t) -> uint32_t { return base + t * LY::kTile; };
+  auto sK = [&](int t, int st) -> uint32_t { return base + t * LY::kTile + LY::kQBytes + st * LY::kKBytes; };
+  auto sV = [&](int t, int st) -> uint32_t {
+    return base + t * LY::kTile + LY::kQBytes + (2 + st) * LY::kKBytes;
+  };
   const uint32_t bars = base + LY::kBar;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + LY::kBar + 8 * B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + LY::kBar + 8 * B_COUNT + 4);
-  auto BAR = [&](int i, int t) -> uint32_t { return bars + 8u * (uint32_t)(i + t); };
+  auto BAR = [&](int i, int t) -> uint32_t { return bars + 8u * (uint32_t)(i + t * B_PER_TILE); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -105,11 +115,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(BAR(B_QF, t), 1);
       mbar_init(BAR(B_QE, t), 1);
-      mbar_init(BAR(B_KF, t), 1);
-      mbar_init(BAR(B_KE, t), 1);
-      mbar_init(BAR(B_VF, t), 1);
-      mbar_init(BAR(B_VE, t), 1);
-      mbar_init(BAR(B_SF, t), 1);
+      for (int st = 0; st < 2; ++st) {
+        mbar_init(BAR(B_KF + st, t), 1);
+        mbar_init(BAR(B_KE + st, t), 1);
+        mbar_init(BAR(B_VF + st, t), 1);
+        mbar_init(BAR(B_VE + st, t), 1);
+        mbar_init(BAR(B_SF + st, t), 1);
+      }
       mbar_init(BAR(B_PF, t), 128);
       mbar_init(BAR(B_PVD, t), 1);
       mbar_init(BAR(B_OE, t), 128);
@@ -128,7 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Watchdog wd{p.status, p.limit_ns, abort_flag};
   const int grid = gridDim.x, cta = blockIdx.x;
   const int64_t n_pairs = p.n_items / 2;  // items 2i, 2i+1: clean and corrupted tile of one head/position
-  // TMEM columns: S of tile t at 128 t (P over its first 64 columns), O of tile t at 256 + 128 t
+  // TMEM columns: S buffers of tile t at 128 t + {0, 64} (P over their first
+  // 32 columns), O of tile t at 256 + 128 t
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -142,44 +155,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (pi >= n_pairs) break;
         const ItemGeo g0 = item_geo(p, 2 * pi), g1 = item_geo(p, 2 * pi + 1);
         const int nmax = g0.n > g1.n ? g0.n : g1.n;
-        #pragma unroll
-        for (int t = 0; t < 2 && ok; ++t) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
           const ItemGeo& g = t ? g1 : g0;
-          if (g.n == 0) continue;
-          if (qc[t] > 0 && !mbar_wait(BAR(B_QE, t), (qc[t] - 1) & 1, wd, 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(BAR(B_QF, t), LY::kTileBytes);
+          if (g.n == 0 || !ok) continue;
+          if (qc[t] > 0 && !mbar_wait(BAR(B_QE, t), (qc[t] - 1) & 1, wd, 1)) { ok = false; continue; }
+          mbar_arrive_expect_tx(BAR(B_QF, t), LY::kQBytes);
           const CUtensorMap* mq = g.stream ? &tQn : &tQc;
 #pragma unroll
           for (int pn = 0; pn < HD / 64; ++pn)
-            tma_load_3d(sQ(t) + pn * kPanelBytes, mq, BAR(B_QF, t), pn * 64, g.head, (int)g.r0);
+            tma_load_3d(sQ(t) + pn * kQPanel, mq, BAR(B_QF, t), pn * 64, g.head, (int)g.r0);
           ++qc[t];
         }
         for (int j = 0; j < nmax && ok; ++j) {
-          // K of both tiles first (their slots free up early), then V
-          #pragma unroll
+#pragma unroll
           for (int t = 0; t < 2; ++t) {
             const ItemGeo& g = t ? g1 : g0;
-            if (j >= g.n) continue;
-            if (kc[t] > 0 && !mbar_wait(BAR(B_KE, t), (kc[t] - 1) & 1, wd, 2)) { ok = false; break; }
+            if (j >= g.n || !ok) continue;
+            const uint32_t k = kc[t];
+            const int st = k & 1;
+            if (k >= 2 && !mbar_wait(BAR(B_KE + st, t), ((k >> 1) - 1) & 1, wd, 2)) { ok = false; continue; }
             const CUtensorMap* mk = j < g.nc ? &tKc : &tKn;
-            const int key0 = (int)tile_key0(g, j);
-            mbar_arrive_expect_tx(BAR(B_KF, t), LY::kTileBytes);
+            mbar_arrive_expect_tx(BAR(B_KF + st, t), LY::kKBytes);
 #pragma unroll
             for (int pn = 0; pn < HD / 64; ++pn)
-              tma_load_3d(sK(t) + pn * kPanelBytes, mk, BAR(B_KF, t), pn * 64, g.kvh, key0);
+              tma_load_3d(sK(t, st) + pn * kKPanel, mk, BAR(B_KF + st, t), pn * 64, g.kvh, (int)tile_key0(g, j));
             ++kc[t];
           }
-          #pragma unroll
-          for (int t = 0; t < 2 && ok; ++t) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
             const ItemGeo& g = t ? g1 : g0;
-            if (j >= g.n) continue;
-            if (vc[t] > 0 && !mbar_wait(BAR(B_VE, t), (vc[t] - 1) & 1, wd, 3)) { ok = false; break; }
+            if (j >= g.n || !ok) continue;
+            const uint32_t v = vc[t];
+            const int st = v & 1;
+            if (v >= 2 && !mbar_wait(BAR(B_VE + st, t), ((v >> 1) - 1) & 1, wd, 3)) { ok = false; continue; }
             const CUtensorMap* mv = j < g.nc ? &tVc : &tVn;
-            const int key0 = (int)tile_key0(g, j);
-            mbar_arrive_expect_tx(BAR(B_VF, t), LY::kTileBytes);
+            mbar_arrive_expect_tx(BAR(B_VF + st, t), LY::kKBytes);
 #pragma unroll
             for (int pn = 0; pn < HD / 64; ++pn)
-              tma_load_3d(sV(t) + pn * kPanelBytes, mv, BAR(B_VF, t), pn * 64, g.kvh, key0);
+              tma_load_3d(sV(t, st) + pn * kKPanel, mv, BAR(B_VF + st, t), pn * 64, g.kvh, (int)tile_key0(g, j));
             ++vc[t];
           }
         }
@@ -190,57 +204,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16(BM, BN, false, false);
       constexpr uint32_t kIdescO = idesc_bf16(BM, HD, false, true);
-      uint32_t qc[2] = {0, 0}, kc[2] = {0, 0}, vc[2] = {0, 0}, pc[2] = {0, 0}, oc[2] = {0, 0};
+      uint32_t qc[2] = {0, 0}, kc[2] = {0, 0}, vc[2] = {0, 0}, oc[2] = {0, 0};
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
         const int64_t pi = snake_item(rnd, cta, grid);
         if (pi >= n_pairs) break;
         const ItemGeo g0 = item_geo(p, 2 * pi), g1 = item_geo(p, 2 * pi + 1);
         const int nmax = g0.n > g1.n ? g0.n : g1.n;
-        #pragma unroll
-        for (int t = 0; t < 2 && ok; ++t) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
           const ItemGeo& g = t ? g1 : g0;
-          if (g.n == 0) continue;
-          if (!mbar_wait(BAR(B_QF, t), qc[t] & 1, wd, 4)) { ok = false; break; }
+          if (g.n == 0 || !ok) continue;
+          if (!mbar_wait(BAR(B_QF, t), qc[t] & 1, wd, 4)) { ok = false; continue; }
           ++qc[t];
         }
         for (int j = 0; j <= nmax && ok; ++j) {
-          #pragma unroll
+          // S(j) of both tiles: buffer (S count & 1); its previous P was read
+          // by the PV MMA issued one iteration earlier
+#pragma unroll
           for (int t = 0; t < 2; ++t) {
             const ItemGeo& g = t ? g1 : g0;
-            const uint32_t tS = tmem + t * 128, tO = tmem + 256 + t * 128;
-            if (j >= 1 && j <= g.n) {
-              // PV(j-1): O += P V with P (bf16) in TMEM over S
-              if (!mbar_wait(BAR(B_PF, t), pc[t] & 1, wd, 5)) { ok = false; break; }
-              if (j == 1 && oc[t] > 0 && !mbar_wait(BAR(B_OE, t), (oc[t] - 1) & 1, wd, 6)) { ok = false; break; }
-              if (!mbar_wait(BAR(B_VF, t), vc[t] & 1, wd, 7)) { ok = false; break; }
-              tc_fence_after();
+            if (j >= g.n || !ok) continue;
+            const uint32_t k = kc[t];
+            const int st = k & 1;
+            if (!mbar_wait(BAR(B_KF + st, t), (k >> 1) & 1, wd, 8)) { ok = false; continue; }
+            tc_fence_after();
+            const uint32_t tS = tmem + t * 128 + st * BN;
 #pragma unroll
-              for (int kk = 0; kk < BN / 16; ++kk) {
-                const uint64_t bd = sdesc_sw128(sV(t) + kk * 2048, kPanelBytes, 1024);
-                tc_mma_ts(tO, tS + kk * 8, bd, kIdescO, (j > 1 || kk > 0) ? 1u : 0u);
-              }
-              tc_commit(BAR(B_VE, t));
-              tc_commit(BAR(B_PVD, t));
-              ++pc[t];
-              ++vc[t];
-              if (j == g.n) ++oc[t];
+            for (int kk = 0; kk < HD / 16; ++kk) {
+              const uint32_t qo = (kk >> 2) * kQPanel + (kk & 3) * 32;
+              const uint32_t ko = (kk >> 2) * kKPanel + (kk & 3) * 32;
+              tc_mma_ss(tS, sdesc_sw128(sQ(t) + qo, 16, 1024), sdesc_sw128(sK(t, st) + ko, 16, 1024), kIdescS,
+                        kk > 0 ? 1u : 0u);
             }
-            if (j < g.n) {
-              // S(j) = Q K^T(j); issued after PV(j-1) so it never overwrites an unread P
-              if (!mbar_wait(BAR(B_KF, t), kc[t] & 1, wd, 8)) { ok = false; break; }
-              tc_fence_after();
+            tc_commit(BAR(B_SF + st, t));
+            tc_commit(BAR(B_KE + st, t));
+            if (j == g.n - 1) tc_commit(BAR(B_QE, t));
+            ++kc[t];
+          }
+          // PV(j-1) of both tiles: O += P V, P (bf16) in TMEM over its S buffer
 #pragma unroll
-              for (int kk = 0; kk < HD / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                tc_mma_ss(tS, sdesc_sw128(sQ(t) + off, 16, 1024), sdesc_sw128(sK(t) + off, 16, 1024), kIdescS,
-                          kk > 0 ? 1u : 0u);
-              }
-              tc_commit(BAR(B_SF, t));
-              tc_commit(BAR(B_KE, t));
-              if (j == g.n - 1) tc_commit(BAR(B_QE, t));
-              ++kc[t];
+          for (int t = 0; t < 2; ++t) {
+            const ItemGeo& g = t ? g1 : g0;
+            if (j < 1 || j > g.n || !ok) continue;
+            const uint32_t v = vc[t];
+            const int st = v & 1;
+            if (!mbar_wait(BAR(B_PF, t), v & 1, wd, 5)) { ok = false; continue; }
+            if (j == 1 && oc[t] > 0 && !mbar_wait(BAR(B_OE, t), (oc[t] - 1) & 1, wd, 6)) { ok = false; continue; }
+            if (!mbar_wait(BAR(B_VF + st, t), (v >> 1) & 1, wd, 7)) { ok = false; continue; }
+            tc_fence_after();
+            const uint32_t tP = tmem + t * 128 + st * BN, tO = tmem + 256 + t * 128;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              const uint64_t bd = sdesc_sw128(sV(t, st) + kk * 2048, kKPanel, 1024);
+              tc_mma_ts(tO, tP + kk * 8, bd, kIdescO, (j > 1 || kk > 0) ? 1u : 0u);
             }
+            tc_commit(BAR(B_VE + st, t));
+            tc_commit(BAR(B_PVD, t));
+            ++vc[t];
+            if (j == g.n) ++oc[t];
           }
         }
       }
@@ -251,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t tl = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tS = tmem + tl + t * 128, tO = tmem + tl + 256 + t * 128;
-    uint32_t sc = 0, pc = 0;
+    const uint32_t tO = tmem + tl + 256 + t * 128;
+    uint32_t sc = 0;
     bool ok = true;
     for (int64_t rnd = 0; ok; ++rnd) {
       const int64_t pi = snake_item(rnd, cta, grid);
@@ -289,28 +311,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t key0 = tile_key0(g, j);
         const bool full = cs ? tile_full(key0, BN, g.q.c_all_lo, g.q.c_all_hi, p.g.L)
                              : tile_full(key0, BN, g.q.n_all_lo, g.q.n_all_hi, p.g.L);
-        ok = mbar_wait(BAR(B_SF, t), sc & 1, wd, 9);
+        const int sb = sc & 1;
+        ok = mbar_wait(BAR(B_SF + sb, t), (sc >> 1) & 1, wd, 9);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        const int lo = full ? -1 : (int)imax64(imin64((cs ? clo : nlo) - key0, BN + 1), -1);
-        const int hi = full ? BN + 1 : (int)imax64(imin64((cs ? chi : nhi) - key0, BN + 1), -1);
-        // pass 1: masked row max (64 columns at a time)
+        const uint32_t tS = tmem + tl + t * 128 + sb * BN;
+        uint32_t a[32], b[32];
+        tmem_ld32x2(tS, tS + 32, a, b);
         float mx = -INFINITY;
+        if (full) {
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t a[32], b[32];
-          tmem_ld32x2(tS + 64 * h2, tS + 64 * h2 + 32, a, b);
-          if (full) {
+          for (int c = 0; c < 32; ++c) mx = fmaxf(mx, fmaxf(__uint_as_float(a[c]), __uint_as_float(b[c])));
+        } else {
+          const int lo = (int)imax64(imin64((cs ? clo : nlo) - key0, BN + 1), -1);
+          const int hi = (int)imax64(imin64((cs ? chi : nhi) - key0, BN + 1), -1);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) mx = fmaxf(mx, fmaxf(__uint_as_float(a[c]), __uint_as_float(b[c])));
-          } else {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const int ca = 64 * h2 + c, cb = ca + 32;
-              if (ca >= lo && ca < hi) mx = fmaxf(mx, __uint_as_float(a[c]));
-              if (cb >= lo && cb < hi) mx = fmaxf(mx, __uint_as_float(b[c]));
-            }
+          for (int c = 0; c < 32; ++c) {
+            if (c < lo || c >= hi) a[c] = __float_as_uint(-INFINITY);
+            if (c + 32 < lo || c + 32 >= hi) b[c] = __float_as_uint(-INFINITY);
+            mx = fmaxf(mx, fmaxf(__uint_as_float(a[c]), __uint_as_float(b[c])));
           }
         }
         const float mx2 = mx * sl2;
@@ -324,37 +344,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = true;
         }
         const float nm = (m_use == -INFINITY) ? 0.f : -m_use;
-        // pass 2: P = exp2(s c - m), row sum, P as packed bf16 over the columns
-        // already read (the PV MMA's A operand)
-        float rs = 0.f;
+        // P = exp2(s c - m) (masked entries are -inf -> 0), row sum, and P as
+        // packed bf16 over the first 32 columns of this S buffer
+        float rs0 = 0.f, rs1 = 0.f;
+        uint32_t pk[32];
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t a[32], b[32];
-          tmem_ld32x2(tS + 64 * h2, tS + 64 * h2 + 32, a, b);
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const uint32_t (&x)[32] = q ? b : a;
-            uint32_t pk[16];
-#pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              const int ca = 64 * h2 + 32 * q + c;
-              float p0 = ex2_approx(fmaf(__uint_as_float(x[c]), sl2, nm));
-              float p1 = ex2_approx(fmaf(__uint_as_float(x[c + 1]), sl2, nm));
-              if (!full) {
-                p0 = (ca >= lo && ca < hi) ? p0 : 0.f;
-                p1 = (ca + 1 >= lo && ca + 1 < hi) ? p1 : 0.f;
-              }
-              rs += p0 + p1;
-              pk[c / 2] = pack_bf16x2(p0, p1);
-            }
-            tmem_st16(tS + 32 * h2 + 16 * q, pk);
-          }
+        for (int c = 0; c < 32; c += 2) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(a[c]), sl2, nm));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(a[c + 1]), sl2, nm));
+          const float q0 = ex2_approx(fmaf(__uint_as_float(b[c]), sl2, nm));
+          const float q1 = ex2_approx(fmaf(__uint_as_float(b[c + 1]), sl2, nm));
+          rs0 += p0 + p1;
+          rs1 += q0 + q1;
+          pk[c / 2] = pack_bf16x2(p0, p1);
+          pk[16 + c / 2] = pack_bf16x2(q0, q1);
         }
-        l = l * alpha + rs;
+        tmem_st32(tS, pk);
+        l = l * alpha + (rs0 + rs1);
         m_ref = m_use;
         if (j > 0) {
           // PV(j-1) must be complete before O is rescaled
-          ok = mbar_wait(BAR(B_PVD, t), (pc - 1) & 1, wd, 10);
+          ok = mbar_wait(BAR(B_PVD, t), (sc - 1) & 1, wd, 10);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after();
@@ -371,10 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(BAR(B_PF, t));
-        ++pc;
       }
       if (!ok) break;
-      ok = mbar_wait(BAR(B_PVD, t), (pc - 1) & 1, wd, 11);
+      ok = mbar_wait(BAR(B_PVD, t), (sc - 1) & 1, wd, 11);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
