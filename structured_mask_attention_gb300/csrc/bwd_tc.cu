@@ -247,11 +247,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(BAR(DQ_DSFULL + db), (dc >> 1) & 1, wd, 24)) return false;
           if (jj == 0 && itn > 0 && !mbar_wait(BAR(DQ_OEMPTY), (itn - 1) & 1, wd, 25)) return false;
           tc_fence_after();
+          const uint64_t bk0 = sdesc_sw128(sK + st * LY::kKTile, LY::kKPanel, 1024);
+          const uint32_t acc0 = jj > 0 ? 1u : 0u;
 #pragma unroll
-          for (int kk = 0; kk < QBN / 16; ++kk) {
-            const uint64_t bd = sdesc_sw128(sK + st * LY::kKTile + kk * 2048, LY::kKPanel, 1024);
-            tc_mma_ts(tmem + 256, tmem + db * QBN + packed_col(kk), bd, kIdQ, (jj > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < QBN / 16; ++kk)
+            tc_mma_ts(tmem + 256, tmem + db * QBN + packed_col(kk), desc_add(bk0, kk * 2048), kIdQ,
+                      kk > 0 ? 1u : acc0);
           tc_commit(BAR(DQ_KVEMPTY + st));
           ++dc;
           return true;
@@ -262,13 +263,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(BAR(DQ_KVFULL + st), (kvc / QNS) & 1, wd, 26)) { ok = false; break; }
           tc_fence_after();
           // buffer sb was last read by dQ(j-2), issued before this point
+          const uint64_t dk0 = sdesc_sw128(sK + st * LY::kKTile, 16, 1024);
+          const uint64_t dv0 = sdesc_sw128(sV + st * LY::kKTile, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint32_t ko = st * LY::kKTile + (kk >> 2) * LY::kKPanel + (kk & 3) * 32;
-            tc_mma_ts(tmem + sb * QBN, tmem + kColQ + kk * 8, sdesc_sw128(sK + ko, 16, 1024), kIdS,
-                      kk > 0 ? 1u : 0u);
-            tc_mma_ts(tmem + 128 + sb * QBN, tmem + kColdO + kk * 8, sdesc_sw128(sV + ko, 16, 1024), kIdS,
-                      kk > 0 ? 1u : 0u);
+            const uint32_t ko = (kk >> 2) * LY::kKPanel + (kk & 3) * 32;
+            tc_mma_ts(tmem + sb * QBN, tmem + kColQ + kk * 8, desc_add(dk0, ko), kIdS, kk > 0 ? 1u : 0u);
+            tc_mma_ts(tmem + 128 + sb * QBN, tmem + kColdO + kk * 8, desc_add(dv0, ko), kIdS, kk > 0 ? 1u : 0u);
           }
           tc_commit(BAR(DQ_SFULL + sb));
           if (j >= 1 && !do_dq(j - 1)) { ok = false; break; }
@@ -596,6 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (R.lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(KBM, KBN, false, false);
       constexpr uint32_t kIdA = idesc_bf16(KBM, HD, false, true);
+      const uint64_t dK0 = sdesc_sw128(sK, 16, 1024), dV0 = sdesc_sw128(sV, 16, 1024);
       uint32_t itn = 0, qc = 0, sc = 0, pc = 0;
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
@@ -612,13 +614,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(BAR(KV_PFULL + pb), (pc >> 1) & 1, wd, 44)) return false;
           if (kk == 0 && itn > 0 && !mbar_wait(BAR(KV_ACCEMPTY), (itn - 1) & 1, wd, 45)) return false;
           tc_fence_after();
+          const uint64_t bo0 = sdesc_sw128(sdO + st * LY::kQTile, LY::kQPanel, 1024);
+          const uint64_t bq0 = sdesc_sw128(sQ + st * LY::kQTile, LY::kQPanel, 1024);
+          const uint32_t acc0 = kk > 0 ? 1u : 0u;
 #pragma unroll
           for (int k4 = 0; k4 < KBN / 16; ++k4) {
-            const uint32_t acc = (kk > 0 || k4 > 0) ? 1u : 0u;
-            const uint64_t bo = sdesc_sw128(sdO + st * LY::kQTile + k4 * 2048, LY::kQPanel, 1024);
-            const uint64_t bq = sdesc_sw128(sQ + st * LY::kQTile + k4 * 2048, LY::kQPanel, 1024);
-            tc_mma_ts(tmem + 128, tmem + 256 + pb * KBN + packed_col(k4), bo, kIdA, acc);
-            tc_mma_ts(tmem + 0, tmem + 384 + pb * KBN + packed_col(k4), bq, kIdA, acc);
+            const uint32_t acc = k4 > 0 ? 1u : acc0;
+            tc_mma_ts(tmem + 128, tmem + 256 + pb * KBN + packed_col(k4), desc_add(bo0, k4 * 2048), kIdA, acc);
+            tc_mma_ts(tmem + 0, tmem + 384 + pb * KBN + packed_col(k4), desc_add(bq0, k4 * 2048), kIdA, acc);
           }
           tc_commit(BAR(KV_QEMPTY + st));
           ++pc;
@@ -630,14 +633,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(BAR(KV_QFULL + st), (qc / KNS) & 1, wd, 46)) { ok = false; break; }
           tc_fence_after();
           // buffer sb was last read by the dV/dK MMAs of step k-2, issued before this point
+          const uint64_t dq0 = sdesc_sw128(sQ + st * LY::kQTile, 16, 1024);
+          const uint64_t do0 = sdesc_sw128(sdO + st * LY::kQTile, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
             const uint32_t ko = (kk >> 2) * LY::kKPanel + (kk & 3) * 32;
-            const uint32_t qo = st * LY::kQTile + (kk >> 2) * LY::kQPanel + (kk & 3) * 32;
-            tc_mma_ss(tmem + 256 + sb * KBN, sdesc_sw128(sK + ko, 16, 1024), sdesc_sw128(sQ + qo, 16, 1024), kIdS,
-                      kk > 0 ? 1u : 0u);
-            tc_mma_ss(tmem + 384 + sb * KBN, sdesc_sw128(sV + ko, 16, 1024), sdesc_sw128(sdO + qo, 16, 1024),
-                      kIdS, kk > 0 ? 1u : 0u);
+            const uint32_t qo = (kk >> 2) * LY::kQPanel + (kk & 3) * 32;
+            tc_mma_ss(tmem + 256 + sb * KBN, desc_add(dK0, ko), desc_add(dq0, qo), kIdS, kk > 0 ? 1u : 0u);
+            tc_mma_ss(tmem + 384 + sb * KBN, desc_add(dV0, ko), desc_add(do0, qo), kIdS, kk > 0 ? 1u : 0u);
           }
           tc_commit(BAR(KV_SFULL + sb));
           if (k >= 1 && !do_acc(k - 1)) { ok = false; break; }

@@ -230,12 +230,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(BAR(B_KF + st, t), (k >> 1) & 1, wd, 8)) { ok = false; continue; }
             tc_fence_after();
             const uint32_t tS = tmem + t * 128 + st * BN;
+            const uint64_t dq0 = sdesc_sw128(sQ(t), 16, 1024), dk0 = sdesc_sw128(sK(t, st), 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {
               const uint32_t qo = (kk >> 2) * kQPanel + (kk & 3) * 32;
               const uint32_t ko = (kk >> 2) * kKPanel + (kk & 3) * 32;
-              tc_mma_ss(tS, sdesc_sw128(sQ(t) + qo, 16, 1024), sdesc_sw128(sK(t, st) + ko, 16, 1024), kIdescS,
-                        kk > 0 ? 1u : 0u);
+              tc_mma_ss(tS, desc_add(dq0, qo), desc_add(dk0, ko), kIdescS, kk > 0 ? 1u : 0u);
             }
             tc_commit(BAR(B_SF + st, t));
             tc_commit(BAR(B_KE + st, t));
@@ -254,11 +254,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(BAR(B_VF + st, t), (v >> 1) & 1, wd, 7)) { ok = false; continue; }
             tc_fence_after();
             const uint32_t tP = tmem + t * 128 + st * BN, tO = tmem + 256 + t * 128;
+            const uint64_t dv0 = sdesc_sw128(sV(t, st), kKPanel, 1024);
+            const uint32_t acc0 = j > 1 ? 1u : 0u;
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              const uint64_t bd = sdesc_sw128(sV(t, st) + kk * 2048, kKPanel, 1024);
-              tc_mma_ts(tO, tP + kk * 8, bd, kIdescO, (j > 1 || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < BN / 16; ++kk)
+              tc_mma_ts(tO, tP + kk * 8, desc_add(dv0, kk * 2048), kIdescO, kk > 0 ? 1u : acc0);
             tc_commit(BAR(B_VE + st, t));
             tc_commit(BAR(B_PVD, t));
             ++vc[t];

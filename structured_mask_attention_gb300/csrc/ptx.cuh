@@ -178,6 +178,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// Descriptor of the same operand `byte_off` bytes further on (the start
+// address field is the low 14 bits, in 16-byte units; offsets stay inside
+// shared memory so the field never carries into the next one).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t byte_off) { return d + (uint64_t)(byte_off >> 4); }
+
 // 32 lanes x 32 columns of 32-bit TMEM -> registers (one row per thread),
 // waiting for completion inside the same statement.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
