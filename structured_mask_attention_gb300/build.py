@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbdlm_attn.so")
-SOURCES = ["abi.cu", "fwd_tc.cu", "bwd_tc.cu", "small_kernels.cu", "noalloc.cu"]
+SOURCES = ["abi.cu", "fwd_tc.cu", "bwd_dq.cu", "bwd_dkv.cu", "small_kernels.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -292,15 +292,11 @@ cudaError_t launch_backward_passes(const BwdParams& p, const DeviceInfo& info, v
   BwdMaps m;
   const int64_t L = p.g.L;
   const int Hq = p.g.Hq, Hkv = p.g.Hkv, d = p.d;
-  struct E { CUtensorMap* map; const void* ptr; int H; int rows; };
-  const E list[16] = {{&m.Qc128, p.Qc, Hq, 128}, {&m.Qn128, p.Qn, Hq, 128}, {&m.dOc128, p.dOc, Hq, 128},
-                      {&m.dOn128, p.dOn, Hq, 128}, {&m.Kc64, p.Kc, Hkv, 64},   {&m.Kn64, p.Kn, Hkv, 64},
-                      {&m.Vc64, p.Vc, Hkv, 64},    {&m.Vn64, p.Vn, Hkv, 64},   {&m.Qc64, p.Qc, Hq, 64},
-                      {&m.Qn64, p.Qn, Hq, 64},     {&m.dOc64, p.dOc, Hq, 64},  {&m.dOn64, p.dOn, Hq, 64},
-                      {&m.Kc128, p.Kc, Hkv, 128},  {&m.Kn128, p.Kn, Hkv, 128}, {&m.Vc128, p.Vc, Hkv, 128},
-                      {&m.Vn128, p.Vn, Hkv, 128}};
+  struct E { CUtensorMap* map; const void* ptr; int H; };
+  const E list[8] = {{&m.Qc, p.Qc, Hq},   {&m.Qn, p.Qn, Hq},   {&m.dOc, p.dOc, Hq}, {&m.dOn, p.dOn, Hq},
+                     {&m.Kc, p.Kc, Hkv}, {&m.Kn, p.Kn, Hkv}, {&m.Vc, p.Vc, Hkv},  {&m.Vn, p.Vn, Hkv}};
   for (const E& x : list)
-    if ((*vstatus = encode_lhd(enc, x.map, x.ptr, L, x.H, d, x.rows)) != BDLM_OK) return cudaSuccess;
+    if ((*vstatus = encode_lhd(enc, x.map, x.ptr, L, x.H, d, kBwdTile)) != BDLM_OK) return cudaSuccess;
   uint32_t* status = static_cast<uint32_t*>(ws);
   cudaError_t e;
   {

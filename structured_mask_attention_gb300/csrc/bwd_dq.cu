@@ -1,0 +1,367 @@
+// bwd_dq.cu -- dQ pass of the two-stream BDLM attention backward (sm_103a).
+//
+// dQ = scale dS K with dS = P o (dP - D), P = exp(scale Q K^T - LSE),
+// dP = dO V^T, over each query row's visible keys (see bwd_common.cuh for
+// the gradient definitions and their source).
+//
+// Item = (128-row query tile, head, stream) in the forward's longest-first
+// order.  Q and dO of the item stay in shared memory; 128-key K tiles stream
+// through a 3-stage TMA ring (a K tile is read by S(j) and by dQ(j), one
+// step later) and V tiles through a 2-stage ring.  Per step j (128 keys),
+// MMA warp:
+//   S(j)  = Q K^T   into S buffer j & 1      (TMEM, 128 columns)
+//   dP(j) = dO V^T  into the dP buffer       (TMEM, 128 columns), issued once
+//                   the elementwise warps have read dP(j-1)
+//   dQ   += dS(j-1) K(j-1)                   (dS as packed bf16 in TMEM over
+//                   S buffer (j-1) & 1, K read as an MN-major operand)
+// The elementwise warps (thread = query row, 64 keys per warpgroup) form dS
+// and write it back over the S columns they have just read.  The S MMA that
+// next reuses a buffer is issued after the dQ MMA reading its dS (the tensor
+// pipe runs in issue order).  Every output row is written once.
+#include "bwd_common.cuh"
+
+namespace bdlm {
+namespace {
+
+using namespace bwd;
+
+constexpr int QBM = 128;  // query rows per item
+constexpr int QBN = 128;  // keys per step
+constexpr int KNS = 3;    // K stages
+constexpr int VNS = 2;    // V stages
+
+enum { DQ_QF = 0, DQ_QE = 1, DQ_KF = 2, DQ_KE = 5, DQ_VF = 8, DQ_VE = 10, DQ_SF = 12, DQ_DPF = 14,
+       DQ_DPFREE = 15, DQ_DSF = 16, DQ_DONE = 18, DQ_OE = 19, DQ_NBAR = 20 };
+
+template <int HD>
+struct DqLayout {
+  static constexpr int kTile = 128 * HD * 2;  // 128 rows x HD bf16 (Q, dO, K, V tiles alike)
+  static constexpr int kPanel = 128 * 128;    // 128 rows x 64 bf16
+  static constexpr int kQ = 0;
+  static constexpr int kdO = kQ + kTile;
+  static constexpr int kK = kdO + kTile;
+  static constexpr int kV = kK + KNS * kTile;
+  static constexpr int kBar = kV + VNS * kTile;
+  static constexpr int kBytes = kBar + 256;
+  static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
+};
+
+struct DqGeo {
+  int stream, head, kvh;
+  int64_t r0;
+  QTileRanges q;
+  int nc, n;
+};
+
+__device__ __forceinline__ DqGeo dq_geo(const BwdParams& p, int64_t idx) {
+  DqGeo t;
+  const QItem it = q_item(p.g, QBM, idx);
+  t.stream = it.stream;
+  t.head = it.head;
+  t.kvh = it.head / (p.g.Hq / p.g.Hkv);
+  t.r0 = it.qtile * QBM;
+  const int64_t r1 = imin64(t.r0 + QBM, p.g.L);
+  t.q = qtile_ranges(p.g, t.stream, t.r0, r1, QBN);
+  t.nc = (int)(t.q.c1 - t.q.c0);
+  t.n = t.nc + (int)(t.q.n1 - t.q.n0);
+  return t;
+}
+
+__device__ __forceinline__ int dq_key0(const DqGeo& t, int j) {
+  return (int)((j < t.nc ? t.q.c0 + j : t.q.n0 + (j - t.nc)) * QBN);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    bdlm_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tQc, const __grid_constant__ CUtensorMap tQn,
+                          const __grid_constant__ CUtensorMap tdOc, const __grid_constant__ CUtensorMap tdOn,
+                          const __grid_constant__ CUtensorMap tKc, const __grid_constant__ CUtensorMap tKn,
+                          const __grid_constant__ CUtensorMap tVc, const __grid_constant__ CUtensorMap tVn,
+                          const BwdParams p, const int64_t n_items, uint32_t* status, const uint64_t limit_ns) {
+  using LY = DqLayout<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw_u32);
+  const uint32_t sQ = base + LY::kQ, sdO = base + LY::kdO, sK = base + LY::kK, sV = base + LY::kV;
+  const uint32_t bars = base + LY::kBar;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + LY::kBar + 8 * DQ_NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + LY::kBar + 8 * DQ_NBAR + 4);
+  auto BAR = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+  const Role R = role();
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(DQ_QF), 1);
+    mbar_init(BAR(DQ_QE), 1);
+    for (int s = 0; s < KNS; ++s) {
+      mbar_init(BAR(DQ_KF + s), 1);
+      mbar_init(BAR(DQ_KE + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(BAR(DQ_VF + s), 1);
+      mbar_init(BAR(DQ_VE + s), 1);
+      mbar_init(BAR(DQ_SF + s), 1);
+      mbar_init(BAR(DQ_DSF + s), kEwThreads);
+    }
+    mbar_init(BAR(DQ_DPF), 1);
+    mbar_init(BAR(DQ_DPFREE), kEwThreads);
+    mbar_init(BAR(DQ_DONE), 1);
+    mbar_init(BAR(DQ_OE), kEwThreads);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (R.warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Watchdog wd{status, limit_ns, abort_flag};
+  const int grid = gridDim.x, cta = blockIdx.x;
+  // TMEM columns: S buffers at 0 and 128 (dS over them), dP at 256, dQ at 384
+  constexpr uint32_t kColDP = 256, kColDQ = 384;
+
+  if (R.warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (R.lane == 0) {
+      uint32_t itn = 0, g = 0;  // items with work, global step count
+      bool ok = true;
+      for (int64_t rnd = 0; ok; ++rnd) {
+        const int64_t idx = snake_item(rnd, cta, grid);
+        if (idx >= n_items) break;
+        const DqGeo t = dq_geo(p, idx);
+        if (t.n == 0) continue;
+        if (itn > 0 && !mbar_wait(BAR(DQ_QE), (itn - 1) & 1, wd, 21)) { ok = false; break; }
+        mbar_arrive_expect_tx(BAR(DQ_QF), 2 * LY::kTile);
+        const CUtensorMap* mq = t.stream ? &tQn : &tQc;
+        const CUtensorMap* mo = t.stream ? &tdOn : &tdOc;
+#pragma unroll
+        for (int pn = 0; pn < HD / 64; ++pn) {
+          tma_load_3d(sQ + pn * LY::kPanel, mq, BAR(DQ_QF), pn * 64, t.head, (int)t.r0);
+          tma_load_3d(sdO + pn * LY::kPanel, mo, BAR(DQ_QF), pn * 64, t.head, (int)t.r0);
+        }
+        ++itn;
+        for (int j = 0; j < t.n; ++j, ++g) {
+          const bool cs = j < t.nc;
+          const int key0 = dq_key0(t, j);
+          const int ks = g % KNS, vs = g & 1;
+          if (g >= KNS && !mbar_wait(BAR(DQ_KE + ks), ((g / KNS) - 1) & 1, wd, 22)) { ok = false; break; }
+          mbar_arrive_expect_tx(BAR(DQ_KF + ks), LY::kTile);
+#pragma unroll
+          for (int pn = 0; pn < HD / 64; ++pn)
+            tma_load_3d(sK + ks * LY::kTile + pn * LY::kPanel, cs ? &tKc : &tKn, BAR(DQ_KF + ks), pn * 64, t.kvh,
+                        key0);
+          if (g >= VNS && !mbar_wait(BAR(DQ_VE + vs), ((g >> 1) - 1) & 1, wd, 23)) { ok = false; break; }
+          mbar_arrive_expect_tx(BAR(DQ_VF + vs), LY::kTile);
+#pragma unroll
+          for (int pn = 0; pn < HD / 64; ++pn)
+            tma_load_3d(sV + vs * LY::kTile + pn * LY::kPanel, cs ? &tVc : &tVn, BAR(DQ_VF + vs), pn * 64, t.kvh,
+                        key0);
+        }
+      }
+    }
+  } else if (R.warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (R.lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(QBM, QBN, false, false);
+      constexpr uint32_t kIdQ = idesc_bf16(QBM, HD, false, true);
+      const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024), do0 = sdesc_sw128(sdO, 16, 1024);
+      uint32_t itn = 0, g = 0;
+      bool ok = true;
+      for (int64_t rnd = 0; ok; ++rnd) {
+        const int64_t idx = snake_item(rnd, cta, grid);
+        if (idx >= n_items) break;
+        const DqGeo t = dq_geo(p, idx);
+        if (t.n == 0) continue;
+        if (!mbar_wait(BAR(DQ_QF), itn & 1, wd, 24)) { ok = false; break; }
+        const uint32_t g0 = g;
+        // dQ += dS(jj) K(jj), dS packed over S buffer of step jj
+        auto do_dq = [&](int jj) -> bool {
+          const uint32_t gg = g0 + jj;
+          const int b = gg & 1, ks = gg % KNS;
+          if (!mbar_wait(BAR(DQ_DSF + b), (gg >> 1) & 1, wd, 25)) return false;
+          if (jj == 0 && itn > 0 && !mbar_wait(BAR(DQ_OE), (itn - 1) & 1, wd, 26)) return false;
+          tc_fence_after();
+          const uint64_t bk0 = sdesc_sw128(sK + ks * LY::kTile, LY::kPanel, 1024);
+          const uint32_t acc0 = jj > 0 ? 1u : 0u;
+#pragma unroll
+          for (int kk = 0; kk < QBN / 16; ++kk)
+            tc_mma_ts(tmem + kColDQ, tmem + b * 128 + packed_col128(kk), desc_add(bk0, kk * 2048), kIdQ,
+                      kk > 0 ? 1u : acc0);
+          tc_commit(BAR(DQ_KE + ks));
+          return true;
+        };
+        for (int j = 0; j < t.n && ok; ++j, ++g) {
+          const int b = g & 1, ks = g % KNS, vs = g & 1;
+          // S(j) into buffer b: the dS last held there (step g-2) was read by
+          // the dQ MMA issued one iteration earlier
+          if (!mbar_wait(BAR(DQ_KF + ks), (g / KNS) & 1, wd, 27)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t dk0 = sdesc_sw128(sK + ks * LY::kTile, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * LY::kPanel + (kk & 3) * 32;
+            tc_mma_ss(tmem + b * 128, desc_add(dq0, off), desc_add(dk0, off), kIdS, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(BAR(DQ_SF + b));
+          // dP(j) once the elementwise warps have read dP(j-1)
+          if (g >= 1 && !mbar_wait(BAR(DQ_DPFREE), (g - 1) & 1, wd, 28)) { ok = false; break; }
+          if (!mbar_wait(BAR(DQ_VF + vs), (g >> 1) & 1, wd, 29)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t dv0 = sdesc_sw128(sV + vs * LY::kTile, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * LY::kPanel + (kk & 3) * 32;
+            tc_mma_ss(tmem + kColDP, desc_add(do0, off), desc_add(dv0, off), kIdS, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(BAR(DQ_DPF));
+          tc_commit(BAR(DQ_VE + vs));
+          if (j == t.n - 1) tc_commit(BAR(DQ_QE));
+          if (j >= 1 && !do_dq(j - 1)) { ok = false; break; }
+        }
+        if (!ok) break;
+        if (!do_dq(t.n - 1)) { ok = false; break; }
+        tc_commit(BAR(DQ_DONE));
+        ++itn;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise
+    // thread = query row; warpgroup `half` = keys [64 half, 64 half + 64) of a
+    // step, taken in two 32-key sub-steps
+    const int row = R.row, half = R.half;
+    uint32_t itn = 0, g = 0;
+    bool ok = true;
+    for (int64_t rnd = 0; ok; ++rnd) {
+      const int64_t idx = snake_item(rnd, cta, grid);
+      if (idx >= n_items) break;
+      const DqGeo t = dq_geo(p, idx);
+      const int64_t r = t.r0 + row;
+      const bool valid = r < p.g.L;
+      void* dqbase = t.stream ? p.dQn : p.dQc;
+      const int64_t oofs = (r * p.g.Hq + t.head) * HD + half * (HD / 2);
+      if (t.n == 0) {
+        // no visible key for the whole tile: dQ rows are zero
+        if (valid && !p.dq_accumulate) {
+          if (p.g_f32) {
+            float4* o = reinterpret_cast<float4*>(static_cast<float*>(dqbase) + oofs);
+#pragma unroll
+            for (int c = 0; c < HD / 8; ++c) o[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+          } else {
+            uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dqbase) + oofs);
+#pragma unroll
+            for (int c = 0; c < HD / 16; ++c) o[c] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        continue;
+      }
+      const int64_t rr = valid ? r : p.g.L - 1;
+      int64_t clo, chi, nlo, nhi;
+      clean_interval(p.g, t.stream, rr, clo, chi);
+      noisy_interval(p.g, t.stream, rr, nlo, nhi);
+      const float nlse2 = valid ? -(t.stream ? p.LSEn : p.LSEc)[(int64_t)t.head * p.g.L + r] * kLog2e : 0.f;
+      const float Dv = valid ? (t.stream ? p.Dn : p.Dc)[(int64_t)t.head * p.g.L + r] : 0.f;
+      const float sl2 = p.scale_log2;
+      for (int j = 0; j < t.n; ++j, ++g) {
+        const bool cs = j < t.nc;
+        const int64_t key0 = dq_key0(t, j);
+        const bool full = cs ? tile_full(key0, QBN, t.q.c_all_lo, t.q.c_all_hi, p.g.L)
+                             : tile_full(key0, QBN, t.q.n_all_lo, t.q.n_all_hi, p.g.L);
+        const int b = g & 1;
+        ok = mbar_wait(BAR(DQ_SF + b), (g >> 1) & 1, wd, 30) && mbar_wait(BAR(DQ_DPF), g & 1, wd, 31);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          const uint32_t col = half * 64 + s * 32;
+          uint32_t us[32], ud[32];
+          tmem_ld32x2(tmem + R.tl + b * 128 + col, tmem + R.tl + kColDP + col, us, ud);
+          if (s == 1) {
+            // both dP halves of this warpgroup read: the next dP may land
+            tc_fence_before();
+            mbar_arrive(BAR(DQ_DPFREE));
+          }
+          uint32_t pk[16];
+          if (full) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const float d0 =
+                  ex2_approx(fmaf(__uint_as_float(us[c]), sl2, nlse2)) * (__uint_as_float(ud[c]) - Dv);
+              const float d1 =
+                  ex2_approx(fmaf(__uint_as_float(us[c + 1]), sl2, nlse2)) * (__uint_as_float(ud[c + 1]) - Dv);
+              pk[c / 2] = pack_bf16x2(d0, d1);
+            }
+          } else {
+            const int64_t k0 = key0 + col;
+            const int lo = (int)imax64(imin64((cs ? clo : nlo) - k0, 33), -1);
+            const int hi = (int)imax64(imin64((cs ? chi : nhi) - k0, 33), -1);
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              float d0 = ex2_approx(fmaf(__uint_as_float(us[c]), sl2, nlse2)) * (__uint_as_float(ud[c]) - Dv);
+              float d1 =
+                  ex2_approx(fmaf(__uint_as_float(us[c + 1]), sl2, nlse2)) * (__uint_as_float(ud[c + 1]) - Dv);
+              d0 = (c >= lo && c < hi) ? d0 : 0.f;
+              d1 = (c + 1 >= lo && c + 1 < hi) ? d1 : 0.f;
+              pk[c / 2] = pack_bf16x2(d0, d1);
+            }
+          }
+          // 32 keys of dS as 16 packed columns over S columns this warpgroup
+          // has already read (layout of packed_col128)
+          tmem_st16(tmem + R.tl + b * 128 + half * 64 + s * 16, pk);
+        }
+        tc_fence_before();
+        mbar_arrive(BAR(DQ_DSF + b));
+      }
+      if (!ok) break;
+      ok = mbar_wait(BAR(DQ_DONE), itn & 1, wd, 32);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c4 = 0; c4 < HD / 64; ++c4) {
+        uint32_t u[32];
+        tmem_ld32(tmem + R.tl + kColDQ + half * (HD / 2) + c4 * 32, u);
+        if (valid) store_row32(dqbase, oofs + c4 * 32, u, p.scale, p.g_f32, p.dq_accumulate);
+      }
+      tc_fence_before();
+      mbar_arrive(BAR(DQ_OE));
+      ++itn;
+    }
+  }
+  __syncthreads();
+  if (*abort_flag) drain_after_abort(200);
+  if (R.warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dq_tc(const BwdMaps& m, const BwdParams& p, int num_sms, uint32_t* status,
+                             uint64_t limit_ns, cudaStream_t stream, int* launches) {
+  const int64_t n = q_items(p.g, QBM);
+  if (n == 0) return cudaSuccess;
+  const int grid = (int)(n < num_sms ? n : num_sms);
+  cudaError_t e;
+  if (p.d == 128) {
+    e = cudaFuncSetAttribute(bdlm_bwd_dq_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DqLayout<128>::kAlloc);
+    if (e != cudaSuccess) return e;
+    bdlm_bwd_dq_tc_kernel<128><<<grid, kThreads, DqLayout<128>::kAlloc, stream>>>(
+        m.Qc, m.Qn, m.dOc, m.dOn, m.Kc, m.Kn, m.Vc, m.Vn, p, n, status, limit_ns);
+  } else {
+    e = cudaFuncSetAttribute(bdlm_bwd_dq_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DqLayout<64>::kAlloc);
+    if (e != cudaSuccess) return e;
+    bdlm_bwd_dq_tc_kernel<64><<<grid, kThreads, DqLayout<64>::kAlloc, stream>>>(
+        m.Qc, m.Qn, m.dOc, m.dOn, m.Kc, m.Kn, m.Vc, m.Vn, p, n, status, limit_ns);
+  }
+  if (launches) ++*launches;
+  return cudaGetLastError();
+}
+
+}  // namespace bdlm

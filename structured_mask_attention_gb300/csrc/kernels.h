@@ -48,10 +48,11 @@ struct BwdParams {
   int dq_accumulate; // dQ += contribution (fp32 only)
 };
 
-// Tensor maps of the tensor-core backward: 128-row and 64-row boxes.
+// Tensor maps of the tensor-core backward passes: [L, H, d] bf16 viewed 3-D,
+// 64-column (128-byte) x 128-row boxes, 128-byte swizzle.
+constexpr int kBwdTile = 128;
 struct BwdMaps {
-  CUtensorMap Qc128, Qn128, dOc128, dOn128, Kc64, Kn64, Vc64, Vn64;  // dQ pass
-  CUtensorMap Qc64, Qn64, dOc64, dOn64, Kc128, Kn128, Vc128, Vn128;  // dK/dV pass
+  CUtensorMap Qc, Qn, dOc, dOn, Kc, Kn, Vc, Vn;
 };
 cudaError_t launch_bwd_dq_tc(const BwdMaps& m, const BwdParams& p, int num_sms, uint32_t* status,
                              uint64_t limit_ns, cudaStream_t stream, int* launches);
