@@ -254,7 +254,7 @@ bdlm_status fwd_common(const void* Qc, const void* Kc, const void* Vc, const voi
   p.o_f32 = o_f32;
   p.LSEc = LSEc;
   p.LSEn = LSEn;
-  p.n_items = q_items(p.g, kFwdTileQ);
+  p.n_items = q_items(p.g, kFwdItemRows);
   p.status = static_cast<uint32_t*>(ws);
   p.limit_ns = wait_limit_ns();
   BDLM_CHECK(clear_status(ws, st));

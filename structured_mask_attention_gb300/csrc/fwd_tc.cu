@@ -9,27 +9,29 @@
 // (clean keys restricted to [kv_begin, kv_end), corrupted own block optional:
 // CSBP, evolve.pub FAQ), writing O = 0, LSE = -inf for rows with no key.
 //
-// Design (one CTA per SM, persistent; 10 warps).  A CTA works on a PAIR of
-// 128-row query tiles at once: the clean and the corrupted tile of the same
-// head and position (equal work: both see (b+1)B keys per row).  Keys come in
-// steps of 64.  Each tile has its own Q slot, two K and two V slots in shared
-// memory, and in TMEM two 64-column S buffers and its O accumulator:
-//   warp 0      TMA producer (K of a step as soon as the S MMA two steps
-//               back released its slot, V likewise after the PV MMA);
-//   warp 1      owns TMEM (512 columns); one lane issues tcgen05.mma: per
-//               step, S(j) = Q K^T(j) of both tiles into the free S buffers,
-//               then PV(j-1) of both tiles, so every tile's softmax of step j
-//               overlaps its own S(j+1) and the other tile's MMAs;
-//   warps 2-5   softmax warpgroup of tile 0, warps 6-9 of tile 1: one query
-//               row per thread, online softmax in the log2 domain with a lazy
+// Design (one CTA per SM, persistent; 10 warps).  An item is 256 consecutive
+// query rows of one stream and head, split into two 128-row sub-tiles that
+// share every key tile (rows of one block see the same keys), so each
+// 128-key K/V tile is loaded once for both:
+//   warp 0      TMA producer: Q of both sub-tiles, then K and V tiles through
+//               two 2-stage rings;
+//   warp 1      owns TMEM (512 columns: S of sub-tile t at 128 t, O of
+//               sub-tile t at 256 + 128 t); one lane issues tcgen05.mma in the
+//               order S0(j), S1(j), PV0(j), S0(j+1), PV1(j), S1(j+1), ... so
+//               the tensor pipe works on one sub-tile while the other one's
+//               softmax runs;
+//   warps 2-5   softmax of sub-tile 0, warps 6-9 of sub-tile 1: one query row
+//               per thread, online softmax in the log2 domain with a lazy
 //               rescale (the reference max moves only when the row max grows
-//               by more than 8), P written back over the S buffer in TMEM as
-//               packed bf16 and consumed from there by the PV MMA (A operand
-//               in TMEM).  The S MMA that next reuses a buffer is issued after
-//               the PV MMA that reads its P (the tensor pipe runs in issue
-//               order).
-// Only key tiles some row of the query tile can see are visited; a per-row
-// interval test masks the tiles that are not fully visible.
+//               by more than 8), P written back over S in TMEM as packed bf16
+//               and read from there by the PV MMA (A operand in TMEM).  The S
+//               MMA that next overwrites a sub-tile's S is issued after the PV
+//               MMA that reads its P (the tensor pipe runs in issue order), and
+//               its completion implies that PV's, so the softmax may rescale O
+//               right after S lands.
+// Every MMA is M = 128, N = 128 (N = d for PV).  Only key tiles some row of
+// the item can see are visited; a per-row interval test masks the tiles that
+// are not fully visible.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -38,26 +40,25 @@
 namespace bdlm {
 namespace {
 
-constexpr int BM = kFwdTileQ;   // query rows per tile
-constexpr int BN = kFwdTileK;   // keys per step (64)
+constexpr int BM = kFwdTileQ;      // query rows per sub-tile (128)
+constexpr int BI = kFwdItemRows;   // query rows per item (256)
+constexpr int BN = kFwdTileK;      // keys per step (128)
 constexpr int kThreads = 320;
-constexpr int kQPanel = BM * 128;  // 128 rows x 128 bytes (64 bf16)
-constexpr int kKPanel = BN * 128;  // 64 rows x 128 bytes
+constexpr int kPanel = 128 * 128;  // 128 rows x 128 bytes (64 bf16)
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// barrier slots per tile (tile t adds t * B_PER_TILE)
-enum { B_QF = 0, B_QE = 1, B_KF = 2, B_KE = 4, B_VF = 6, B_VE = 8, B_SF = 10, B_PF = 12, B_PVD = 13, B_OE = 14,
-       B_PER_TILE = 15, B_COUNT = 30 };
+enum { B_QF = 0, B_QE = 1, B_KF = 2, B_KE = 4, B_VF = 6, B_VE = 8, B_SF = 10, B_PF = 12, B_OD = 14, B_OE = 16,
+       B_COUNT = 18 };
 
 template <int HD>
 struct Layout {
-  static constexpr int kQBytes = BM * HD * 2;  // 128 rows x HD bf16
-  static constexpr int kKBytes = BN * HD * 2;  // 64 rows x HD bf16
-  // per tile t at t * kTile: Q, K[2], V[2]
-  static constexpr int kTile = kQBytes + 4 * kKBytes;
-  static constexpr int kBar = 2 * kTile;
-  static constexpr int kBytes = kBar + 512;
+  static constexpr int kTile = 128 * HD * 2;  // 128 rows x HD bf16 (Q sub-tile, K, V alike)
+  static constexpr int kQ = 0;                // Q of sub-tiles 0, 1
+  static constexpr int kK = 2 * kTile;        // K stages 0, 1
+  static constexpr int kV = 4 * kTile;        // V stages 0, 1
+  static constexpr int kBar = 6 * kTile;
+  static constexpr int kBytes = kBar + 256;
   // 1024 bytes of slack for alignment; never below 120 KB so that a second
   // CTA cannot share the SM (each CTA holds all 512 TMEM columns).
   static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
@@ -67,17 +68,17 @@ struct ItemGeo {
   int stream, head, kvh;
   int64_t r0;
   QTileRanges q;
-  int nc, n;  // clean tiles, total tiles
+  int nc, n;  // clean key tiles, all key tiles
 };
 
 __device__ __forceinline__ ItemGeo item_geo(const FwdParams& p, int64_t idx) {
   ItemGeo t;
-  const QItem it = q_item(p.g, BM, idx);
+  const QItem it = q_item(p.g, BI, idx);
   t.stream = it.stream;
   t.head = it.head;
   t.kvh = it.head / (p.g.Hq / p.g.Hkv);
-  t.r0 = it.qtile * BM;
-  const int64_t r1 = imin64(t.r0 + BM, p.g.L);
+  t.r0 = it.qtile * BI;
+  const int64_t r1 = imin64(t.r0 + BI, p.g.L);
   t.q = qtile_ranges(p.g, t.stream, t.r0, r1, BN);
   t.nc = (int)(t.q.c1 - t.q.c0);
   t.n = t.nc + (int)(t.q.n1 - t.q.n0);
@@ -87,6 +88,10 @@ __device__ __forceinline__ ItemGeo item_geo(const FwdParams& p, int64_t idx) {
 __device__ __forceinline__ int64_t tile_key0(const ItemGeo& t, int j) {
   return (j < t.nc ? t.q.c0 + j : t.q.n0 + (j - t.nc)) * BN;
 }
+
+// P is stored as packed bf16 over the first 64 S columns, two keys per
+// column in key order; the 16 keys of PV K-step kk start at column 8 kk.
+__device__ __forceinline__ uint32_t p_col(int kk) { return (uint32_t)(kk * 8); }
 
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -99,32 +104,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw_u32);
-  auto sQ = [&](int t) -> uint32_t { return base + t * LY::kTile; };
-  auto sK = [&](int t, int st) -> uint32_t { return base + t * LY::kTile + LY::kQBytes + st * LY::kKBytes; };
-  auto sV = [&](int t, int st) -> uint32_t {
-    return base + t * LY::kTile + LY::kQBytes + (2 + st) * LY::kKBytes;
-  };
+  const uint32_t sQ = base + LY::kQ, sK = base + LY::kK, sV = base + LY::kV;
   const uint32_t bars = base + LY::kBar;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + LY::kBar + 8 * B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + LY::kBar + 8 * B_COUNT + 4);
-  auto BAR = [&](int i, int t) -> uint32_t { return bars + 8u * (uint32_t)(i + t * B_PER_TILE); };
+  auto BAR = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(BAR(B_QF, t), 1);
-      mbar_init(BAR(B_QE, t), 1);
-      for (int st = 0; st < 2; ++st) {
-        mbar_init(BAR(B_KF + st, t), 1);
-        mbar_init(BAR(B_KE + st, t), 1);
-        mbar_init(BAR(B_VF + st, t), 1);
-        mbar_init(BAR(B_VE + st, t), 1);
-        mbar_init(BAR(B_SF + st, t), 1);
-      }
-      mbar_init(BAR(B_PF, t), 128);
-      mbar_init(BAR(B_PVD, t), 1);
-      mbar_init(BAR(B_OE, t), 128);
+    mbar_init(BAR(B_QF), 1);
+    mbar_init(BAR(B_QE), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(BAR(B_KF + s), 1);
+      mbar_init(BAR(B_KE + s), 1);
+      mbar_init(BAR(B_VF + s), 1);
+      mbar_init(BAR(B_VE + s), 1);
+      mbar_init(BAR(B_SF + s), 1);
+      mbar_init(BAR(B_PF + s), 128);
+      mbar_init(BAR(B_OD + s), 1);
+      mbar_init(BAR(B_OE + s), 128);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -139,148 +138,130 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const Watchdog wd{p.status, p.limit_ns, abort_flag};
   const int grid = gridDim.x, cta = blockIdx.x;
-  const int64_t n_pairs = p.n_items / 2;  // items 2i, 2i+1: clean and corrupted tile of one head/position
-  // TMEM columns: S buffers of tile t at 128 t + {0, 64} (P over their first
-  // 32 columns), O of tile t at 256 + 128 t
+  const int64_t n_items = p.n_items;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tQc); tma_prefetch_desc(&tQn); tma_prefetch_desc(&tKc);
       tma_prefetch_desc(&tKn); tma_prefetch_desc(&tVc); tma_prefetch_desc(&tVn);
-      uint32_t qc[2] = {0, 0}, kc[2] = {0, 0}, vc[2] = {0, 0};
+      uint32_t itn = 0, kc = 0;
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
-        const int64_t pi = snake_item(rnd, cta, grid);
-        if (pi >= n_pairs) break;
-        const ItemGeo g0 = item_geo(p, 2 * pi), g1 = item_geo(p, 2 * pi + 1);
-        const int nmax = g0.n > g1.n ? g0.n : g1.n;
+        const int64_t idx = snake_item(rnd, cta, grid);
+        if (idx >= n_items) break;
+        const ItemGeo g = item_geo(p, idx);
+        if (g.n == 0) continue;
+        if (itn > 0 && !mbar_wait(BAR(B_QE), (itn - 1) & 1, wd, 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(BAR(B_QF), 2 * LY::kTile);
+        const CUtensorMap* mq = g.stream ? &tQn : &tQc;
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const ItemGeo& g = t ? g1 : g0;
-          if (g.n == 0 || !ok) continue;
-          if (qc[t] > 0 && !mbar_wait(BAR(B_QE, t), (qc[t] - 1) & 1, wd, 1)) { ok = false; continue; }
-          mbar_arrive_expect_tx(BAR(B_QF, t), LY::kQBytes);
-          const CUtensorMap* mq = g.stream ? &tQn : &tQc;
+        for (int t = 0; t < 2; ++t)
 #pragma unroll
           for (int pn = 0; pn < HD / 64; ++pn)
-            tma_load_3d(sQ(t) + pn * kQPanel, mq, BAR(B_QF, t), pn * 64, g.head, (int)g.r0);
-          ++qc[t];
-        }
-        for (int j = 0; j < nmax && ok; ++j) {
+            tma_load_3d(sQ + t * LY::kTile + pn * kPanel, mq, BAR(B_QF), pn * 64, g.head, (int)(g.r0 + t * BM));
+        ++itn;
+        for (int j = 0; j < g.n; ++j, ++kc) {
+          const int st = kc & 1;
+          const bool cs = j < g.nc;
+          const int key0 = (int)tile_key0(g, j);
+          if (kc >= 2 && !mbar_wait(BAR(B_KE + st), ((kc >> 1) - 1) & 1, wd, 2)) { ok = false; break; }
+          mbar_arrive_expect_tx(BAR(B_KF + st), LY::kTile);
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const ItemGeo& g = t ? g1 : g0;
-            if (j >= g.n || !ok) continue;
-            const uint32_t k = kc[t];
-            const int st = k & 1;
-            if (k >= 2 && !mbar_wait(BAR(B_KE + st, t), ((k >> 1) - 1) & 1, wd, 2)) { ok = false; continue; }
-            const CUtensorMap* mk = j < g.nc ? &tKc : &tKn;
-            mbar_arrive_expect_tx(BAR(B_KF + st, t), LY::kKBytes);
+          for (int pn = 0; pn < HD / 64; ++pn)
+            tma_load_3d(sK + st * LY::kTile + pn * kPanel, cs ? &tKc : &tKn, BAR(B_KF + st), pn * 64, g.kvh, key0);
+          if (kc >= 2 && !mbar_wait(BAR(B_VE + st), ((kc >> 1) - 1) & 1, wd, 3)) { ok = false; break; }
+          mbar_arrive_expect_tx(BAR(B_VF + st), LY::kTile);
 #pragma unroll
-            for (int pn = 0; pn < HD / 64; ++pn)
-              tma_load_3d(sK(t, st) + pn * kKPanel, mk, BAR(B_KF + st, t), pn * 64, g.kvh, (int)tile_key0(g, j));
-            ++kc[t];
-          }
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const ItemGeo& g = t ? g1 : g0;
-            if (j >= g.n || !ok) continue;
-            const uint32_t v = vc[t];
-            const int st = v & 1;
-            if (v >= 2 && !mbar_wait(BAR(B_VE + st, t), ((v >> 1) - 1) & 1, wd, 3)) { ok = false; continue; }
-            const CUtensorMap* mv = j < g.nc ? &tVc : &tVn;
-            mbar_arrive_expect_tx(BAR(B_VF + st, t), LY::kKBytes);
-#pragma unroll
-            for (int pn = 0; pn < HD / 64; ++pn)
-              tma_load_3d(sV(t, st) + pn * kKPanel, mv, BAR(B_VF + st, t), pn * 64, g.kvh, (int)tile_key0(g, j));
-            ++vc[t];
-          }
+          for (int pn = 0; pn < HD / 64; ++pn)
+            tma_load_3d(sV + st * LY::kTile + pn * kPanel, cs ? &tVc : &tVn, BAR(B_VF + st), pn * 64, g.kvh, key0);
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdescS = idesc_bf16(BM, BN, false, false);
-      constexpr uint32_t kIdescO = idesc_bf16(BM, HD, false, true);
-      uint32_t qc[2] = {0, 0}, kc[2] = {0, 0}, vc[2] = {0, 0}, oc[2] = {0, 0};
+      constexpr uint32_t kIdS = idesc_bf16(BM, BN, false, false);
+      constexpr uint32_t kIdO = idesc_bf16(BM, HD, false, true);
+      const uint64_t dq[2] = {sdesc_sw128(sQ, 16, 1024), sdesc_sw128(sQ + LY::kTile, 16, 1024)};
+      // S_t(k) = Q_t K(k)^T into the S columns of sub-tile t
+      auto issue_s = [&](int t, uint32_t k) {
+        const uint64_t dk0 = sdesc_sw128(sK + (k & 1) * LY::kTile, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+          tc_mma_ss(tmem + t * 128, desc_add(dq[t], off), desc_add(dk0, off), kIdS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(BAR(B_SF + t));
+      };
+      // O_t += P_t(k) V(k), P_t packed bf16 over the S columns
+      auto issue_pv = [&](int t, uint32_t k, bool first) {
+        const uint64_t dv0 = sdesc_sw128(sV + (k & 1) * LY::kTile, kPanel, 1024);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          tc_mma_ts(tmem + 256 + t * 128, tmem + t * 128 + p_col(kk), desc_add(dv0, kk * 2048), kIdO,
+                    (kk > 0 || !first) ? 1u : 0u);
+      };
+      uint32_t itn = 0, kc = 0;
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
-        const int64_t pi = snake_item(rnd, cta, grid);
-        if (pi >= n_pairs) break;
-        const ItemGeo g0 = item_geo(p, 2 * pi), g1 = item_geo(p, 2 * pi + 1);
-        const int nmax = g0.n > g1.n ? g0.n : g1.n;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const ItemGeo& g = t ? g1 : g0;
-          if (g.n == 0 || !ok) continue;
-          if (!mbar_wait(BAR(B_QF, t), qc[t] & 1, wd, 4)) { ok = false; continue; }
-          ++qc[t];
-        }
-        for (int j = 0; j <= nmax && ok; ++j) {
-          // S(j) of both tiles: buffer (S count & 1); its previous P was read
-          // by the PV MMA issued one iteration earlier
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const ItemGeo& g = t ? g1 : g0;
-            if (j >= g.n || !ok) continue;
-            const uint32_t k = kc[t];
-            const int st = k & 1;
-            if (!mbar_wait(BAR(B_KF + st, t), (k >> 1) & 1, wd, 8)) { ok = false; continue; }
+        const int64_t idx = snake_item(rnd, cta, grid);
+        if (idx >= n_items) break;
+        const ItemGeo g = item_geo(p, idx);
+        if (g.n == 0) continue;
+        if (!mbar_wait(BAR(B_QF), itn & 1, wd, 4)) { ok = false; break; }
+        if (!mbar_wait(BAR(B_KF + (kc & 1)), (kc >> 1) & 1, wd, 5)) { ok = false; break; }
+        tc_fence_after();
+        issue_s(0, kc);
+        issue_s(1, kc);
+        tc_commit(BAR(B_KE + (kc & 1)));
+        if (g.n == 1) tc_commit(BAR(B_QE));
+        for (int j = 0; j < g.n; ++j) {
+          const uint32_t k = kc + j;
+          const bool last = j == g.n - 1;
+          // PV0(j), then S0(j+1) over P0(j)
+          if (!mbar_wait(BAR(B_PF + 0), k & 1, wd, 6)) { ok = false; break; }
+          if (j == 0 && itn > 0 && !mbar_wait(BAR(B_OE + 0), (itn - 1) & 1, wd, 7)) { ok = false; break; }
+          if (!mbar_wait(BAR(B_VF + (k & 1)), (k >> 1) & 1, wd, 8)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(0, k, j == 0);
+          if (last) tc_commit(BAR(B_OD + 0));
+          if (!last) {
+            if (!mbar_wait(BAR(B_KF + ((k + 1) & 1)), ((k + 1) >> 1) & 1, wd, 9)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t tS = tmem + t * 128 + st * BN;
-            const uint64_t dq0 = sdesc_sw128(sQ(t), 16, 1024), dk0 = sdesc_sw128(sK(t, st), 16, 1024);
-#pragma unroll
-            for (int kk = 0; kk < HD / 16; ++kk) {
-              const uint32_t qo = (kk >> 2) * kQPanel + (kk & 3) * 32;
-              const uint32_t ko = (kk >> 2) * kKPanel + (kk & 3) * 32;
-              tc_mma_ss(tS, desc_add(dq0, qo), desc_add(dk0, ko), kIdescS, kk > 0 ? 1u : 0u);
-            }
-            tc_commit(BAR(B_SF + st, t));
-            tc_commit(BAR(B_KE + st, t));
-            if (j == g.n - 1) tc_commit(BAR(B_QE, t));
-            ++kc[t];
+            issue_s(0, k + 1);
           }
-          // PV(j-1) of both tiles: O += P V, P (bf16) in TMEM over its S buffer
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const ItemGeo& g = t ? g1 : g0;
-            if (j < 1 || j > g.n || !ok) continue;
-            const uint32_t v = vc[t];
-            const int st = v & 1;
-            if (!mbar_wait(BAR(B_PF, t), v & 1, wd, 5)) { ok = false; continue; }
-            if (j == 1 && oc[t] > 0 && !mbar_wait(BAR(B_OE, t), (oc[t] - 1) & 1, wd, 6)) { ok = false; continue; }
-            if (!mbar_wait(BAR(B_VF + st, t), (v >> 1) & 1, wd, 7)) { ok = false; continue; }
-            tc_fence_after();
-            const uint32_t tP = tmem + t * 128 + st * BN, tO = tmem + 256 + t * 128;
-            const uint64_t dv0 = sdesc_sw128(sV(t, st), kKPanel, 1024);
-            const uint32_t acc0 = j > 1 ? 1u : 0u;
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              tc_mma_ts(tO, tP + kk * 8, desc_add(dv0, kk * 2048), kIdescO, kk > 0 ? 1u : acc0);
-            tc_commit(BAR(B_VE + st, t));
-            tc_commit(BAR(B_PVD, t));
-            ++vc[t];
-            if (j == g.n) ++oc[t];
+          // PV1(j), then S1(j+1) over P1(j)
+          if (!mbar_wait(BAR(B_PF + 1), k & 1, wd, 10)) { ok = false; break; }
+          if (j == 0 && itn > 0 && !mbar_wait(BAR(B_OE + 1), (itn - 1) & 1, wd, 11)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(1, k, j == 0);
+          tc_commit(BAR(B_VE + (k & 1)));
+          if (last) tc_commit(BAR(B_OD + 1));
+          if (!last) {
+            issue_s(1, k + 1);
+            tc_commit(BAR(B_KE + ((k + 1) & 1)));
+            if (j + 1 == g.n - 1) tc_commit(BAR(B_QE));
           }
         }
+        kc += g.n;
+        ++itn;
       }
     }
   } else {
-    // ------------------------------------------------------------ softmax (thread = row of tile t)
+    // ------------------------------------------------------------ softmax (thread = row of sub-tile t)
     const int t = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t tl = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tO = tmem + tl + 256 + t * 128;
-    uint32_t sc = 0;
+    const uint32_t tS = tmem + tl + t * 128, tO = tmem + tl + 256 + t * 128;
+    uint32_t sc = 0, itn = 0;
     bool ok = true;
     for (int64_t rnd = 0; ok; ++rnd) {
-      const int64_t pi = snake_item(rnd, cta, grid);
-      if (pi >= n_pairs) break;
-      const ItemGeo g = item_geo(p, 2 * pi + t);
-      const int64_t r = g.r0 + row;
+      const int64_t idx = snake_item(rnd, cta, grid);
+      if (idx >= n_items) break;
+      const ItemGeo g = item_geo(p, idx);
+      const int64_t r = g.r0 + t * BM + row;
       const bool valid = r < p.g.L;
       float* lse_out = (g.stream ? p.LSEn : p.LSEc) + (int64_t)g.head * p.g.L;
       void* obase = g.stream ? p.On : p.Oc;
@@ -300,39 +281,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      const int64_t rr = valid ? r : p.g.L - 1;
-      int64_t clo, chi, nlo, nhi;
-      clean_interval(p.g, g.stream, rr, clo, chi);
-      noisy_interval(p.g, g.stream, rr, nlo, nhi);
+      // loop state in 32-bit (rows and keys are TMA coordinates, < 2^31):
+      // key tile ranges, keys every row of the item sees (clipped to L), and
+      // this row's visible key intervals
+      int lo_c, hi_c, lo_n, hi_n;
+      {
+        const int64_t rr = valid ? r : p.g.L - 1;
+        int64_t a0, a1, b0, b1;
+        clean_interval(p.g, g.stream, rr, a0, a1);
+        noisy_interval(p.g, g.stream, rr, b0, b1);
+        lo_c = (int)a0; hi_c = (int)a1; lo_n = (int)b0; hi_n = (int)b1;
+      }
+      const int nc = g.nc, n = g.n, c0 = (int)g.q.c0, n0 = (int)g.q.n0;
+      const int call_lo = (int)g.q.c_all_lo, call_hi = (int)imin64(g.q.c_all_hi, p.g.L);
+      const int nall_lo = (int)g.q.n_all_lo, nall_hi = (int)imin64(g.q.n_all_hi, p.g.L);
       const float sl2 = p.scale_log2;
       float m_ref = -INFINITY, l = 0.f;
-      for (int j = 0; j < g.n; ++j, ++sc) {
-        const bool cs = j < g.nc;
-        const int64_t key0 = tile_key0(g, j);
-        const bool full = cs ? tile_full(key0, BN, g.q.c_all_lo, g.q.c_all_hi, p.g.L)
-                             : tile_full(key0, BN, g.q.n_all_lo, g.q.n_all_hi, p.g.L);
-        const int sb = sc & 1;
-        ok = mbar_wait(BAR(B_SF + sb, t), (sc >> 1) & 1, wd, 9);
+      for (int j = 0; j < n; ++j, ++sc) {
+        const bool cs = j < nc;
+        const int key0 = (cs ? c0 + j : n0 + (j - nc)) * BN;
+        const bool full = cs ? (key0 >= call_lo && key0 + BN <= call_hi) : (key0 >= nall_lo && key0 + BN <= nall_hi);
+        ok = mbar_wait(BAR(B_SF + t), sc & 1, wd, 12);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t tS = tmem + tl + t * 128 + sb * BN;
-        uint32_t a[32], b[32];
-        tmem_ld32x2(tS, tS + 32, a, b);
-        float mx = -INFINITY;
-        if (full) {
+        // the whole 128-key row of S in registers
+        uint32_t s[4][32];
+        tmem_ld32x2(tS, tS + 32, s[0], s[1]);
+        tmem_ld32x2(tS + 64, tS + 96, s[2], s[3]);
+        if (!full) {
+          const int lo = max(min((cs ? lo_c : lo_n) - key0, BN + 1), -1);
+          const int hi = max(min((cs ? hi_c : hi_n) - key0, BN + 1), -1);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) mx = fmaxf(mx, fmaxf(__uint_as_float(a[c]), __uint_as_float(b[c])));
-        } else {
-          const int lo = (int)imax64(imin64((cs ? clo : nlo) - key0, BN + 1), -1);
-          const int hi = (int)imax64(imin64((cs ? chi : nhi) - key0, BN + 1), -1);
+          for (int q = 0; q < 4; ++q)
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            if (c < lo || c >= hi) a[c] = __float_as_uint(-INFINITY);
-            if (c + 32 < lo || c + 32 >= hi) b[c] = __float_as_uint(-INFINITY);
-            mx = fmaxf(mx, fmaxf(__uint_as_float(a[c]), __uint_as_float(b[c])));
-          }
+            for (int c = 0; c < 32; ++c)
+              if (q * 32 + c < lo || q * 32 + c >= hi) s[q][c] = __float_as_uint(-INFINITY);
         }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          mx = fmaxf(mx, fmaxf(fmaxf(__uint_as_float(s[0][c]), __uint_as_float(s[1][c])),
+                               fmaxf(__uint_as_float(s[2][c]), __uint_as_float(s[3][c]))));
         const float mx2 = mx * sl2;
         bool rescale = false;
         float alpha = 1.f, m_use = m_ref;
@@ -344,46 +334,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = true;
         }
         const float nm = (m_use == -INFINITY) ? 0.f : -m_use;
-        // P = exp2(s c - m) (masked entries are -inf -> 0), row sum, and P as
-        // packed bf16 over the first 32 columns of this S buffer
-        float rs0 = 0.f, rs1 = 0.f;
-        uint32_t pk[32];
+        // P = exp2(s c - m) (masked entries are -inf -> 0), its row sum, and P
+        // as packed bf16 over the first 64 S columns (layout of p_col)
+        float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(a[c]), sl2, nm));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(a[c + 1]), sl2, nm));
-          const float q0 = ex2_approx(fmaf(__uint_as_float(b[c]), sl2, nm));
-          const float q1 = ex2_approx(fmaf(__uint_as_float(b[c + 1]), sl2, nm));
-          rs0 += p0 + p1;
-          rs1 += q0 + q1;
-          pk[c / 2] = pack_bf16x2(p0, p1);
-          pk[16 + c / 2] = pack_bf16x2(q0, q1);
+        for (int q = 0; q < 4; ++q) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(s[q][c]), sl2, nm));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(s[q][c + 1]), sl2, nm));
+            rs[q] += p0 + p1;
+            pk[c / 2] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tS + q * 16, pk);
         }
-        tmem_st32(tS, pk);
-        l = l * alpha + (rs0 + rs1);
+        l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
         m_ref = m_use;
-        if (j > 0) {
-          // PV(j-1) must be complete before O is rescaled
-          ok = mbar_wait(BAR(B_PVD, t), (sc - 1) & 1, wd, 10);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, rescale)) {
+        // O is complete up to step j-1 (S_t(j) was issued after PV_t(j-1))
+        if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-            for (int c4 = 0; c4 < HD / 32; ++c4) {
-              uint32_t o[32];
-              tmem_ld32(tO + c4 * 32, o);
+          for (int c4 = 0; c4 < HD / 32; ++c4) {
+            uint32_t o[32];
+            tmem_ld32(tO + c4 * 32, o);
 #pragma unroll
-              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-              tmem_st32(tO + c4 * 32, o);
-            }
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st32(tO + c4 * 32, o);
           }
         }
         tc_fence_before();
-        mbar_arrive(BAR(B_PF, t));
+        mbar_arrive(BAR(B_PF + t));
       }
       if (!ok) break;
-      ok = mbar_wait(BAR(B_PVD, t), (sc - 1) & 1, wd, 11);
+      ok = mbar_wait(BAR(B_OD + t), itn & 1, wd, 13);
+      const ItemGeo ge = item_geo(p, idx);
+      const int64_t re = ge.r0 + t * BM + row;
+      const bool ve = re < p.g.L;
+      float* lse_e = (ge.stream ? p.LSEn : p.LSEc) + (int64_t)ge.head * p.g.L;
+      void* obase_e = ge.stream ? p.On : p.Oc;
+      const int64_t oofs_e = (re * p.g.Hq + ge.head) * HD;
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -392,9 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c4 = 0; c4 < HD / 64; ++c4) {
         uint32_t a[32], b[32];
         tmem_ld32x2(tO + c4 * 64, tO + c4 * 64 + 32, a, b);
-        if (valid) {
+        if (ve) {
           if (p.o_f32) {
-            float4* o = reinterpret_cast<float4*>(static_cast<float*>(obase) + oofs + c4 * 64);
+            float4* o = reinterpret_cast<float4*>(static_cast<float*>(obase_e) + oofs_e + c4 * 64);
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               o[c] = make_float4(__uint_as_float(a[4 * c]) * inv, __uint_as_float(a[4 * c + 1]) * inv,
@@ -403,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      __uint_as_float(b[4 * c + 2]) * inv, __uint_as_float(b[4 * c + 3]) * inv);
             }
           } else {
-            uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(obase) + oofs + c4 * 64);
+            uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(obase_e) + oofs_e + c4 * 64);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               o[c] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * c + 0]) * inv, __uint_as_float(a[8 * c + 1]) * inv),
@@ -420,8 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(BAR(B_OE, t));
-      if (valid) lse_out[r] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      mbar_arrive(BAR(B_OE + t));
+      if (ve) lse_e[re] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      ++itn;
     }
   }
 
@@ -437,8 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, int d, int num_sms, cudaStream_t stream,
                        int* launches) {
-  const int64_t n_pairs = p.n_items / 2;
-  const int64_t grid64 = n_pairs < num_sms ? n_pairs : num_sms;
+  const int64_t grid64 = p.n_items < num_sms ? p.n_items : num_sms;
   const int grid = (int)(grid64 > 0 ? grid64 : 1);
   cudaError_t e;
   if (d == 128) {

@@ -28,9 +28,11 @@ struct FwdMaps {
   CUtensorMap Qc, Qn, Kc, Kn, Vc, Vn;
 };
 
-// Tile sizes of the tensor-core forward: 128 query rows x 64 keys per step.
+// Tile sizes of the tensor-core forward: items of 256 query rows (two
+// 128-row sub-tiles sharing their key tiles), 128 keys per step.
 constexpr int kFwdTileQ = 128;
-constexpr int kFwdTileK = 64;
+constexpr int kFwdItemRows = 256;
+constexpr int kFwdTileK = 128;
 
 cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, int d, int num_sms, cudaStream_t stream,
                        int* launches);
