@@ -89,9 +89,60 @@ __device__ __forceinline__ int64_t tile_key0(const ItemGeo& t, int j) {
   return (j < t.nc ? t.q.c0 + j : t.q.n0 + (j - t.nc)) * BN;
 }
 
-// P is stored as packed bf16 over the first 64 S columns, two keys per
-// column in key order; the 16 keys of PV K-step kk start at column 8 kk.
-__device__ __forceinline__ uint32_t p_col(int kk) { return (uint32_t)(kk * 8); }
+// P is stored as packed bf16 over the S columns it replaces: keys [64, 128)
+// (held in registers since the row-max pass) at columns [64, 96), keys
+// [0, 64) (loaded again) at columns [0, 32).  The 16 keys of PV K-step kk
+// start at column
+__device__ __forceinline__ uint32_t p_col(int kk) { return (uint32_t)(kk * 8 + (kk >= 4 ? 32 : 0)); }
+
+// max of 64 scores: a tree of 3-input maxima (32 instructions)
+__device__ __forceinline__ float max64(const uint32_t (&a)[32], const uint32_t (&b)[32]) {
+  float u[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c)
+    u[c] = fmax3(__uint_as_float(a[2 * c]), __uint_as_float(a[2 * c + 1]), __uint_as_float(b[c]));
+#pragma unroll
+  for (int c = 0; c < 8; ++c) u[c] = fmax3(u[2 * c], u[2 * c + 1], __uint_as_float(b[16 + c]));
+#pragma unroll
+  for (int c = 0; c < 4; ++c) u[c] = fmax3(u[2 * c], u[2 * c + 1], __uint_as_float(b[24 + c]));
+#pragma unroll
+  for (int c = 0; c < 2; ++c) u[c] = fmax3(u[2 * c], u[2 * c + 1], __uint_as_float(b[28 + c]));
+  return fmax3(u[0], u[1], fmaxf(__uint_as_float(b[30]), __uint_as_float(b[31])));
+}
+
+// Scores outside [lo, hi) (key offsets within the step) become -inf.
+__device__ __forceinline__ void mask64(uint32_t (&a)[32], uint32_t (&b)[32], int off, int lo, int hi) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    if (off + c < lo || off + c >= hi) a[c] = __float_as_uint(-INFINITY);
+    if (off + 32 + c < lo || off + 32 + c >= hi) b[c] = __float_as_uint(-INFINITY);
+  }
+}
+
+// P = exp2(s sl2 - m) of 32 scores (masked -inf -> 0), stored as 16 packed
+// bf16 columns at taddr; returns the partial row sums of even and odd keys.
+// The fma runs on packed fp32 pairs (half the issue slots of scalar code).
+__device__ __forceinline__ uint64_t exp_store32(const uint32_t (&a)[32], uint64_t sl2x2, uint64_t nm2,
+                                                uint32_t taddr) {
+  uint32_t pk[16];
+  float r0 = 0.f, r1 = 0.f;
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    float x0, x1;
+    f2_split(f2_fma(f2(__uint_as_float(a[c]), __uint_as_float(a[c + 1])), sl2x2, nm2), x0, x1);
+    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    r0 += p0; r1 += p1;
+    pk[c / 2] = pack_bf16x2(p0, p1);
+  }
+  tmem_st16(taddr, pk);
+  return f2(r0, r1);
+}
+// The same for 64 scores (two 32-key halves).
+__device__ __forceinline__ uint64_t exp_store64(const uint32_t (&a)[32], const uint32_t (&b)[32], uint64_t sl2x2,
+                                                uint64_t nm2, uint32_t taddr) {
+  const uint64_t r = exp_store32(a, sl2x2, nm2, taddr);
+  return f2_add(r, exp_store32(b, sl2x2, nm2, taddr + 16));
+}
 
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -305,24 +356,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        // the whole 128-key row of S in registers
-        uint32_t s[4][32];
-        tmem_ld32x2(tS, tS + 32, s[0], s[1]);
-        tmem_ld32x2(tS + 64, tS + 96, s[2], s[3]);
+        // pass 1, the row max; S of keys [64, 128) stays in registers
+        int lo = -1, hi = BN + 1;
         if (!full) {
-          const int lo = max(min((cs ? lo_c : lo_n) - key0, BN + 1), -1);
-          const int hi = max(min((cs ? hi_c : hi_n) - key0, BN + 1), -1);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-              if (q * 32 + c < lo || q * 32 + c >= hi) s[q][c] = __float_as_uint(-INFINITY);
+          lo = max(min((cs ? lo_c : lo_n) - key0, BN + 1), -1);
+          hi = max(min((cs ? hi_c : hi_n) - key0, BN + 1), -1);
         }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          mx = fmaxf(mx, fmaxf(fmaxf(__uint_as_float(s[0][c]), __uint_as_float(s[1][c])),
-                               fmaxf(__uint_as_float(s[2][c]), __uint_as_float(s[3][c]))));
+        uint32_t a0[32], a1[32], h0[32], h1[32];
+        tmem_ld32x2(tS, tS + 32, a0, a1);
+        if (!full) mask64(a0, a1, 0, lo, hi);
+        const float mx01 = max64(a0, a1);
+        tmem_ld32x2(tS + 64, tS + 96, h0, h1);
+        if (!full) mask64(h0, h1, 64, lo, hi);
+        const float mx = fmaxf(mx01, max64(h0, h1));
         const float mx2 = mx * sl2;
         bool rescale = false;
         float alpha = 1.f, m_use = m_ref;
@@ -334,22 +380,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = true;
         }
         const float nm = (m_use == -INFINITY) ? 0.f : -m_use;
-        // P = exp2(s c - m) (masked entries are -inf -> 0), its row sum, and P
-        // as packed bf16 over the first 64 S columns (layout of p_col)
-        float rs[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(s[q][c]), sl2, nm));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(s[q][c + 1]), sl2, nm));
-            rs[q] += p0 + p1;
-            pk[c / 2] = pack_bf16x2(p0, p1);
-          }
-          tmem_st16(tS + q * 16, pk);
-        }
-        l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+        // P and its row sum: keys [64, 128) from registers, then keys [0, 64)
+        // loaded again (layout of p_col)
+        const uint64_t sl2x2 = f2(sl2, sl2), nm2 = f2(nm, nm);
+        uint64_t rs = exp_store64(h0, h1, sl2x2, nm2, tS + 64);
+        tmem_ld32x2(tS, tS + 32, a0, a1);
+        // (lo, hi made opaque so that the compiler recomputes this mask
+        // instead of keeping the first pass's 64 predicates alive)
+        asm volatile("" : "+r"(lo), "+r"(hi));
+        if (!full) mask64(a0, a1, 0, lo, hi);
+        rs = f2_add(rs, exp_store64(a0, a1, sl2x2, nm2, tS));
+        float r0, r1;
+        f2_split(rs, r0, r1);
+        l = l * alpha + (r0 + r1);
         m_ref = m_use;
         // O is complete up to step j-1 (S_t(j) was issued after PV_t(j-1))
         if (__any_sync(0xffffffffu, rescale)) {
