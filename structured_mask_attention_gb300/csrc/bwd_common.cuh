@@ -71,6 +71,27 @@ __device__ __forceinline__ void store_row32(void* base, int64_t off, const uint3
   }
 }
 
+// dS = exp2(s sl2 + nl) (dP - D) for 32 keys of one query row (nl = -LSE
+// log2 e, nD = -D, both broadcast in packed pairs); keys outside [lo, hi)
+// (offsets within the 32) give 0 unless FULL.  Packed bf16 pairs into pk.
+// fma, add and mul run on packed fp32 pairs.
+template <bool FULL>
+__device__ __forceinline__ void ds_row32(const uint32_t (&us)[32], const uint32_t (&ud)[32], uint64_t sl2x2,
+                                         uint64_t nl2, uint64_t nD2, int lo, int hi, uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    float x0, x1, d0, d1;
+    f2_split(f2_fma(f2(__uint_as_float(us[c]), __uint_as_float(us[c + 1])), sl2x2, nl2), x0, x1);
+    const uint64_t t = f2_add(f2(__uint_as_float(ud[c]), __uint_as_float(ud[c + 1])), nD2);
+    f2_split(f2_mul(f2(ex2_approx(x0), ex2_approx(x1)), t), d0, d1);
+    if (!FULL) {
+      d0 = (c >= lo && c < hi) ? d0 : 0.f;
+      d1 = (c + 1 >= lo && c + 1 < hi) ? d1 : 0.f;
+    }
+    pk[c / 2] = pack_bf16x2(d0, d1);
+  }
+}
+
 // A 128-wide step is read and rewritten in four 32-column quarters: quarter q
 // (warpgroup q / 2, sub-step q % 2) reads fp32 columns [32 q, 32 q + 32) and
 // writes its 16 packed bf16 columns at 32 (q / 2) * 2 + 16 (q % 2), i.e. over

@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = R.row, half = R.half;
     uint32_t itn = 0, qc = 0;
     bool ok = true;
-    const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = f2(p.scale_log2, p.scale_log2), nlog2e = f2(-kLog2e, -kLog2e);
     for (int64_t rnd = 0; ok; ++rnd) {
       const int64_t idx = snake_item(rnd, cta, grid);
       if (idx >= n_items) break;
@@ -356,16 +356,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
             const float4 l4 = *reinterpret_cast<const float4*>(stl + sub * 32 + 4 * c4);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            const uint64_t nlA = f2_mul(f2(l4.x, l4.y), nlog2e), nlB = f2_mul(f2(l4.z, l4.w), nlog2e);
+            const int c = sub * 32 + 4 * c4;
+            float x0, x1, x2, x3;
+            f2_split(f2_fma(f2(__uint_as_float(us[4 * c4]), __uint_as_float(us[4 * c4 + 1])), sl2x2, nlA), x0, x1);
+            f2_split(f2_fma(f2(__uint_as_float(us[4 * c4 + 2]), __uint_as_float(us[4 * c4 + 3])), sl2x2, nlB), x2,
+                     x3);
+            float pe[4] = {ex2_approx(x0), ex2_approx(x1), ex2_approx(x2), ex2_approx(x3)};
+            if (!full) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = sub * 32 + 4 * c4 + e;
-              float pe = ex2_approx(fmaf(__uint_as_float(us[4 * c4 + e]), sl2, -lv[e] * kLog2e));
-              if (!full) pe = (c >= lo && c < hi) ? pe : 0.f;
-              pf[c] = pe;
+              for (int e = 0; e < 4; ++e) pe[e] = (c + e >= lo && c + e < hi) ? pe[e] : 0.f;
             }
-            pk[2 * c4] = pack_bf16x2(pf[sub * 32 + 4 * c4], pf[sub * 32 + 4 * c4 + 1]);
-            pk[2 * c4 + 1] = pack_bf16x2(pf[sub * 32 + 4 * c4 + 2], pf[sub * 32 + 4 * c4 + 3]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pf[c + e] = pe[e];
+            pk[2 * c4] = pack_bf16x2(pe[0], pe[1]);
+            pk[2 * c4 + 1] = pack_bf16x2(pe[2], pe[3]);
           }
           // P^T (bf16) over S^T columns this warpgroup has already read
           tmem_st16(tmem + R.tl + kColS + half * 64 + sub * 16, pk);
@@ -385,10 +390,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c4 = 0; c4 < 8; ++c4) {
             const float4 d4 = *reinterpret_cast<const float4*>(stl + KBN + sub * 32 + 4 * c4);
             const int c = sub * 32 + 4 * c4;
-            dk[2 * c4] = pack_bf16x2(pf[c] * (__uint_as_float(ud[4 * c4]) - d4.x),
-                                     pf[c + 1] * (__uint_as_float(ud[4 * c4 + 1]) - d4.y));
-            dk[2 * c4 + 1] = pack_bf16x2(pf[c + 2] * (__uint_as_float(ud[4 * c4 + 2]) - d4.z),
-                                         pf[c + 3] * (__uint_as_float(ud[4 * c4 + 3]) - d4.w));
+            const uint64_t tA = f2_sub(f2(__uint_as_float(ud[4 * c4]), __uint_as_float(ud[4 * c4 + 1])), f2(d4.x, d4.y));
+            const uint64_t tB =
+                f2_sub(f2(__uint_as_float(ud[4 * c4 + 2]), __uint_as_float(ud[4 * c4 + 3])), f2(d4.z, d4.w));
+            float s0, s1, s2, s3;
+            f2_split(f2_mul(f2(pf[c], pf[c + 1]), tA), s0, s1);
+            f2_split(f2_mul(f2(pf[c + 2], pf[c + 3]), tB), s2, s3);
+            dk[2 * c4] = pack_bf16x2(s0, s1);
+            dk[2 * c4 + 1] = pack_bf16x2(s2, s3);
           }
           // dS^T (bf16) over dP^T columns this warpgroup has already read
           tmem_st16(tmem + R.tl + kColDP + half * 64 + sub * 16, dk);

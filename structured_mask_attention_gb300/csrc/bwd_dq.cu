@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       noisy_interval(p.g, t.stream, rr, nlo, nhi);
       const float nlse2 = valid ? -(t.stream ? p.LSEn : p.LSEc)[(int64_t)t.head * p.g.L + r] * kLog2e : 0.f;
       const float Dv = valid ? (t.stream ? p.Dn : p.Dc)[(int64_t)t.head * p.g.L + r] : 0.f;
-      const float sl2 = p.scale_log2;
+      const uint64_t sl2x2 = f2(p.scale_log2, p.scale_log2), nl2 = f2(nlse2, nlse2), nD2 = f2(-Dv, -Dv);
       for (int j = 0; j < t.n; ++j, ++g) {
         const bool cs = j < t.nc;
         const int64_t key0 = dq_key0(t, j);
@@ -285,29 +285,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(BAR(DQ_DPFREE));
           }
           uint32_t pk[16];
-          if (full) {
-#pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              const float d0 =
-                  ex2_approx(fmaf(__uint_as_float(us[c]), sl2, nlse2)) * (__uint_as_float(ud[c]) - Dv);
-              const float d1 =
-                  ex2_approx(fmaf(__uint_as_float(us[c + 1]), sl2, nlse2)) * (__uint_as_float(ud[c + 1]) - Dv);
-              pk[c / 2] = pack_bf16x2(d0, d1);
-            }
-          } else {
+          int lo = -1, hi = 33;
+          if (!full) {
             const int64_t k0 = key0 + col;
-            const int lo = (int)imax64(imin64((cs ? clo : nlo) - k0, 33), -1);
-            const int hi = (int)imax64(imin64((cs ? chi : nhi) - k0, 33), -1);
-#pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              float d0 = ex2_approx(fmaf(__uint_as_float(us[c]), sl2, nlse2)) * (__uint_as_float(ud[c]) - Dv);
-              float d1 =
-                  ex2_approx(fmaf(__uint_as_float(us[c + 1]), sl2, nlse2)) * (__uint_as_float(ud[c + 1]) - Dv);
-              d0 = (c >= lo && c < hi) ? d0 : 0.f;
-              d1 = (c + 1 >= lo && c + 1 < hi) ? d1 : 0.f;
-              pk[c / 2] = pack_bf16x2(d0, d1);
-            }
+            lo = (int)imax64(imin64((cs ? clo : nlo) - k0, 33), -1);
+            hi = (int)imax64(imin64((cs ? chi : nhi) - k0, 33), -1);
           }
+          if (full) ds_row32<true>(us, ud, sl2x2, nl2, nD2, lo, hi, pk);
+          else ds_row32<false>(us, ud, sl2x2, nl2, nD2, lo, hi, pk);
           // 32 keys of dS as 16 packed columns over S columns this warpgroup
           // has already read (layout of packed_col128)
           tmem_st16(tmem + R.tl + b * 128 + half * 64 + s * 16, pk);
