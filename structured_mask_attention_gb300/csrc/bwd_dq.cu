@@ -30,8 +30,8 @@ constexpr int QBN = 128;  // keys per step
 constexpr int KNS = 3;    // K stages
 constexpr int VNS = 2;    // V stages
 
-enum { DQ_QF = 0, DQ_QE = 1, DQ_KF = 2, DQ_KE = 5, DQ_VF = 8, DQ_VE = 10, DQ_SF = 12, DQ_DPF = 14,
-       DQ_DPFREE = 15, DQ_DSF = 16, DQ_DONE = 18, DQ_OE = 19, DQ_NBAR = 20 };
+enum { DQ_QF = 0, DQ_QE = 1, DQ_KF = 2, DQ_KE = 5, DQ_VF = 8, DQ_VE = 10, DQ_DPF = 12, DQ_DPFREE = 13,
+       DQ_DSF = 14, DQ_DONE = 16, DQ_OE = 17, DQ_NBAR = 18 };
 
 template <int HD>
 struct DqLayout {
@@ -100,7 +100,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(BAR(DQ_VF + s), 1);
       mbar_init(BAR(DQ_VE + s), 1);
-      mbar_init(BAR(DQ_SF + s), 1);
       mbar_init(BAR(DQ_DSF + s), kEwThreads);
     }
     mbar_init(BAR(DQ_DPF), 1);
@@ -169,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdQ = idesc_bf16(QBM, HD, false, true);
       const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024), do0 = sdesc_sw128(sdO, 16, 1024);
       uint32_t itn = 0, g = 0;
+      uint32_t ks = 0, kph = 0;  // K stage of step g and its phase parity
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
         const int64_t idx = snake_item(rnd, cta, grid);
@@ -176,28 +176,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const DqGeo t = dq_geo(p, idx);
         if (t.n == 0) continue;
         if (!mbar_wait(BAR(DQ_QF), itn & 1, wd, 24)) { ok = false; break; }
-        const uint32_t g0 = g;
-        // dQ += dS(jj) K(jj), dS packed over S buffer of step jj
-        auto do_dq = [&](int jj) -> bool {
-          const uint32_t gg = g0 + jj;
-          const int b = gg & 1, ks = gg % KNS;
+        // stage of the previous step (read by its dQ MMA)
+        uint32_t pks = 0;
+        // dQ += dS(g-1) K(g-1), dS packed over S buffer (g-1) & 1
+        auto do_dq = [&](uint32_t gg, uint32_t kst, bool first) -> bool {
+          const uint32_t b = gg & 1;
           if (!mbar_wait(BAR(DQ_DSF + b), (gg >> 1) & 1, wd, 25)) return false;
-          if (jj == 0 && itn > 0 && !mbar_wait(BAR(DQ_OE), (itn - 1) & 1, wd, 26)) return false;
+          if (first && itn > 0 && !mbar_wait(BAR(DQ_OE), (itn - 1) & 1, wd, 26)) return false;
           tc_fence_after();
-          const uint64_t bk0 = sdesc_sw128(sK + ks * LY::kTile, LY::kPanel, 1024);
-          const uint32_t acc0 = jj > 0 ? 1u : 0u;
+          const uint64_t bk0 = sdesc_sw128(sK + kst * LY::kTile, LY::kPanel, 1024);
+          const uint32_t a0 = tmem + b * 128;
 #pragma unroll
           for (int kk = 0; kk < QBN / 16; ++kk)
-            tc_mma_ts(tmem + kColDQ, tmem + b * 128 + packed_col128(kk), desc_add(bk0, kk * 2048), kIdQ,
-                      kk > 0 ? 1u : acc0);
-          tc_commit(BAR(DQ_KE + ks));
+            tc_mma_ts(tmem + kColDQ, a0 + packed_col128(kk), desc_add(bk0, kk * 2048), kIdQ,
+                      (kk > 0 || !first) ? 1u : 0u);
+          tc_commit(BAR(DQ_KE + kst));
           return true;
         };
         for (int j = 0; j < t.n && ok; ++j, ++g) {
-          const int b = g & 1, ks = g % KNS, vs = g & 1;
+          const uint32_t b = g & 1, vs = g & 1;
           // S(j) into buffer b: the dS last held there (step g-2) was read by
           // the dQ MMA issued one iteration earlier
-          if (!mbar_wait(BAR(DQ_KF + ks), (g / KNS) & 1, wd, 27)) { ok = false; break; }
+          if (!mbar_wait(BAR(DQ_KF + ks), kph, wd, 27)) { ok = false; break; }
           tc_fence_after();
           const uint64_t dk0 = sdesc_sw128(sK + ks * LY::kTile, 16, 1024);
 #pragma unroll
@@ -205,8 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t off = (kk >> 2) * LY::kPanel + (kk & 3) * 32;
             tc_mma_ss(tmem + b * 128, desc_add(dq0, off), desc_add(dk0, off), kIdS, kk > 0 ? 1u : 0u);
           }
-          tc_commit(BAR(DQ_SF + b));
-          // dP(j) once the elementwise warps have read dP(j-1)
+          // dP(j) once the elementwise warps have read dP(j-1); its commit
+          // also tells them that S(j) is complete
           if (g >= 1 && !mbar_wait(BAR(DQ_DPFREE), (g - 1) & 1, wd, 28)) { ok = false; break; }
           if (!mbar_wait(BAR(DQ_VF + vs), (g >> 1) & 1, wd, 29)) { ok = false; break; }
           tc_fence_after();
@@ -219,10 +219,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit(BAR(DQ_DPF));
           tc_commit(BAR(DQ_VE + vs));
           if (j == t.n - 1) tc_commit(BAR(DQ_QE));
-          if (j >= 1 && !do_dq(j - 1)) { ok = false; break; }
+          if (j >= 1 && !do_dq(g - 1, pks, j == 1)) { ok = false; break; }
+          pks = ks;
+          if (++ks == KNS) { ks = 0; kph ^= 1; }
         }
         if (!ok) break;
-        if (!do_dq(t.n - 1)) { ok = false; break; }
+        if (!do_dq(g - 1, pks, t.n == 1)) { ok = false; break; }
         tc_commit(BAR(DQ_DONE));
         ++itn;
       }
@@ -270,7 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool full = cs ? tile_full(key0, QBN, t.q.c_all_lo, t.q.c_all_hi, p.g.L)
                              : tile_full(key0, QBN, t.q.n_all_lo, t.q.n_all_hi, p.g.L);
         const int b = g & 1;
-        ok = mbar_wait(BAR(DQ_SF + b), (g >> 1) & 1, wd, 30) && mbar_wait(BAR(DQ_DPF), g & 1, wd, 31);
+        // dP(j) complete (its commit follows S(j)'s MMAs)
+        ok = mbar_wait(BAR(DQ_DPF), g & 1, wd, 31);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
