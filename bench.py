@@ -153,9 +153,18 @@ def blas_threads():
 
 
 # ------------------------------------------------------------------ traffic
+def sources_digest(paths):
+    """First 16 hex digits of the SHA-256 of the concatenated files."""
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def committed_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
+    """DRAM bytes per full-size launch from the committed ncu summary, if it
+    was taken on the current kernel sources (else None)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
@@ -164,12 +173,10 @@ def committed_traffic(kernel):
     ent = d.get(kernel)
     if not ent:
         return None
-    src = os.path.join(ROOT, ent["source"])
-    if not os.path.exists(src):
+    srcs = ent.get("sources", [])
+    if not srcs or not all(os.path.exists(os.path.join(ROOT, s)) for s in srcs):
         return None
-    with open(src, "rb") as fh:
-        h = hashlib.sha256(fh.read()).hexdigest()[:16]
-    if h != ent.get("source_sha256_16"):
+    if sources_digest(srcs) != ent.get("sources_sha256_16"):
         return None
     return ent.get("dram_bytes_per_launch_full")
 
