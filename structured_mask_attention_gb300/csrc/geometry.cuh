@@ -134,6 +134,8 @@ BDLM_HD QItem q_item(const Geom& g, int tq, int64_t idx) {
   return it;
 }
 
+constexpr int kRoundItems = 152;  // key tiles per (block, KV head) of the dK/dV list
+
 // Persistent-grid assignment: CTA `cta` of `grid` takes, in round r, the item
 // r*grid + cta on even rounds and r*grid + (grid-1-cta) on odd rounds.  Over
 // a longest-first list this boustrophedon order evens the CTAs' totals.
@@ -145,7 +147,9 @@ BDLM_HD int64_t snake_item(int64_t round, int cta, int grid) {
 // dK/dV work items: (key stream, key/value head, key tile).  Clean key tiles
 // first in increasing position (a clean key is read by every later row, so
 // earlier tiles carry more work), then corrupted key tiles (each read only by
-// its own block's rows).  Only tiles that intersect this call's keys count.
+// its own block's rows); each range in blocks of kRoundItems tiles with one
+// KV head after the other inside a block, so the items running together read
+// one head's Q and dO.  Only tiles that intersect this call's keys count.
 struct KVItem {
   int key_stream, kv_head;
   int64_t ktile;
@@ -172,15 +176,22 @@ BDLM_HD KVItem kv_item(const Geom& g, int tk, int64_t idx) {
   int64_t cf, cc, nc;
   kv_tile_span(g, tk, cf, cc, nc);
   KVItem it;
-  const int64_t t = idx / g.Hkv;
-  it.kv_head = (int)(idx % g.Hkv);
-  if (t < cc) {
-    it.key_stream = 0;
-    it.ktile = cf + t;
-  } else {
+  // clean key tiles first, then corrupted ones; each range in blocks of
+  // kRoundItems tiles, one KV head after the other inside a block
+  int64_t i = idx, base = cf, count = cc;
+  it.key_stream = 0;
+  if (idx >= cc * g.Hkv) {
+    i = idx - cc * g.Hkv;
+    base = 0;
+    count = nc;
     it.key_stream = 1;
-    it.ktile = t - cc;
   }
+  const int64_t bi = i / ((int64_t)kRoundItems * g.Hkv);
+  const int64_t t0 = bi * kRoundItems;
+  const int64_t nb = imin64(kRoundItems, count - t0);
+  const int64_t r = i - t0 * g.Hkv;
+  it.kv_head = (int)(r / nb);
+  it.ktile = base + t0 + r % nb;
   return it;
 }
 
