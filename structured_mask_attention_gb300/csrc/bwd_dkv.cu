@@ -116,6 +116,37 @@ __device__ __forceinline__ void key_rows(const Geom& g, int ks, int64_t j, int s
   }
 }
 
+// P = exp2(s sl2 - LSE log2 e) for 32 query rows (columns of S^T) of one key
+// row: scores us, their rows' LSE in lse[0..32), key offsets c0 + [0, 32)
+// outside [lo, hi) give 0 unless FULL.  fp32 P into pf, packed bf16 into pk.
+// The masked variant is a separate instantiation so that the common, fully
+// visible case is one straight-line block the compiler can schedule.
+template <bool FULL>
+__device__ __forceinline__ void p_cols32(const uint32_t (&us)[32], const float* lse, uint64_t sl2x2,
+                                         uint64_t nlog2e, int c0, int lo, int hi, float (&pf)[32],
+                                         uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int c4 = 0; c4 < 8; ++c4) {
+    const float4 l4 = *reinterpret_cast<const float4*>(lse + 4 * c4);
+    const uint64_t nlA = f2_mul(f2(l4.x, l4.y), nlog2e), nlB = f2_mul(f2(l4.z, l4.w), nlog2e);
+    float x0, x1, x2, x3;
+    f2_split(f2_fma(f2(__uint_as_float(us[4 * c4]), __uint_as_float(us[4 * c4 + 1])), sl2x2, nlA), x0, x1);
+    f2_split(f2_fma(f2(__uint_as_float(us[4 * c4 + 2]), __uint_as_float(us[4 * c4 + 3])), sl2x2, nlB), x2, x3);
+    float pe[4] = {ex2_approx(x0), ex2_approx(x1), ex2_approx(x2), ex2_approx(x3)};
+    if (!FULL) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = c0 + 4 * c4 + e;
+        pe[e] = (c >= lo && c < hi) ? pe[e] : 0.f;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pf[4 * c4 + e] = pe[e];
+    pk[2 * c4] = pack_bf16x2(pe[0], pe[1]);
+    pk[2 * c4 + 1] = pack_bf16x2(pe[2], pe[3]);
+  }
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     bdlm_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tQc, const __grid_constant__ CUtensorMap tQn,
@@ -347,31 +378,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lo = full ? -1 : max(min(k_lo - base_row, 65), -1);
         const int hi = full ? 65 : max(min(k_hi - base_row, 65), -1);
         // P = exp(scale S - LSE) on this half's 64 query rows, kept in fp32
-        float pf[64];
+        float pf[2][32];
 #pragma unroll
         for (int sub = 0; sub < 2; ++sub) {
           uint32_t us[32];
           tmem_ld32(tmem + R.tl + kColS + half * 64 + sub * 32, us);
           uint32_t pk[16];
-#pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(stl + sub * 32 + 4 * c4);
-            const uint64_t nlA = f2_mul(f2(l4.x, l4.y), nlog2e), nlB = f2_mul(f2(l4.z, l4.w), nlog2e);
-            const int c = sub * 32 + 4 * c4;
-            float x0, x1, x2, x3;
-            f2_split(f2_fma(f2(__uint_as_float(us[4 * c4]), __uint_as_float(us[4 * c4 + 1])), sl2x2, nlA), x0, x1);
-            f2_split(f2_fma(f2(__uint_as_float(us[4 * c4 + 2]), __uint_as_float(us[4 * c4 + 3])), sl2x2, nlB), x2,
-                     x3);
-            float pe[4] = {ex2_approx(x0), ex2_approx(x1), ex2_approx(x2), ex2_approx(x3)};
-            if (!full) {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) pe[e] = (c + e >= lo && c + e < hi) ? pe[e] : 0.f;
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) pf[c + e] = pe[e];
-            pk[2 * c4] = pack_bf16x2(pe[0], pe[1]);
-            pk[2 * c4 + 1] = pack_bf16x2(pe[2], pe[3]);
-          }
+          if (full) p_cols32<true>(us, stl + sub * 32, sl2x2, nlog2e, sub * 32, lo, hi, pf[sub], pk);
+          else p_cols32<false>(us, stl + sub * 32, sl2x2, nlog2e, sub * 32, lo, hi, pf[sub], pk);
           // P^T (bf16) over S^T columns this warpgroup has already read
           tmem_st16(tmem + R.tl + kColS + half * 64 + sub * 16, pk);
         }
@@ -389,13 +403,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
             const float4 d4 = *reinterpret_cast<const float4*>(stl + KBN + sub * 32 + 4 * c4);
-            const int c = sub * 32 + 4 * c4;
             const uint64_t tA = f2_sub(f2(__uint_as_float(ud[4 * c4]), __uint_as_float(ud[4 * c4 + 1])), f2(d4.x, d4.y));
             const uint64_t tB =
                 f2_sub(f2(__uint_as_float(ud[4 * c4 + 2]), __uint_as_float(ud[4 * c4 + 3])), f2(d4.z, d4.w));
             float s0, s1, s2, s3;
-            f2_split(f2_mul(f2(pf[c], pf[c + 1]), tA), s0, s1);
-            f2_split(f2_mul(f2(pf[c + 2], pf[c + 3]), tB), s2, s3);
+            f2_split(f2_mul(f2(pf[sub][4 * c4], pf[sub][4 * c4 + 1]), tA), s0, s1);
+            f2_split(f2_mul(f2(pf[sub][4 * c4 + 2], pf[sub][4 * c4 + 3]), tB), s2, s3);
             dk[2 * c4] = pack_bf16x2(s0, s1);
             dk[2 * c4 + 1] = pack_bf16x2(s2, s3);
           }
