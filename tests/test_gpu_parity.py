@@ -63,6 +63,8 @@ def test_tiny_workload_brute(lib):
     (512, 256, 2, 1, 128),   # blocks larger than a tile
     (640, 160, 5, 1, 64),    # GQA 5, blocks not a multiple of the tile
     (96, 32, 1, 1, 128),     # shorter than one tile
+    (1024, 16, 2, 1, 64),    # many small blocks: every key step partially masked
+    (768, 96, 4, 4, 128),    # 256-row forward items spanning three blocks, MHA
 ])
 def test_shapes(lib, L, B, Hq, Hkv, d):
     _run_case(lib, L, B, Hq, Hkv, d, seed=L + B)
