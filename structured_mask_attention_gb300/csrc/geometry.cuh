@@ -135,6 +135,10 @@ BDLM_HD QItem q_item(const Geom& g, int tq, int64_t idx) {
 }
 
 constexpr int kRoundItems = 152;  // key tiles per (block, KV head) of the dK/dV list
+// Below this many key tiles per key stream the dK/dV list stays tile-major:
+// blocks then cover tiles of very different lengths and unbalance the grid
+// (host simulation of the snake assignment: 32 % spread at L = 16k).
+constexpr int64_t kBlockedMinTiles = 6 * kRoundItems;
 
 // Persistent-grid assignment: CTA `cta` of `grid` takes, in round r, the item
 // r*grid + cta on even rounds and r*grid + (grid-1-cta) on odd rounds.  Over
@@ -147,9 +151,11 @@ BDLM_HD int64_t snake_item(int64_t round, int cta, int grid) {
 // dK/dV work items: (key stream, key/value head, key tile).  Clean key tiles
 // first in increasing position (a clean key is read by every later row, so
 // earlier tiles carry more work), then corrupted key tiles (each read only by
-// its own block's rows); each range in blocks of kRoundItems tiles with one
-// KV head after the other inside a block, so the items running together read
-// one head's Q and dO.  Only tiles that intersect this call's keys count.
+// its own block's rows).  A long range (at least kBlockedMinTiles tiles) goes
+// in blocks of kRoundItems tiles with one KV head after the other inside a
+// block, so the items running together read one head's Q and dO; a short
+// range goes tile by tile with the KV heads inside.  Only tiles that
+// intersect this call's keys count.
 struct KVItem {
   int key_stream, kv_head;
   int64_t ktile;
@@ -176,8 +182,6 @@ BDLM_HD KVItem kv_item(const Geom& g, int tk, int64_t idx) {
   int64_t cf, cc, nc;
   kv_tile_span(g, tk, cf, cc, nc);
   KVItem it;
-  // clean key tiles first, then corrupted ones; each range in blocks of
-  // kRoundItems tiles, one KV head after the other inside a block
   int64_t i = idx, base = cf, count = cc;
   it.key_stream = 0;
   if (idx >= cc * g.Hkv) {
@@ -186,6 +190,15 @@ BDLM_HD KVItem kv_item(const Geom& g, int tk, int64_t idx) {
     count = nc;
     it.key_stream = 1;
   }
+  if (count < kBlockedMinTiles) {
+    // short range: tile-major, KV head minor (rounds of similar lengths)
+    it.kv_head = (int)(i % g.Hkv);
+    it.ktile = base + i / g.Hkv;
+    return it;
+  }
+  // long range: blocks of kRoundItems tiles, one KV head after the other
+  // inside a block; a block of one head is one grid round, and the snake
+  // assignment pairs each round's long items with the next round's short ones
   const int64_t bi = i / ((int64_t)kRoundItems * g.Hkv);
   const int64_t t0 = bi * kRoundItems;
   const int64_t nb = imin64(kRoundItems, count - t0);
