@@ -195,10 +195,16 @@ bdlm_status bdlm_attn_bwd_shard(const void* Qc, const void* Kc, const void* Vc,
                                 void* workspace, size_t ws_bytes, bdlm_stream stream);
 
 /* Host-only: the forward work list in launch order, for inspection and tests.
- * One item per (query tile of tile_q rows, query head, stream), query tiles
- * from the last to the first: the number of visible key tiles never grows
- * along the list for the clean stream and grows by at most one tile for the
- * corrupted stream, so the persistent kernels take the longest items first.
+ * One item per (query tile of tile_q rows, query head, stream), longest
+ * first: query tiles from the last to the first.  With at least
+ * 6 * 152 / (2 Hq / Hkv) query tiles they go in blocks of 152 / (2 Hq / Hkv)
+ * tiles, and inside a block the items of one KV head (its query heads, both
+ * streams) come together, one KV head after the other, so that the items a
+ * persistent grid runs at the same time read the same keys; otherwise the two
+ * streams of one head are adjacent, then the heads.  Along the list the
+ * number of visible key tiles never exceeds the largest seen so far (plus one
+ * tile for the corrupted stream, whose own-block range can straddle one more
+ * tile).
  * Each item is 8 int32:
  *   {stream (0 clean, 1 corrupted), head, q_tile, clean_tile_begin,
  *    clean_tile_end, corrupted_tile_begin, corrupted_tile_end, n_tiles}

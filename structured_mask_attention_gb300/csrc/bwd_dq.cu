@@ -51,6 +51,7 @@ struct DqGeo {
   int64_t r0;
   QTileRanges q;
   int nc, n;
+  int rot;  // the clean-key sweep starts at clean tile c0 + rot
 };
 
 __device__ __forceinline__ DqGeo dq_geo(const BwdParams& p, int64_t idx) {
@@ -64,11 +65,16 @@ __device__ __forceinline__ DqGeo dq_geo(const BwdParams& p, int64_t idx) {
   t.q = qtile_ranges(p.g, t.stream, t.r0, r1, QBN);
   t.nc = (int)(t.q.c1 - t.q.c0);
   t.n = t.nc + (int)(t.q.n1 - t.q.n0);
+  t.rot = sweep_rotation(idx, t.nc);
   return t;
 }
 
+// First key of step j: clean tiles from c0 + rot round to c0 + rot - 1, then
+// the corrupted tiles (dQ sums over keys in any order).
 __device__ __forceinline__ int dq_key0(const DqGeo& t, int j) {
-  return (int)((j < t.nc ? t.q.c0 + j : t.q.n0 + (j - t.nc)) * QBN);
+  int c = j + t.rot;
+  if (c >= t.nc) c -= t.nc;
+  return (int)((j < t.nc ? t.q.c0 + c : t.q.n0 + (j - t.nc)) * QBN);
 }
 
 template <int HD>

@@ -69,6 +69,7 @@ struct ItemGeo {
   int64_t r0;
   QTileRanges q;
   int nc, n;  // clean key tiles, all key tiles
+  int rot;    // the clean-key sweep starts at clean tile c0 + rot
 };
 
 __device__ __forceinline__ ItemGeo item_geo(const FwdParams& p, int64_t idx) {
@@ -82,11 +83,18 @@ __device__ __forceinline__ ItemGeo item_geo(const FwdParams& p, int64_t idx) {
   t.q = qtile_ranges(p.g, t.stream, t.r0, r1, BN);
   t.nc = (int)(t.q.c1 - t.q.c0);
   t.n = t.nc + (int)(t.q.n1 - t.q.n0);
+  t.rot = sweep_rotation(idx, t.nc);
   return t;
 }
 
+// First key of step j: the clean tiles from c0 + rot round to c0 + rot - 1,
+// then the corrupted tiles (the online softmax is order-independent).
+__device__ __forceinline__ int clean_step(int j, int rot, int nc) {
+  const int x = j + rot;
+  return x < nc ? x : x - nc;
+}
 __device__ __forceinline__ int64_t tile_key0(const ItemGeo& t, int j) {
-  return (j < t.nc ? t.q.c0 + j : t.q.n0 + (j - t.nc)) * BN;
+  return (j < t.nc ? t.q.c0 + clean_step(j, t.rot, t.nc) : t.q.n0 + (j - t.nc)) * BN;
 }
 
 // P is stored as packed bf16 over the S columns it replaces: keys [64, 128)
@@ -343,14 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         noisy_interval(p.g, g.stream, rr, b0, b1);
         lo_c = (int)a0; hi_c = (int)a1; lo_n = (int)b0; hi_n = (int)b1;
       }
-      const int nc = g.nc, n = g.n, c0 = (int)g.q.c0, n0 = (int)g.q.n0;
+      const int nc = g.nc, n = g.n, c0 = (int)g.q.c0, n0 = (int)g.q.n0, rot = g.rot;
       const int call_lo = (int)g.q.c_all_lo, call_hi = (int)imin64(g.q.c_all_hi, p.g.L);
       const int nall_lo = (int)g.q.n_all_lo, nall_hi = (int)imin64(g.q.n_all_hi, p.g.L);
       const float sl2 = p.scale_log2;
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j, ++sc) {
         const bool cs = j < nc;
-        const int key0 = (cs ? c0 + j : n0 + (j - nc)) * BN;
+        const int key0 = (cs ? c0 + clean_step(j, rot, nc) : n0 + (j - nc)) * BN;
         const bool full = cs ? (key0 >= call_lo && key0 + BN <= call_hi) : (key0 >= nall_lo && key0 + BN <= nall_hi);
         ok = mbar_wait(BAR(B_SF + t), sc & 1, wd, 12);
         ok = __all_sync(0xffffffffu, ok);

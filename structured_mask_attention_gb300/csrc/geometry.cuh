@@ -110,31 +110,67 @@ BDLM_HD bool tile_full(int64_t j0, int tk, int64_t all_lo, int64_t all_hi, int64
   return j0 >= all_lo && j0 + tk <= all_hi && j0 + tk <= L;
 }
 
-// Forward / dQ work items: (query tile, head, stream), ordered by
-// non-increasing visible-key count.  For a fixed shard the visible key count
-// of a query tile never decreases with its position, so walking query tiles
-// from the last to the first is longest-first.  Inside one query-tile index
-// the two streams of one head are adjacent, then the heads of one GQA group,
-// so items running at the same time read the same key/value tiles.
+// Forward / dQ work items: (query tile, head, stream), longest first.  For a
+// fixed shard the visible key count of a query tile never decreases with its
+// position, so query tiles are taken from the last to the first.  With many
+// query tiles (at least kBlockedMinQBlocks blocks) they go in blocks of
+// q_block() tiles, and inside a block the items of one KV head (its query
+// heads, both streams) come together, one KV head after the other: such a
+// block is about one round of a 152-CTA persistent grid, whose key sweeps
+// then read one head's K and V, which fit in L2, instead of every head's.
+// Otherwise, inside one query-tile index the two streams of one head are
+// adjacent, then the heads.  (The kernels also start each item's clean-key
+// sweep at a different tile, so that the items of a round do not all read
+// the same tile at once.)
 struct QItem {
   int stream, head;
   int64_t qtile;
 };
 
+constexpr int kRoundItems = 152;        // items per block and KV head, about one grid round
+constexpr int64_t kBlockedMinQBlocks = 6;
+
 BDLM_HD int64_t q_items(const Geom& g, int tq) { return cdiv64(g.L, tq) * g.Hq * 2; }
+
+BDLM_HD int64_t q_block(const Geom& g) {
+  const int64_t per_kv = (int64_t)(g.Hq / g.Hkv) * 2;  // items per query tile and KV head
+  const int64_t qb = kRoundItems / per_kv;
+  return qb > 0 ? qb : 1;
+}
 
 BDLM_HD QItem q_item(const Geom& g, int tq, int64_t idx) {
   const int64_t nqt = cdiv64(g.L, tq);
-  const int64_t per = (int64_t)g.Hq * 2;
+  const int64_t qb = q_block(g);
   QItem it;
-  it.qtile = nqt - 1 - idx / per;
-  const int64_t rem = idx % per;
-  it.stream = (int)(rem % 2);
-  it.head = (int)(rem / 2);
+  if (nqt < kBlockedMinQBlocks * qb) {
+    const int64_t per = (int64_t)g.Hq * 2;
+    it.qtile = nqt - 1 - idx / per;
+    const int64_t rem = idx % per;
+    it.stream = (int)(rem % 2);
+    it.head = (int)(rem / 2);
+    return it;
+  }
+  const int grp = g.Hq / g.Hkv;
+  const int64_t per_kv = (int64_t)grp * 2;
+  const int64_t per_block = qb * g.Hq * 2;  // items of a full block
+  const int64_t bi = idx / per_block;
+  const int64_t hi = nqt - 1 - bi * qb;      // first (largest) query tile of the block
+  const int64_t lo = imax64(0, hi - qb + 1);
+  const int64_t nb = hi - lo + 1;            // query tiles in this block
+  const int64_t r = idx - bi * per_block;
+  const int64_t kv = r / (nb * per_kv);
+  const int64_t r2 = r - kv * (nb * per_kv);
+  const int64_t combo = r2 % per_kv;
+  it.qtile = hi - r2 / per_kv;
+  it.stream = (int)(combo % 2);
+  it.head = (int)(kv * grp + combo / 2);
   return it;
 }
 
-constexpr int kRoundItems = 152;  // key tiles per (block, KV head) of the dK/dV list
+// First clean key tile of an item's sweep, relative to its clean range of nc
+// tiles: items that run together start at different tiles.
+BDLM_HD int sweep_rotation(int64_t idx, int nc) { return nc > 0 ? (int)(idx % nc) : 0; }
+
 // Below this many key tiles per key stream the dK/dV list stays tile-major:
 // blocks then cover tiles of very different lengths and unbalance the grid
 // (host simulation of the snake assignment: 32 % spread at L = 16k).

@@ -128,9 +128,10 @@ def test_worklist_covers_exactly_visible_tiles(lib, L, B, Hq, Hkv, tq, tk, kb, k
         else:
             assert n0 == n1
     assert len(seen) == len(items)
-    # query tiles from last to first: per stream, the visible key-tile count
-    # never increases (clean stream) or rises by at most one tile (corrupted
-    # stream, whose own-block range can straddle one more tile)
+    # longest first (block by block for long lists): per stream, the visible
+    # key-tile count never exceeds the largest seen so far, by more than one
+    # tile for the corrupted stream (whose own-block range can straddle one
+    # more tile)
     for s in (0, 1):
         costs = [it[7] for it in items if it[0] == s]
         slack = 0 if s == 0 else 1
