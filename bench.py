@@ -36,6 +36,23 @@ METRIC = "useful fwd+bwd TFLOP/s & tokens/s at 1 GB300; % of bf16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def job_time_ms(ms_local, world, device):
+    """The job's time for a step: the maximum over ranks of each rank's own
+    CUDA-event time (ranks are replicas, so the slowest one ends the step)."""
+    if world <= 1:
+        return ms_local
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world, ms):
+    """Whole-job rate: the units all ranks processed divided by the job's time."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def useful_flops(L, B, Hq, d):
     return 14.0 * d * L * (L + B) * Hq
 
@@ -238,11 +255,7 @@ def run_native(args, rank, world, local_rank):
     clk = clocks.stop()
     m.bdlm_timing_enable(False)
     ktimes = m.bdlm_timing_report(reset=True)
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = job_time_ms(ev0.elapsed_time(ev1), world, dev)
     m.bdlm_sync_status(ws_f)
     m.bdlm_sync_status(ws_b)
     ms_step = ms / args.steps
@@ -321,14 +334,10 @@ def run_native(args, rank, world, local_rank):
         b.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ems = a.elapsed_time(b) / k2
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": round(world * useful_flops(L, B, Hq, d) / (ems * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+        ems = job_time_ms(a.elapsed_time(b) / k2, world, dev)
+        e2e = {"value": round(job_rate(useful_flops(L, B, Hq, d), world, ems) / 1e12, 3), "unit": "TFLOP/s",
                "ms_per_step": round(ems, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "tokens_per_s": round(world * 2 * L / (ems * 1e-3), 1), "steps": k2,
+               "tokens_per_s": round(job_rate(2 * L, world, ems), 1), "steps": k2,
                "pipelined": "uploads and downloads overlap neighbouring steps' compute (two buffer sets)",
                "h2d_gbs_alone": round(h2d_gbs, 1), "d2h_gbs_alone": round(d2h_gbs, 1)}
         del sets, h_in, h_out
@@ -351,7 +360,7 @@ def run_native(args, rank, world, local_rank):
                                                                       else " (of fallback)"),
                 "algorithmic_flop_per_launch": alg[dom]}
 
-    value = world * useful_flops(L, B, Hq, d) / (ms_step * 1e-3) / 1e12
+    value = job_rate(useful_flops(L, B, Hq, d), world, ms_step) / 1e12
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
@@ -359,8 +368,8 @@ def run_native(args, rank, world, local_rank):
         "config": {"workload": args.workload, "L": L, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d, "batch": 1,
                    "tokens_per_step": 2 * L, "l2": "inputs larger than L2 (129 MB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "tokens_per_s": round(world * 2 * L / (ms_step * 1e-3), 1),
-        "strict_tflops": round(world * strict_flops(L, B, Hq, d) / (ms_step * 1e-3) / 1e12, 3),
+        "tokens_per_s": round(job_rate(2 * L, world, ms_step), 1),
+        "strict_tflops": round(job_rate(strict_flops(L, B, Hq, d), world, ms_step) / 1e12, 3),
         "pct_of_peak": round(100.0 * value / world / peak_tf, 2),
         "clocks": clk, "gpu_launches": int(launches), "kernels": per_kernel, "roofline": roofline,
         "e2e": e2e,
