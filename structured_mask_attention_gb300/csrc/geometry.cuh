@@ -169,7 +169,10 @@ BDLM_HD QItem q_item(const Geom& g, int tq, int64_t idx) {
 
 // First clean key tile of an item's sweep, relative to its clean range of nc
 // tiles: items that run together start at different tiles.
-BDLM_HD int sweep_rotation(int64_t idx, int nc) { return nc > 0 ? (int)(idx % nc) : 0; }
+// (32-bit arithmetic: item indices stay far below 2^32.)
+BDLM_HD int sweep_rotation(int64_t idx, int nc) {
+  return nc > 0 ? (int)((uint32_t)idx % (uint32_t)nc) : 0;
+}
 
 // Below this many key tiles per key stream the dK/dV list stays tile-major:
 // blocks then cover tiles of very different lengths and unbalance the grid
