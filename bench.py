@@ -383,6 +383,135 @@ def run_native(args, rank, world, local_rank):
     return line
 
 
+# ------------------------------------------------------------------ sweep (measurement tables)
+def run_sweep(args):
+    """Per-config timings, the schedule ablation and the sharded block-size
+    sweep; one JSON line each (not the single bench line)."""
+    import statistics
+
+    import torch
+
+    import structured_mask_attention_gb300 as m
+    from structured_mask_attention_gb300.inputs import SHARDED_BLOCK_SIZES, WORKLOADS, make_torch
+
+    m.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    peak_tf = peak_value(peaks, "bf16_tflops_sustained")
+    names = ("Qc", "Kc", "Vc", "Qn", "Kn", "Vn")
+    reps, warm = max(10, args.steps), args.warmup
+
+    def timed(fn):
+        """Median CUDA-event time (ms) of fn over reps runs after warm runs."""
+        for _ in range(warm):
+            fn()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    def emit(d):
+        print(json.dumps(d), flush=True)
+
+    # ---- configs: forward and backward separately
+    for name in ("gqa-8k", "gqa-32k", "long-128k"):
+        w = WORKLOADS[name]
+        L, B, Hq, Hkv, d = w["L"], w["B"], w["Hq"], w["Hkv"], w["d"]
+        X = make_torch(L, Hq, Hkv, d, seed=0, device=dev)
+        ins = [X[k] for k in names]
+        sc = 1.0 / math.sqrt(d)
+        f = m.bdlm_attn_fwd(*ins, B, sc)
+        g = m.bdlm_attn_bwd(*ins, f[0], f[1], X["dOc"], X["dOn"], f[2], f[3], B, sc)
+        fms = timed(lambda: m.bdlm_attn_fwd(*ins, B, sc, out=f))
+        bms = timed(lambda: m.bdlm_attn_bwd(*ins, f[0], f[1], X["dOc"], X["dOn"], f[2], f[3], B, sc, out=g))
+        tot = fms + bms
+        useful = useful_flops(L, B, Hq, d) / (tot * 1e-3) / 1e12
+        emit({"sweep": "config", "workload": name, "L": L, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d,
+              "fwd_ms": round(fms, 3), "bwd_ms": round(bms, 3), "step_ms": round(tot, 3),
+              "useful_tflops": round(useful, 1), "strict_tflops": round(strict_flops(L, B, Hq, d) / (tot * 1e-3) / 1e12, 1),
+              "tokens_per_s": round(2 * L / (tot * 1e-3), 1), "pct_of_peak": round(100 * useful / peak_tf, 2),
+              "peak": peak_src, "reps": reps})
+        if name == "long-128k":
+            # schedule ablation: natural order + round robin vs longest first + boustrophedon
+            step = lambda: (m.bdlm_attn_fwd(*ins, B, sc, out=f),
+                            m.bdlm_attn_bwd(*ins, f[0], f[1], X["dOc"], X["dOn"], f[2], f[3], B, sc, out=g))
+            res = {}
+            for sched in ("naive", "lpt"):
+                os.environ["BDLM_SCHED"] = sched
+                res[sched] = timed(step)
+            os.environ.pop("BDLM_SCHED", None)
+            emit({"sweep": "schedule", "workload": name, "naive_ms": round(res["naive"], 3),
+                  "lpt_ms": round(res["lpt"], 3), "speedup": round(res["naive"] / res["lpt"], 3)})
+        del X, ins, f, g
+        torch.cuda.empty_cache()
+
+    # ---- sharded-256k: block-size sweep, sharded vs unsharded, merge share
+    w = WORKLOADS["sharded-256k"]
+    L, Hq, Hkv, d, P = w["L"], w["Hq"], w["Hkv"], w["d"], w["P"]
+    sc = 1.0 / math.sqrt(d)
+    for B in SHARDED_BLOCK_SIZES:
+        X = make_torch(L, Hq, Hkv, d, seed=B, device=dev)
+        ins = [X[k] for k in names]
+        step = L // P
+        bounds = [(s * step, (s + 1) * step) for s in range(P)]
+        fu = m.bdlm_attn_fwd(*ins, B, sc)
+        gu = m.bdlm_attn_bwd(*ins, fu[0], fu[1], X["dOc"], X["dOn"], fu[2], fu[3], B, sc)
+        un_f = timed(lambda: m.bdlm_attn_fwd(*ins, B, sc, out=fu))
+        un_b = timed(lambda: m.bdlm_attn_bwd(*ins, fu[0], fu[1], X["dOc"], X["dOn"], fu[2], fu[3], B, sc, out=gu))
+        parts = [m.bdlm_attn_fwd_shard(*ins, B, lo, hi, False, sc) for (lo, hi) in bounds]
+        parts.append(m.bdlm_attn_fwd_shard(*ins, B, 0, 0, True, sc))
+        spec = [(lo, hi, False) for (lo, hi) in bounds] + [(0, 0, True)]
+
+        def part_fwd():
+            for (lo, hi, loc), pt in zip(spec, parts):
+                m.bdlm_attn_fwd_shard(*ins, B, lo, hi, loc, sc, out=pt)
+
+        mo = [torch.empty((L, Hq, d), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        ml = [torch.empty((Hq, L), dtype=torch.float32, device=dev) for _ in range(2)]
+
+        def merge():
+            m.bdlm_lse_merge([p_[0] for p_ in parts], [p_[2] for p_ in parts], out=mo[0], lse_out=ml[0])
+            m.bdlm_lse_merge([p_[1] for p_ in parts], [p_[3] for p_ in parts], out=mo[1], lse_out=ml[1])
+
+        sh_f = timed(part_fwd)
+        mg = timed(merge)
+        Dc = m.bdlm_bwd_preprocess(mo[0], X["dOc"])
+        Dn = m.bdlm_bwd_preprocess(mo[1], X["dOn"])
+        pre = timed(lambda: (m.bdlm_bwd_preprocess(mo[0], X["dOc"], out=Dc),
+                             m.bdlm_bwd_preprocess(mo[1], X["dOn"], out=Dn)))
+        z = lambda H: torch.zeros((L, H, d), dtype=torch.float32, device=dev)
+        dQc, dQn, dKc, dVc, dKn, dVn = z(Hq), z(Hq), z(Hkv), z(Hkv), z(Hkv), z(Hkv)
+
+        def part_bwd():
+            for (lo, hi, loc) in spec:
+                m.bdlm_attn_bwd_shard(*ins, X["dOc"], X["dOn"], ml[0], ml[1], Dc, Dn, B, lo, hi, loc,
+                                      dQc, dQn, dKc, dVc, dKn, dVn, sc)
+
+        sh_b = timed(part_bwd)
+        # merge bytes: every non-empty (row, head, partial) O row read, all LSE_p read, O (bf16) and LSE written
+        nonempty = sum(int((p_[2] > float("-inf")).sum().item() + (p_[3] > float("-inf")).sum().item())
+                       for p_ in parts)
+        mbytes = nonempty * d * 4 + len(parts) * 2 * L * Hq * 4 + 2 * L * Hq * (d * 2 + 4)
+        pbytes = 2 * (2 * L * Hq * d * 2 + L * Hq * 4)
+        sh_tot = sh_f + mg + pre + sh_b
+        emit({"sweep": "sharded", "workload": "sharded-256k", "B": B, "P": P,
+              "unsharded_fwd_ms": round(un_f, 3), "unsharded_bwd_ms": round(un_b, 3),
+              "sharded_fwd_ms": round(sh_f, 3), "merge_ms": round(mg, 3), "preprocess_ms": round(pre, 3),
+              "sharded_bwd_ms": round(sh_b, 3), "sharded_total_ms": round(sh_tot, 3),
+              "unsharded_useful_tflops": round(useful_flops(L, B, Hq, d) / ((un_f + un_b) * 1e-3) / 1e12, 1),
+              "sharded_useful_tflops": round(useful_flops(L, B, Hq, d) / (sh_tot * 1e-3) / 1e12, 1),
+              "merge_share": round(mg / sh_tot, 5), "merge_gbs": round(mbytes / (mg * 1e-3) / 1e9, 1),
+              "merge_bytes": mbytes, "preprocess_gbs": round(pbytes / (pre * 1e-3) / 1e9, 1)})
+        del X, ins, fu, gu, parts, mo, ml, Dc, Dn, dQc, dQn, dKc, dVc, dKn, dVn
+        torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args):
     from structured_mask_attention_gb300.inputs import WORKLOADS
@@ -419,6 +548,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for the CPU baseline")
+    ap.add_argument("--sweep", action="store_true",
+                    help="measurement tables instead of the bench line: per-config fwd/bwd times, the "
+                         "schedule ablation (BDLM_SCHED=naive vs longest first) and the sharded-256k "
+                         "block-size sweep with merge and preprocess bandwidth")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -428,6 +561,10 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.sweep:
+        if rank == 0:
+            run_sweep(args)
         return
     if world > 1:
         import torch

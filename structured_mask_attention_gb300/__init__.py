@@ -307,7 +307,7 @@ def bdlm_attn_bwd_shard(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn, B:
         _stream(stream)))
 
 
-def bdlm_worklist(L: int, B: int, Hq: int, Hkv: int, tile_q: int = 128, tile_k: int = 64,
+def bdlm_worklist(L: int, B: int, Hq: int, Hkv: int, tile_q: int = 256, tile_k: int = 128,
                   kv_begin: int = 0, kv_end: int | None = None, include_local: bool = True):
     """The forward work list as a list of 8-tuples (host only, no GPU)."""
     kv_end = L if kv_end is None else kv_end

@@ -219,6 +219,14 @@ uint64_t wait_limit_ns() {
   return v;
 }
 
+// BDLM_SCHED=naive: work items in natural order, round robin over the grid
+// (the load-balancing ablation); otherwise longest first, boustrophedon.
+// Read on every call, so one process can time both.
+int naive_schedule() {
+  const char* s = std::getenv("BDLM_SCHED");
+  return (s && std::strcmp(s, "naive") == 0) ? 1 : 0;
+}
+
 bdlm_status clear_status(void* ws, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(ws, 0, 4, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
@@ -248,6 +256,7 @@ bdlm_status fwd_common(const void* Qc, const void* Kc, const void* Vc, const voi
   BDLM_CHECK(encode_lhd(enc, &maps.Vn, Vn, L, Hkv, d, kFwdTileK));
   FwdParams p;
   p.g = Geom{L, B, Hq, Hkv, kv_begin, kv_end, include_local ? 1 : 0};
+  p.g.naive_order = naive_schedule();
   p.scale_log2 = scale * 1.4426950408889634f;
   p.Oc = Oc;
   p.On = On;
@@ -271,6 +280,7 @@ BwdParams bwd_params(const void* Qc, const void* Kc, const void* Vc, const void*
                      int64_t kv_end, int include_local) {
   BwdParams p;
   p.g = Geom{L, B, Hq, Hkv, kv_begin, kv_end, include_local ? 1 : 0};
+  p.g.naive_order = naive_schedule();
   p.d = d;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -508,7 +518,8 @@ int64_t bdlm_worklist(int64_t L, int64_t B, int Hq, int Hkv, int tile_q, int til
     if (L <= 0 || B <= 0 || L % B || Hq <= 0 || Hkv <= 0 || Hq % Hkv || tile_q <= 0 || tile_k <= 0) return -1;
     if (kv_begin < 0 || kv_end < kv_begin || kv_end > L) return -1;
     if (cap > 0 && !out) return -1;
-    const Geom g{L, B, Hq, Hkv, kv_begin, kv_end, include_local ? 1 : 0};
+    Geom g{L, B, Hq, Hkv, kv_begin, kv_end, include_local ? 1 : 0};
+    g.naive_order = naive_schedule();
     const int64_t n = q_items(g, tile_q);
     for (int64_t i = 0; i < n && i < cap; ++i) {
       const QItem it = q_item(g, tile_q, i);

@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t itn = 0, qc = 0;
     bool ok = true;
     for (int64_t rnd = 0; ok; ++rnd) {
-      const int64_t idx = snake_item(rnd, cta, grid);
+      const int64_t idx = sched_item(p.g, rnd, cta, grid);
       if (idx >= n_items) break;
       const DkvGeo t = dkv_geo(p, idx);
       if (t.n == 0) continue;
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t itn = 0, qc = 0;
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
-        const int64_t idx = snake_item(rnd, cta, grid);
+        const int64_t idx = sched_item(p.g, rnd, cta, grid);
         if (idx >= n_items) break;
         const DkvGeo t = dkv_geo(p, idx);
         if (t.n == 0) continue;
@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     const uint64_t sl2x2 = f2(p.scale_log2, p.scale_log2), nlog2e = f2(-kLog2e, -kLog2e);
     for (int64_t rnd = 0; ok; ++rnd) {
-      const int64_t idx = snake_item(rnd, cta, grid);
+      const int64_t idx = sched_item(p.g, rnd, cta, grid);
       if (idx >= n_items) break;
       const DkvGeo t = dkv_geo(p, idx);
       if (t.n == 0) continue;

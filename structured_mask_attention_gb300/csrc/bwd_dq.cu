@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t itn = 0, g = 0;  // items with work, global step count
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
-        const int64_t idx = snake_item(rnd, cta, grid);
+        const int64_t idx = sched_item(p.g, rnd, cta, grid);
         if (idx >= n_items) break;
         const DqGeo t = dq_geo(p, idx);
         if (t.n == 0) continue;
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ks = 0, kph = 0;  // K stage of step g and its phase parity
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
-        const int64_t idx = snake_item(rnd, cta, grid);
+        const int64_t idx = sched_item(p.g, rnd, cta, grid);
         if (idx >= n_items) break;
         const DqGeo t = dq_geo(p, idx);
         if (t.n == 0) continue;
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t itn = 0, g = 0;
     bool ok = true;
     for (int64_t rnd = 0; ok; ++rnd) {
-      const int64_t idx = snake_item(rnd, cta, grid);
+      const int64_t idx = sched_item(p.g, rnd, cta, grid);
       if (idx >= n_items) break;
       const DqGeo t = dq_geo(p, idx);
       const int64_t r = t.r0 + row;

@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t itn = 0, kc = 0;
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
-        const int64_t idx = snake_item(rnd, cta, grid);
+        const int64_t idx = sched_item(p.g, rnd, cta, grid);
         if (idx >= n_items) break;
         const ItemGeo g = item_geo(p, idx);
         if (g.n == 0) continue;
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t itn = 0, kc = 0;
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
-        const int64_t idx = snake_item(rnd, cta, grid);
+        const int64_t idx = sched_item(p.g, rnd, cta, grid);
         if (idx >= n_items) break;
         const ItemGeo g = item_geo(p, idx);
         if (g.n == 0) continue;
@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t sc = 0, itn = 0;
     bool ok = true;
     for (int64_t rnd = 0; ok; ++rnd) {
-      const int64_t idx = snake_item(rnd, cta, grid);
+      const int64_t idx = sched_item(p.g, rnd, cta, grid);
       if (idx >= n_items) break;
       const ItemGeo g = item_geo(p, idx);
       const int64_t r = g.r0 + t * BM + row;

@@ -31,6 +31,7 @@ struct Geom {
   int Hq, Hkv;
   int64_t kv_begin, kv_end;  // clean key range of this call
   int include_local;         // corrupted rows also read their own block
+  int naive_order = 0;       // 1: items in natural order, round-robin over the grid
 };
 
 BDLM_HD int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
@@ -142,6 +143,14 @@ BDLM_HD QItem q_item(const Geom& g, int tq, int64_t idx) {
   const int64_t nqt = cdiv64(g.L, tq);
   const int64_t qb = q_block(g);
   QItem it;
+  if (g.naive_order) {  // natural order: first query tile first
+    const int64_t per = (int64_t)g.Hq * 2;
+    it.qtile = idx / per;
+    const int64_t rem = idx % per;
+    it.stream = (int)(rem % 2);
+    it.head = (int)(rem / 2);
+    return it;
+  }
   if (nqt < kBlockedMinQBlocks * qb) {
     const int64_t per = (int64_t)g.Hq * 2;
     it.qtile = nqt - 1 - idx / per;
@@ -187,6 +196,12 @@ BDLM_HD int64_t snake_item(int64_t round, int cta, int grid) {
   return round * grid + pos;
 }
 
+// Item of CTA `cta` in round r: the boustrophedon order above, or plain
+// round robin for the natural-order schedule (load-balancing ablation).
+BDLM_HD int64_t sched_item(const Geom& g, int64_t round, int cta, int grid) {
+  return g.naive_order ? round * grid + cta : snake_item(round, cta, grid);
+}
+
 // dK/dV work items: (key stream, key/value head, key tile).  Clean key tiles
 // first in increasing position (a clean key is read by every later row, so
 // earlier tiles carry more work), then corrupted key tiles (each read only by
@@ -229,7 +244,7 @@ BDLM_HD KVItem kv_item(const Geom& g, int tk, int64_t idx) {
     count = nc;
     it.key_stream = 1;
   }
-  if (count < kBlockedMinTiles) {
+  if (count < kBlockedMinTiles || g.naive_order) {
     // short range: tile-major, KV head minor (rounds of similar lengths)
     it.kv_head = (int)(i % g.Hkv);
     it.ktile = base + i / g.Hkv;

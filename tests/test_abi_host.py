@@ -155,3 +155,17 @@ def test_snake_assignment_balances_clean_costs(lib):
                 tot[c] += costs[i]
     assert tot.max() - tot.min() <= costs.max()
     assert tot.max() / tot.mean() < 1.01
+
+
+def test_naive_schedule_lists_items_in_natural_order(lib, monkeypatch):
+    """BDLM_SCHED=naive (the load-balancing ablation): query tiles from the
+    first to the last, the two streams of one head adjacent, then the heads."""
+    L, B, Hq, Hkv = 4096, 256, 4, 2
+    monkeypatch.setenv("BDLM_SCHED", "naive")
+    items = m.bdlm_worklist(L, B, Hq, Hkv)
+    monkeypatch.delenv("BDLM_SCHED")
+    lpt = m.bdlm_worklist(L, B, Hq, Hkv)
+    assert sorted(items) == sorted(lpt)
+    keys = [(t, h, s) for (s, h, t, *_rest) in items]
+    assert keys == sorted(keys)
+    assert [it[2] for it in lpt][0] == max(it[2] for it in lpt)
