@@ -194,6 +194,43 @@ bdlm_status bdlm_attn_bwd_shard(const void* Qc, const void* Kc, const void* Vc,
                                 float* dKc, float* dVc, float* dKn, float* dVn,
                                 void* workspace, size_t ws_bytes, bdlm_stream stream);
 
+/* ---- Packed variable-length batch (batch > 1) ---------------------------
+ * Several independent two-stream problems in one call, for batches of
+ * sequences (the pages tune the batch size alongside the parallelism:
+ * "Block Parallelism ...", nips.cc abstract).  n_seqs sequences are stored
+ * back to back along the token dimension: sequence s owns rows
+ * [seq_offsets[s], seq_offsets[s+1]) of both streams of Q/K/V/O/dO and of the
+ * gradients ([T, H, d], T = seq_offsets[n_seqs]) and the same columns of LSE
+ * ([Hq, T], natural log).  seq_offsets is a host array of n_seqs + 1 int64,
+ * seq_offsets[0] = 0, every sequence length a positive multiple of B; a row
+ * attends only within its own sequence, with the mask of the one-sequence
+ * calls.  All sequences run in one launch per kernel: the work items of all
+ * of them form one longest-first list (built on the host, copied into the
+ * workspace, so the host array may be freed on return).  Same conventions,
+ * dtypes and error behaviour as bdlm_attn_fwd / bdlm_attn_bwd.
+ *
+ * bdlm_workspace_size_varlen: bytes of workspace for op BDLM_OP_FWD or
+ * BDLM_OP_BWD (0 for another op or a bad shape). */
+size_t bdlm_workspace_size_varlen(int op, const int64_t* seq_offsets, int n_seqs, int Hq, int Hkv, int d);
+
+bdlm_status bdlm_attn_fwd_varlen(const void* Qc, const void* Kc, const void* Vc,
+                                 const void* Qn, const void* Kn, const void* Vn,
+                                 const int64_t* seq_offsets, int n_seqs, int64_t B,
+                                 int Hq, int Hkv, int d, float scale,
+                                 void* Oc, void* On, bdlm_dtype o_dtype,
+                                 float* LSEc, float* LSEn,
+                                 void* workspace, size_t ws_bytes, bdlm_stream stream);
+
+bdlm_status bdlm_attn_bwd_varlen(const void* Qc, const void* Kc, const void* Vc,
+                                 const void* Qn, const void* Kn, const void* Vn,
+                                 const void* Oc, const void* On, const void* dOc, const void* dOn,
+                                 const float* LSEc, const float* LSEn,
+                                 const int64_t* seq_offsets, int n_seqs, int64_t B,
+                                 int Hq, int Hkv, int d, float scale,
+                                 void* dQc, void* dKc, void* dVc, void* dQn, void* dKn, void* dVn,
+                                 bdlm_dtype g_dtype, void* workspace, size_t ws_bytes,
+                                 bdlm_stream stream);
+
 /* Host-only: the forward work list in launch order, for inspection and tests.
  * One item per (query tile of tile_q rows, query head, stream), longest
  * first: query tiles from the last to the first.  With at least

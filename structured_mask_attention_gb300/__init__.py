@@ -19,7 +19,7 @@ import re
 __all__ = [
     "BdlmError", "load_library", "bdlm_workspace_size", "bdlm_attn_fwd", "bdlm_attn_fwd_shard",
     "bdlm_lse_merge", "bdlm_bwd_preprocess", "bdlm_attn_bwd", "bdlm_attn_bwd_noalloc", "bdlm_attn_bwd_shard",
-    "bdlm_worklist",
+    "bdlm_worklist", "bdlm_workspace_size_varlen", "bdlm_attn_fwd_varlen", "bdlm_attn_bwd_varlen",
     "bdlm_sync_status", "bdlm_watchdog_selftest", "bdlm_kernel_launches", "bdlm_last_error",
     "bdlm_version", "bdlm_timing_enable", "bdlm_timing_report", "header_functions", "LIB_PATH",
     "HEADER_PATH",
@@ -61,6 +61,9 @@ _SIGS = {
                             + [_P, _SZ, _P]),
     "bdlm_attn_bwd_noalloc": (_I, [_P] * 12 + [_I64, _I64, _I, _I, _I, _F] + [_P] * 6 + [_I, _P]),
     "bdlm_worklist": (_I64, [_I64, _I64, _I, _I, _I, _I, _I64, _I64, _I, _P, _I64]),
+    "bdlm_workspace_size_varlen": (_SZ, [_I, _P, _I, _I, _I, _I]),
+    "bdlm_attn_fwd_varlen": (_I, [_P] * 6 + [_P, _I, _I64, _I, _I, _I, _F, _P, _P, _I, _P, _P, _P, _SZ, _P]),
+    "bdlm_attn_bwd_varlen": (_I, [_P] * 12 + [_P, _I, _I64, _I, _I, _I, _F] + [_P] * 6 + [_I, _P, _SZ, _P]),
     "bdlm_sync_status": (_I, [_P, _P]),
     "bdlm_watchdog_selftest": (_I, [_P, _SZ, ctypes.c_uint32, _P]),
     "bdlm_kernel_launches": (ctypes.c_uint64, []),
@@ -319,6 +322,82 @@ def bdlm_worklist(L: int, B: int, Hq: int, Hkv: int, tile_q: int = 256, tile_k: 
     lib.bdlm_worklist(L, B, Hq, Hkv, tile_q, tile_k, kv_begin, kv_end, int(include_local),
                       ctypes.cast(buf, ctypes.c_void_p), n)
     return [tuple(buf[8 * i:8 * i + 8]) for i in range(n)]
+
+
+def _offsets(seq_lens):
+    """Host int64 array of the n + 1 row offsets of packed sequences."""
+    lens = [int(x) for x in seq_lens]
+    arr = (ctypes.c_int64 * (len(lens) + 1))()
+    acc = 0
+    for i, n in enumerate(lens):
+        arr[i] = acc
+        acc += n
+    arr[len(lens)] = acc
+    return arr, len(lens), acc
+
+
+def bdlm_workspace_size_varlen(op: int, seq_lens, Hq: int, Hkv: int, d: int) -> int:
+    arr, n, _ = _offsets(seq_lens)
+    return load_library().bdlm_workspace_size_varlen(op, ctypes.cast(arr, ctypes.c_void_p), n, Hq, Hkv, d)
+
+
+def _workspace_varlen(op, seq_lens, Hq, Hkv, d, device, ws):
+    torch = _torch()
+    need = bdlm_workspace_size_varlen(op, seq_lens, Hq, Hkv, d)
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    return ws
+
+
+def bdlm_attn_fwd_varlen(Qc, Kc, Vc, Qn, Kn, Vn, seq_lens, B: int, scale: float | None = None, o_dtype=None,
+                         out=None, workspace=None, stream=None):
+    """Packed batch: sequences of the given lengths stored back to back along
+    the token dimension ([T, H, d], T = sum of the lengths).  Returns
+    (Oc, On, LSEc, LSEn) with LSE as [Hq, T]."""
+    torch = _torch()
+    _check_inputs(Qc, Kc, Vc, Qn, Kn, Vn)
+    T, Hq, Hkv, d = _shape(Qc, Kc)
+    arr, n, tot = _offsets(seq_lens)
+    if tot != T:
+        raise ValueError(f"sequence lengths sum to {tot}, tensors hold {T} rows")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o_dtype = torch.bfloat16 if o_dtype is None else o_dtype
+    if out is None:
+        out = (torch.empty((T, Hq, d), dtype=o_dtype, device=Qc.device),
+               torch.empty((T, Hq, d), dtype=o_dtype, device=Qc.device),
+               torch.empty((Hq, T), dtype=torch.float32, device=Qc.device),
+               torch.empty((Hq, T), dtype=torch.float32, device=Qc.device))
+    Oc, On, LSEc, LSEn = out
+    ws = _workspace_varlen(OP_FWD, seq_lens, Hq, Hkv, d, Qc.device, workspace)
+    _check(load_library().bdlm_attn_fwd_varlen(
+        _ptr(Qc), _ptr(Kc), _ptr(Vc), _ptr(Qn), _ptr(Kn), _ptr(Vn), ctypes.cast(arr, ctypes.c_void_p), n, B,
+        Hq, Hkv, d, scale, _ptr(Oc), _ptr(On), _dt(Oc.dtype), _ptr(LSEc), _ptr(LSEn), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return Oc, On, LSEc, LSEn
+
+
+def bdlm_attn_bwd_varlen(Qc, Kc, Vc, Qn, Kn, Vn, Oc, On, dOc, dOn, LSEc, LSEn, seq_lens, B: int,
+                         scale: float | None = None, g_dtype=None, out=None, workspace=None, stream=None):
+    """Gradients of a packed batch.  Returns (dQc, dKc, dVc, dQn, dKn, dVn)."""
+    torch = _torch()
+    _check_inputs(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn)
+    T, Hq, Hkv, d = _shape(Qc, Kc)
+    arr, n, tot = _offsets(seq_lens)
+    if tot != T:
+        raise ValueError(f"sequence lengths sum to {tot}, tensors hold {T} rows")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    g_dtype = torch.bfloat16 if g_dtype is None else g_dtype
+    if out is None:
+        mk = lambda H: torch.empty((T, H, d), dtype=g_dtype, device=Qc.device)
+        out = (mk(Hq), mk(Hkv), mk(Hkv), mk(Hq), mk(Hkv), mk(Hkv))
+    dQc, dKc, dVc, dQn, dKn, dVn = out
+    ws = _workspace_varlen(OP_BWD, seq_lens, Hq, Hkv, d, Qc.device, workspace)
+    _check(load_library().bdlm_attn_bwd_varlen(
+        _ptr(Qc), _ptr(Kc), _ptr(Vc), _ptr(Qn), _ptr(Kn), _ptr(Vn), _ptr(Oc), _ptr(On), _ptr(dOc), _ptr(dOn),
+        _ptr(LSEc), _ptr(LSEn), ctypes.cast(arr, ctypes.c_void_p), n, B, Hq, Hkv, d, scale,
+        _ptr(dQc), _ptr(dKc), _ptr(dVc), _ptr(dQn), _ptr(dKn), _ptr(dVn), _dt(dQc.dtype), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return out
 
 
 def bdlm_sync_status(workspace, stream=None):

@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <initializer_list>
@@ -242,7 +243,7 @@ bdlm_status finish(cudaError_t e, int launches, const char* what) {
 bdlm_status fwd_common(const void* Qc, const void* Kc, const void* Vc, const void* Qn, const void* Kn,
                        const void* Vn, int64_t L, int64_t B, int Hq, int Hkv, int d, float scale, int64_t kv_begin,
                        int64_t kv_end, int include_local, void* Oc, void* On, int o_f32, float* LSEc, float* LSEn,
-                       void* ws, size_t ws_bytes, cudaStream_t st) {
+                       void* ws, size_t ws_bytes, cudaStream_t st, const VarlenTabs* vt = nullptr) {
   DeviceInfo info;
   BDLM_CHECK(device_info(info));
   EncodeTiledFn enc;
@@ -263,13 +264,13 @@ bdlm_status fwd_common(const void* Qc, const void* Kc, const void* Vc, const voi
   p.o_f32 = o_f32;
   p.LSEc = LSEc;
   p.LSEn = LSEn;
-  p.n_items = q_items(p.g, kFwdItemRows);
+  p.n_items = vt ? vt->n_q : q_items(p.g, kFwdItemRows);
   p.status = static_cast<uint32_t*>(ws);
   p.limit_ns = wait_limit_ns();
   BDLM_CHECK(clear_status(ws, st));
   int launches = 0;
   ScopedKernelTimer tm(K_FWD, st);
-  cudaError_t e = launch_fwd(maps, p, d, info.sms, st, &launches);
+  cudaError_t e = launch_fwd(maps, p, vt, d, info.sms, st, &launches);
   tm.stop();
   return finish(e, launches, "forward launch");
 }
@@ -293,9 +294,9 @@ BwdParams bwd_params(const void* Qc, const void* Kc, const void* Vc, const void*
   return p;
 }
 
-// Launches the dK/dV pass then the dQ pass for the key set of p.
+// Launches the dK/dV pass then the dQ pass for the key set of p (vt: item tables of a packed batch, or null).
 cudaError_t launch_backward_passes(const BwdParams& p, const DeviceInfo& info, void* ws, cudaStream_t st,
-                                   int* launches, bdlm_status* vstatus) {
+                                   int* launches, bdlm_status* vstatus, const VarlenTabs* vt = nullptr) {
   *vstatus = BDLM_OK;
   EncodeTiledFn enc;
   if ((*vstatus = get_encoder(enc)) != BDLM_OK) return cudaSuccess;
@@ -311,11 +312,11 @@ cudaError_t launch_backward_passes(const BwdParams& p, const DeviceInfo& info, v
   cudaError_t e;
   {
     ScopedKernelTimer tm(K_DKV, st);
-    e = launch_bwd_dkv_tc(m, p, info.sms, status, wait_limit_ns(), st, launches);
+    e = launch_bwd_dkv_tc(m, p, vt, info.sms, status, wait_limit_ns(), st, launches);
   }
   if (e == cudaSuccess) {
     ScopedKernelTimer tm(K_DQ, st);
-    e = launch_bwd_dq_tc(m, p, info.sms, status, wait_limit_ns(), st, launches);
+    e = launch_bwd_dq_tc(m, p, vt, info.sms, status, wait_limit_ns(), st, launches);
   }
   return e;
 }
@@ -329,6 +330,103 @@ bdlm_status guarded(F&& f) {
   } catch (...) {
     return fail(BDLM_ERR_INVALID_ARG, "internal exception");
   }
+}
+
+
+// ------------------------------------------------------------ packed batch
+// Sequence s owns rows [off[s], off[s+1]) of the packed tensors; the kernels
+// read their items from tables built here, longest first over all sequences.
+constexpr int64_t kMaxSeqs = 1 << 20;
+
+bdlm_status check_varlen(const int64_t* off, int n, int64_t B, int Hq, int Hkv, int d, int64_t* T) {
+  if (!off) return fail(BDLM_ERR_INVALID_ARG, "seq_offsets is null");
+  if (n <= 0 || n > kMaxSeqs) return fail(BDLM_ERR_SHAPE, "n_seqs=%d must be in [1, 2^20]", n);
+  if (off[0] != 0) return fail(BDLM_ERR_SHAPE, "seq_offsets[0]=%lld must be 0", (long long)off[0]);
+  for (int s = 0; s < n; ++s) {
+    const int64_t len = off[s + 1] - off[s];
+    if (len <= 0 || (B > 0 && len % B))
+      return fail(BDLM_ERR_SHAPE, "sequence %d has length %lld: must be a positive multiple of B=%lld", s,
+                  (long long)len, (long long)B);
+  }
+  *T = off[n];
+  return check_shape(*T, B > 0 ? B : *T, Hq, Hkv, d);
+}
+
+int64_t varlen_q_count(const int64_t* off, int n, int Hq, int tq) {
+  int64_t c = 0;
+  for (int s = 0; s < n; ++s) c += cdiv64(off[s + 1] - off[s], tq) * Hq * 2;
+  return c;
+}
+
+int64_t varlen_kv_count(const int64_t* off, int n, int Hkv, int tk) {
+  int64_t c = 0;
+  for (int s = 0; s < n; ++s) c += cdiv64(off[s + 1] - off[s], tk) * 2 * Hkv;
+  return c;
+}
+
+// {sequence, stream + 2 * head, query tile, visible key tiles}, longest first
+std::vector<int4> varlen_q_table(const Geom& all, const int64_t* off, int n, int tq, int tk) {
+  std::vector<int4> v;
+  v.reserve((size_t)varlen_q_count(off, n, all.Hq, tq));
+  for (int s = 0; s < n; ++s) {
+    const Geom g = seq_geom(all, off[s + 1] - off[s]);
+    const int64_t nqt = cdiv64(g.L, tq);
+    for (int64_t qt = 0; qt < nqt; ++qt)
+      for (int h = 0; h < g.Hq; ++h)
+        for (int st = 0; st < 2; ++st) {
+          const int64_t r0 = qt * tq, r1 = imin64(r0 + tq, g.L);
+          const QTileRanges q = qtile_ranges(g, st, r0, r1, tk);
+          v.push_back(make_int4(s, st + 2 * h, (int)qt, (int)((q.c1 - q.c0) + (q.n1 - q.n0))));
+        }
+  }
+  std::stable_sort(v.begin(), v.end(), [](const int4& a, const int4& b) { return a.w > b.w; });
+  return v;
+}
+
+// {sequence, key stream + 2 * KV head, key tile, query rows that see it}, longest first
+std::vector<int4> varlen_kv_table(const Geom& all, const int64_t* off, int n, int tk) {
+  std::vector<int4> v;
+  v.reserve((size_t)varlen_kv_count(off, n, all.Hkv, tk));
+  for (int s = 0; s < n; ++s) {
+    const Geom g = seq_geom(all, off[s + 1] - off[s]);
+    const int64_t nt = cdiv64(g.L, tk);
+    for (int ks = 0; ks < 2; ++ks)
+      for (int h = 0; h < g.Hkv; ++h)
+        for (int64_t kt = 0; kt < nt; ++kt) {
+          int64_t cl, ch, nl, nh;
+          kv_tile_rows(g, ks, kt * tk, imin64(kt * tk + tk, g.L), cl, ch, nl, nh);
+          const int64_t rows = imax64(0, ch - cl) + imax64(0, nh - nl);
+          v.push_back(make_int4(s, ks + 2 * h, (int)kt, (int)rows));
+        }
+  }
+  std::stable_sort(v.begin(), v.end(), [](const int4& a, const int4& b) { return a.w > b.w; });
+  return v;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workspace of a packed-batch call: header, [D of both streams], offsets, item tables.
+struct VarlenLayout {
+  size_t d_bytes, off_at, q_at, kv_at, total;
+};
+VarlenLayout varlen_layout(int op, const int64_t* off, int n, int Hq, int Hkv, int64_t T) {
+  VarlenLayout l;
+  l.d_bytes = op == BDLM_OP_BWD ? round256(2 * (size_t)Hq * (size_t)T * sizeof(float)) : 0;
+  l.off_at = kWsHeader + l.d_bytes;
+  l.q_at = l.off_at + round256((size_t)(n + 1) * sizeof(int64_t));
+  const int64_t nq = op == BDLM_OP_BWD ? varlen_q_count(off, n, Hq, kBwdTile) : varlen_q_count(off, n, Hq, kFwdItemRows);
+  l.kv_at = l.q_at + round256((size_t)nq * sizeof(int4));
+  const int64_t nkv = op == BDLM_OP_BWD ? varlen_kv_count(off, n, Hkv, kBwdTile) : 0;
+  l.total = l.kv_at + round256((size_t)nkv * sizeof(int4));
+  return l;
+}
+
+bdlm_status upload(void* dst, const void* src, size_t bytes, cudaStream_t st) {
+  if (!bytes) return BDLM_OK;
+  // pageable source: the copy is staged before the call returns
+  cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(work list)");
+  return BDLM_OK;
 }
 
 }  // namespace
@@ -615,6 +713,96 @@ int64_t bdlm_timing_report(char* buf, int64_t cap, int reset) {
   } catch (...) {
     return -1;
   }
+}
+
+
+// ------------------------------------------------------------ packed batch
+size_t bdlm_workspace_size_varlen(int op, const int64_t* seq_offsets, int n_seqs, int Hq, int Hkv, int d) {
+  try {
+    if (op != BDLM_OP_FWD && op != BDLM_OP_BWD) return 0;
+    int64_t T;
+    if (check_varlen(seq_offsets, n_seqs, 0, Hq, Hkv, d, &T) != BDLM_OK) return 0;
+    return varlen_layout(op, seq_offsets, n_seqs, Hq, Hkv, T).total;
+  } catch (...) {
+    return 0;
+  }
+}
+
+bdlm_status bdlm_attn_fwd_varlen(const void* Qc, const void* Kc, const void* Vc, const void* Qn, const void* Kn,
+                                 const void* Vn, const int64_t* seq_offsets, int n_seqs, int64_t B, int Hq,
+                                 int Hkv, int d, float scale, void* Oc, void* On, bdlm_dtype o_dtype, float* LSEc,
+                                 float* LSEn, void* workspace, size_t ws_bytes, bdlm_stream stream) {
+  return guarded([&]() -> bdlm_status {
+    int64_t T;
+    BDLM_CHECK(check_varlen(seq_offsets, n_seqs, B, Hq, Hkv, d, &T));
+    BDLM_CHECK(check_scale(scale));
+    if (o_dtype != BDLM_BF16 && o_dtype != BDLM_F32) return fail(BDLM_ERR_INVALID_ARG, "bad o_dtype %d", (int)o_dtype);
+    BDLM_CHECK(check_ptrs("bdlm_attn_fwd_varlen(Qc,Kc,Vc,Qn,Kn,Vn,Oc,On,LSEc,LSEn)",
+                          {Qc, Kc, Vc, Qn, Kn, Vn, Oc, On, LSEc, LSEn}));
+    const VarlenLayout lay = varlen_layout(BDLM_OP_FWD, seq_offsets, n_seqs, Hq, Hkv, T);
+    BDLM_CHECK(check_ws(workspace, ws_bytes, lay.total));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char* w = static_cast<char*>(workspace);
+    const Geom all{T, B, Hq, Hkv, 0, T, 1};
+    const std::vector<int4> tab = varlen_q_table(all, seq_offsets, n_seqs, kFwdItemRows, kFwdTileK);
+    BDLM_CHECK(upload(w + lay.off_at, seq_offsets, (size_t)(n_seqs + 1) * sizeof(int64_t), st));
+    BDLM_CHECK(upload(w + lay.q_at, tab.data(), tab.size() * sizeof(int4), st));
+    const VarlenTabs vt{reinterpret_cast<const int4*>(w + lay.q_at), nullptr,
+                        reinterpret_cast<const int64_t*>(w + lay.off_at), (int64_t)tab.size(), 0};
+    return fwd_common(Qc, Kc, Vc, Qn, Kn, Vn, T, B, Hq, Hkv, d, scale, 0, T, 1, Oc, On, o_dtype == BDLM_F32, LSEc,
+                      LSEn, workspace, ws_bytes, st, &vt);
+  });
+}
+
+bdlm_status bdlm_attn_bwd_varlen(const void* Qc, const void* Kc, const void* Vc, const void* Qn, const void* Kn,
+                                 const void* Vn, const void* Oc, const void* On, const void* dOc, const void* dOn,
+                                 const float* LSEc, const float* LSEn, const int64_t* seq_offsets, int n_seqs,
+                                 int64_t B, int Hq, int Hkv, int d, float scale, void* dQc, void* dKc, void* dVc,
+                                 void* dQn, void* dKn, void* dVn, bdlm_dtype g_dtype, void* workspace, size_t ws_bytes,
+                                 bdlm_stream stream) {
+  return guarded([&]() -> bdlm_status {
+    int64_t T;
+    BDLM_CHECK(check_varlen(seq_offsets, n_seqs, B, Hq, Hkv, d, &T));
+    BDLM_CHECK(check_scale(scale));
+    if (g_dtype != BDLM_BF16 && g_dtype != BDLM_F32) return fail(BDLM_ERR_INVALID_ARG, "bad g_dtype %d", (int)g_dtype);
+    BDLM_CHECK(check_ptrs("bdlm_attn_bwd_varlen(Qc,Kc,Vc,Qn,Kn,Vn,Oc,On,dOc,dOn,LSEc,LSEn)",
+                          {Qc, Kc, Vc, Qn, Kn, Vn, Oc, On, dOc, dOn, LSEc, LSEn}));
+    BDLM_CHECK(check_ptrs("bdlm_attn_bwd_varlen(dQc,dKc,dVc,dQn,dKn,dVn)", {dQc, dKc, dVc, dQn, dKn, dVn}));
+    const VarlenLayout lay = varlen_layout(BDLM_OP_BWD, seq_offsets, n_seqs, Hq, Hkv, T);
+    BDLM_CHECK(check_ws(workspace, ws_bytes, lay.total));
+    DeviceInfo info;
+    BDLM_CHECK(device_info(info));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char* w = static_cast<char*>(workspace);
+    float* Dc = reinterpret_cast<float*>(w + kWsHeader);
+    float* Dn = Dc + (size_t)Hq * T;
+    const Geom all{T, B, Hq, Hkv, 0, T, 1};
+    const std::vector<int4> qt = varlen_q_table(all, seq_offsets, n_seqs, kBwdTile, kBwdTile);
+    const std::vector<int4> kvt = varlen_kv_table(all, seq_offsets, n_seqs, kBwdTile);
+    BDLM_CHECK(clear_status(workspace, st));
+    BDLM_CHECK(upload(w + lay.off_at, seq_offsets, (size_t)(n_seqs + 1) * sizeof(int64_t), st));
+    BDLM_CHECK(upload(w + lay.q_at, qt.data(), qt.size() * sizeof(int4), st));
+    BDLM_CHECK(upload(w + lay.kv_at, kvt.data(), kvt.size() * sizeof(int4), st));
+    int launches = 0;
+    cudaError_t e;
+    {
+      ScopedKernelTimer tm(K_PREP, st);
+      e = launch_preprocess(Oc, 0, dOc, T, Hq, d, Dc, st, &launches);
+    }
+    if (e == cudaSuccess) {
+      ScopedKernelTimer tm(K_PREP, st);
+      e = launch_preprocess(On, 0, dOn, T, Hq, d, Dn, st, &launches);
+    }
+    BwdParams p = bwd_params(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn, T, B, Hq, Hkv, d, scale, 0, T, 1);
+    p.dQc = dQc; p.dQn = dQn; p.dKc = dKc; p.dVc = dVc; p.dKn = dKn; p.dVn = dVn;
+    p.g_f32 = g_dtype == BDLM_F32;
+    const VarlenTabs vt{reinterpret_cast<const int4*>(w + lay.q_at), reinterpret_cast<const int4*>(w + lay.kv_at),
+                        reinterpret_cast<const int64_t*>(w + lay.off_at), (int64_t)qt.size(), (int64_t)kvt.size()};
+    bdlm_status vs = BDLM_OK;
+    if (e == cudaSuccess) e = launch_backward_passes(p, info, workspace, st, &launches, &vs, &vt);
+    if (vs != BDLM_OK) return vs;
+    return finish(e, launches, "varlen backward launch");
+  });
 }
 
 uint64_t bdlm_kernel_launches(void) { return g_launches.load(); }

@@ -54,16 +54,31 @@ struct DkvGeo {
   int64_t t00, t01;                // first query tile of each stream
   int nt0, nt1;                    // query tiles of each stream
   int per_head, n;                 // steps per head, total steps
+  int64_t off, L;                  // first row of the item's sequence in the packed tensors, its length
 };
 
-__device__ __forceinline__ DkvGeo dkv_geo(const BwdParams& p, int64_t idx) {
+// VL: packed variable-length batch (a separate instantiation).
+template <bool VL>
+__device__ __forceinline__ DkvGeo dkv_geo(const BwdParams& p, const VarlenTabs& vt, int64_t idx) {
   DkvGeo t;
-  const KVItem it = kv_item(p.g, KBM, idx);
-  t.ks = it.key_stream;
-  t.kvh = it.kv_head;
-  t.j0 = it.ktile * KBM;
-  const int64_t j1 = imin64(t.j0 + KBM, p.g.L);
-  kv_tile_rows(p.g, t.ks, t.j0, j1, t.rlo0, t.rhi0, t.rlo1, t.rhi1);
+  Geom g = p.g;
+  t.off = 0;
+  if (VL) {  // packed batch: the item and its sequence from the tables
+    const int4 e = vt.kv_items[idx];
+    t.ks = e.y & 1;
+    t.kvh = e.y >> 1;
+    t.j0 = (int64_t)e.z * KBM;
+    t.off = vt.seq_off[e.x];
+    g = seq_geom(p.g, vt.seq_off[e.x + 1] - t.off);
+  } else {
+    const KVItem it = kv_item(p.g, KBM, idx);
+    t.ks = it.key_stream;
+    t.kvh = it.kv_head;
+    t.j0 = it.ktile * KBM;
+  }
+  t.L = g.L;
+  const int64_t j1 = imin64(t.j0 + KBM, g.L);
+  kv_tile_rows(g, t.ks, t.j0, j1, t.rlo0, t.rhi0, t.rlo1, t.rhi1);
   if (t.rhi0 > t.rlo0) {
     t.t00 = t.rlo0 / KBN;
     t.nt0 = (int)(cdiv64(t.rhi0, KBN) - t.t00);
@@ -147,13 +162,14 @@ __device__ __forceinline__ void p_cols32(const uint32_t (&us)[32], const float* 
   }
 }
 
-template <int HD>
+template <int HD, bool VL>
 __global__ void __launch_bounds__(kThreads, 1)
     bdlm_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tQc, const __grid_constant__ CUtensorMap tQn,
                            const __grid_constant__ CUtensorMap tdOc, const __grid_constant__ CUtensorMap tdOn,
                            const __grid_constant__ CUtensorMap tKc, const __grid_constant__ CUtensorMap tKn,
                            const __grid_constant__ CUtensorMap tVc, const __grid_constant__ CUtensorMap tVn,
-                           const BwdParams p, const int64_t n_items, uint32_t* status, const uint64_t limit_ns) {
+                           const BwdParams p, const VarlenTabs vt, const int64_t n_items, uint32_t* status,
+                           const uint64_t limit_ns) {
   using LY = DkvLayout<HD>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -203,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t rnd = 0; ok; ++rnd) {
       const int64_t idx = sched_item(p.g, rnd, cta, grid);
       if (idx >= n_items) break;
-      const DkvGeo t = dkv_geo(p, idx);
+      const DkvGeo t = dkv_geo<VL>(p, vt, idx);
       if (t.n == 0) continue;
       if (itn > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(BAR(KV_KE), (itn - 1) & 1, wd, 41));
@@ -215,8 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* mv = t.ks ? &tVn : &tVc;
 #pragma unroll
         for (int pn = 0; pn < HD / 64; ++pn) {
-          tma_load_3d(sK + pn * LY::kPanel, mk, BAR(KV_KF), pn * 64, t.kvh, (int)t.j0);
-          tma_load_3d(sV + pn * LY::kPanel, mv, BAR(KV_KF), pn * 64, t.kvh, (int)t.j0);
+          tma_load_3d(sK + pn * LY::kPanel, mk, BAR(KV_KF), pn * 64, t.kvh, (int)((VL ? t.off : 0) + t.j0));
+          tma_load_3d(sV + pn * LY::kPanel, mv, BAR(KV_KF), pn * 64, t.kvh, (int)((VL ? t.off : 0) + t.j0));
         }
       }
       DkvCursor cur;
@@ -236,18 +252,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const CUtensorMap* mo = s ? &tdOn : &tdOc;
 #pragma unroll
           for (int pn = 0; pn < HD / 64; ++pn) {
-            tma_load_3d(sQ + st * LY::kTile + pn * LY::kPanel, mq, BAR(KV_QF + st), pn * 64, head, (int)q0);
-            tma_load_3d(sdO + st * LY::kTile + pn * LY::kPanel, mo, BAR(KV_QF + st), pn * 64, head, (int)q0);
+            tma_load_3d(sQ + st * LY::kTile + pn * LY::kPanel, mq, BAR(KV_QF + st), pn * 64, head,
+                        (int)((VL ? t.off : 0) + q0));
+            tma_load_3d(sdO + st * LY::kTile + pn * LY::kPanel, mo, BAR(KV_QF + st), pn * 64, head,
+                        (int)((VL ? t.off : 0) + q0));
           }
         }
         // LSE and D of the tile's 128 rows, asynchronously (rows >= L read as 0)
-        const float* LSE = (s ? p.LSEn : p.LSEc) + (int64_t)head * p.g.L;
-        const float* Dr = (s ? p.Dn : p.Dc) + (int64_t)head * p.g.L;
+        const float* LSE = (s ? p.LSEn : p.LSEc) + (int64_t)head * p.g.L + (VL ? t.off : 0);
+        const float* Dr = (s ? p.Dn : p.Dc) + (int64_t)head * p.g.L + (VL ? t.off : 0);
         const uint32_t stat = sStat + st * 2 * KBN * 4;
 #pragma unroll
         for (int c = R.lane; c < KBN; c += 32) {
           const int64_t r = q0 + c;
-          const bool v = r < p.g.L;
+          const bool v = r < (VL ? t.L : p.g.L);
           cp_async4(stat + c * 4, LSE + (v ? r : 0), v);
           cp_async4(stat + (KBN + c) * 4, Dr + (v ? r : 0), v);
         }
@@ -267,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t rnd = 0; ok; ++rnd) {
         const int64_t idx = sched_item(p.g, rnd, cta, grid);
         if (idx >= n_items) break;
-        const DkvGeo t = dkv_geo(p, idx);
+        const DkvGeo t = dkv_geo<VL>(p, vt, idx);
         if (t.n == 0) continue;
         if (!mbar_wait(BAR(KV_KF), itn & 1, wd, 43)) { ok = false; break; }
         const uint32_t q_base = qc;
@@ -334,22 +352,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t rnd = 0; ok; ++rnd) {
       const int64_t idx = sched_item(p.g, rnd, cta, grid);
       if (idx >= n_items) break;
-      const DkvGeo t = dkv_geo(p, idx);
+      const DkvGeo t = dkv_geo<VL>(p, vt, idx);
       if (t.n == 0) continue;
       const int64_t j = t.j0 + row;
       // query-row bounds as 32-bit values (rows are TMA coordinates, < 2^31):
       // rows of each stream this key sees, and rows every key of the tile sees
       int kl[2], kh[2], al[2], ah[2];
       {
-        const int64_t jl = imin64(t.j0 + KBM, p.g.L) - 1;
-        bool all_in = t.j0 + KBM <= p.g.L;
-        if (t.ks == 0) all_in = all_in && t.j0 >= p.g.kv_begin && t.j0 + KBM <= p.g.kv_end;
+        const Geom gm = VL ? seq_geom(p.g, t.L) : p.g;
+        const int64_t jl = imin64(t.j0 + KBM, gm.L) - 1;
+        bool all_in = t.j0 + KBM <= gm.L;
+        if (t.ks == 0) all_in = all_in && t.j0 >= gm.kv_begin && t.j0 + KBM <= gm.kv_end;
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           int64_t lo, hi, a0, b0, a1, b1;
-          key_rows(p.g, t.ks, j, s, lo, hi);
-          key_rows(p.g, t.ks, t.j0, s, a0, b0);
-          key_rows(p.g, t.ks, jl, s, a1, b1);
+          key_rows(gm, t.ks, j, s, lo, hi);
+          key_rows(gm, t.ks, t.j0, s, a0, b0);
+          key_rows(gm, t.ks, jl, s, a1, b1);
           kl[s] = (int)lo;
           kh[s] = (int)hi;
           al[s] = (int)imax64(a0, a1);
@@ -424,10 +443,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       // the key set of this call: clean keys in [kv_begin, kv_end), corrupted keys all
-      const bool wr = j < p.g.L && (t.ks == 1 || (j >= p.g.kv_begin && j < p.g.kv_end));
+      const bool wr = VL ? j < t.L
+                         : j < p.g.L && (t.ks == 1 || (j >= p.g.kv_begin && j < p.g.kv_end));
       void* dKo = t.ks ? p.dKn : p.dKc;
       void* dVo = t.ks ? p.dVn : p.dVc;
-      const int64_t oofs = (j * p.g.Hkv + t.kvh) * HD + half * (HD / 2);
+      const int64_t oofs = (((VL ? t.off : 0) + j) * p.g.Hkv + t.kvh) * HD + half * (HD / 2);
 #pragma unroll
       for (int c4 = 0; c4 < HD / 64; ++c4) {
         uint32_t uk[32], uv[32];
@@ -453,25 +473,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_bwd_dkv_tc(const BwdMaps& m, const BwdParams& p, int num_sms, uint32_t* status,
-                              uint64_t limit_ns, cudaStream_t stream, int* launches) {
-  const int64_t n = kv_items(p.g, KBM);
+template <int HD, bool VL>
+cudaError_t launch_dkv_t(const BwdMaps& m, const BwdParams& p, const VarlenTabs& vt, int64_t n, int grid,
+                         uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {
+  auto k = bdlm_bwd_dkv_tc_kernel<HD, VL>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvLayout<HD>::kAlloc);
+  if (e != cudaSuccess) return e;
+  k<<<grid, kThreads, DkvLayout<HD>::kAlloc, stream>>>(m.Qc, m.Qn, m.dOc, m.dOn, m.Kc, m.Kn, m.Vc, m.Vn, p, vt, n,
+                                                        status, limit_ns);
+  return cudaSuccess;
+}
+
+cudaError_t launch_bwd_dkv_tc(const BwdMaps& m, const BwdParams& p, const VarlenTabs* vt, int num_sms,
+                              uint32_t* status, uint64_t limit_ns, cudaStream_t stream, int* launches) {
+  const int64_t n = vt ? vt->n_kv : kv_items(p.g, KBM);
   if (n == 0) return cudaSuccess;
   const int grid = (int)(n < num_sms ? n : num_sms);
-  cudaError_t e;
-  if (p.d == 128) {
-    e = cudaFuncSetAttribute(bdlm_bwd_dkv_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DkvLayout<128>::kAlloc);
-    if (e != cudaSuccess) return e;
-    bdlm_bwd_dkv_tc_kernel<128><<<grid, kThreads, DkvLayout<128>::kAlloc, stream>>>(
-        m.Qc, m.Qn, m.dOc, m.dOn, m.Kc, m.Kn, m.Vc, m.Vn, p, n, status, limit_ns);
-  } else {
-    e = cudaFuncSetAttribute(bdlm_bwd_dkv_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DkvLayout<64>::kAlloc);
-    if (e != cudaSuccess) return e;
-    bdlm_bwd_dkv_tc_kernel<64><<<grid, kThreads, DkvLayout<64>::kAlloc, stream>>>(
-        m.Qc, m.Qn, m.dOc, m.dOn, m.Kc, m.Kn, m.Vc, m.Vn, p, n, status, limit_ns);
-  }
+  const VarlenTabs none{nullptr, nullptr, nullptr, 0, 0};
+  const VarlenTabs& t = vt ? *vt : none;
+  cudaError_t e = p.d == 128 ? (vt ? launch_dkv_t<128, true>(m, p, t, n, grid, status, limit_ns, stream)
+                                   : launch_dkv_t<128, false>(m, p, t, n, grid, status, limit_ns, stream))
+                             : (vt ? launch_dkv_t<64, true>(m, p, t, n, grid, status, limit_ns, stream)
+                                   : launch_dkv_t<64, false>(m, p, t, n, grid, status, limit_ns, stream));
+  if (e != cudaSuccess) return e;
   if (launches) ++*launches;
   return cudaGetLastError();
 }

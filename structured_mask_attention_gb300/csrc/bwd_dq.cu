@@ -51,18 +51,35 @@ struct DqGeo {
   int64_t r0;
   QTileRanges q;
   int nc, n;
-  int rot;  // the clean-key sweep starts at clean tile c0 + rot
+  int rot;         // the clean-key sweep starts at clean tile c0 + rot
+  int64_t off, L;  // first row of the item's sequence in the packed tensors, its length
 };
 
-__device__ __forceinline__ DqGeo dq_geo(const BwdParams& p, int64_t idx) {
+// VL: packed variable-length batch (a separate instantiation).
+template <bool VL>
+__device__ __forceinline__ DqGeo dq_geo(const BwdParams& p, const VarlenTabs& vt, int64_t idx) {
   DqGeo t;
-  const QItem it = q_item(p.g, QBM, idx);
-  t.stream = it.stream;
-  t.head = it.head;
-  t.kvh = it.head / (p.g.Hq / p.g.Hkv);
-  t.r0 = it.qtile * QBM;
-  const int64_t r1 = imin64(t.r0 + QBM, p.g.L);
-  t.q = qtile_ranges(p.g, t.stream, t.r0, r1, QBN);
+  Geom g = p.g;
+  int64_t qtile;
+  t.off = 0;
+  if (VL) {  // packed batch: the item and its sequence from the tables
+    const int4 e = vt.q_items[idx];
+    t.stream = e.y & 1;
+    t.head = e.y >> 1;
+    qtile = e.z;
+    t.off = vt.seq_off[e.x];
+    g = seq_geom(p.g, vt.seq_off[e.x + 1] - t.off);
+  } else {
+    const QItem it = q_item(p.g, QBM, idx);
+    t.stream = it.stream;
+    t.head = it.head;
+    qtile = it.qtile;
+  }
+  t.L = g.L;
+  t.kvh = t.head / (p.g.Hq / p.g.Hkv);
+  t.r0 = qtile * QBM;
+  const int64_t r1 = imin64(t.r0 + QBM, g.L);
+  t.q = qtile_ranges(g, t.stream, t.r0, r1, QBN);
   t.nc = (int)(t.q.c1 - t.q.c0);
   t.n = t.nc + (int)(t.q.n1 - t.q.n0);
   t.rot = sweep_rotation(idx, t.nc);
@@ -77,13 +94,14 @@ __device__ __forceinline__ int dq_key0(const DqGeo& t, int j) {
   return (int)((j < t.nc ? t.q.c0 + c : t.q.n0 + (j - t.nc)) * QBN);
 }
 
-template <int HD>
+template <int HD, bool VL>
 __global__ void __launch_bounds__(kThreads, 1)
     bdlm_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tQc, const __grid_constant__ CUtensorMap tQn,
                           const __grid_constant__ CUtensorMap tdOc, const __grid_constant__ CUtensorMap tdOn,
                           const __grid_constant__ CUtensorMap tKc, const __grid_constant__ CUtensorMap tKn,
                           const __grid_constant__ CUtensorMap tVc, const __grid_constant__ CUtensorMap tVn,
-                          const BwdParams p, const int64_t n_items, uint32_t* status, const uint64_t limit_ns) {
+                          const BwdParams p, const VarlenTabs vt, const int64_t n_items, uint32_t* status,
+                          const uint64_t limit_ns) {
   using LY = DqLayout<HD>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -136,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t rnd = 0; ok; ++rnd) {
         const int64_t idx = sched_item(p.g, rnd, cta, grid);
         if (idx >= n_items) break;
-        const DqGeo t = dq_geo(p, idx);
+        const DqGeo t = dq_geo<VL>(p, vt, idx);
         if (t.n == 0) continue;
         if (itn > 0 && !mbar_wait(BAR(DQ_QE), (itn - 1) & 1, wd, 21)) { ok = false; break; }
         mbar_arrive_expect_tx(BAR(DQ_QF), 2 * LY::kTile);
@@ -144,13 +162,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* mo = t.stream ? &tdOn : &tdOc;
 #pragma unroll
         for (int pn = 0; pn < HD / 64; ++pn) {
-          tma_load_3d(sQ + pn * LY::kPanel, mq, BAR(DQ_QF), pn * 64, t.head, (int)t.r0);
-          tma_load_3d(sdO + pn * LY::kPanel, mo, BAR(DQ_QF), pn * 64, t.head, (int)t.r0);
+          tma_load_3d(sQ + pn * LY::kPanel, mq, BAR(DQ_QF), pn * 64, t.head, (int)((VL ? t.off : 0) + t.r0));
+          tma_load_3d(sdO + pn * LY::kPanel, mo, BAR(DQ_QF), pn * 64, t.head, (int)((VL ? t.off : 0) + t.r0));
         }
         ++itn;
         for (int j = 0; j < t.n; ++j, ++g) {
           const bool cs = j < t.nc;
-          const int key0 = dq_key0(t, j);
+          const int key0 = (int)((VL ? t.off : 0) + dq_key0(t, j));  // packed-tensor row
           const int ks = g % KNS, vs = g & 1;
           if (g >= KNS && !mbar_wait(BAR(DQ_KE + ks), ((g / KNS) - 1) & 1, wd, 22)) { ok = false; break; }
           mbar_arrive_expect_tx(BAR(DQ_KF + ks), LY::kTile);
@@ -179,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t rnd = 0; ok; ++rnd) {
         const int64_t idx = sched_item(p.g, rnd, cta, grid);
         if (idx >= n_items) break;
-        const DqGeo t = dq_geo(p, idx);
+        const DqGeo t = dq_geo<VL>(p, vt, idx);
         if (t.n == 0) continue;
         if (!mbar_wait(BAR(DQ_QF), itn & 1, wd, 24)) { ok = false; break; }
         // stage of the previous step (read by its dQ MMA)
@@ -245,11 +263,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t rnd = 0; ok; ++rnd) {
       const int64_t idx = sched_item(p.g, rnd, cta, grid);
       if (idx >= n_items) break;
-      const DqGeo t = dq_geo(p, idx);
-      const int64_t r = t.r0 + row;
-      const bool valid = r < p.g.L;
+      const DqGeo t = dq_geo<VL>(p, vt, idx);
+      // (one sequence: its length and offset come from the parameters)
+      const int64_t seqL = VL ? t.L : p.g.L, seq0 = VL ? t.off : 0;
+      const int64_t r = t.r0 + row;  // row within the item's sequence
+      const bool valid = r < seqL;
       void* dqbase = t.stream ? p.dQn : p.dQc;
-      const int64_t oofs = (r * p.g.Hq + t.head) * HD + half * (HD / 2);
+      const int64_t oofs = ((seq0 + r) * p.g.Hq + t.head) * HD + half * (HD / 2);
       if (t.n == 0) {
         // no visible key for the whole tile: dQ rows are zero
         if (valid && !p.dq_accumulate) {
@@ -265,18 +285,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      const int64_t rr = valid ? r : p.g.L - 1;
+      const int64_t rr = valid ? r : seqL - 1;
+      const Geom gm = VL ? seq_geom(p.g, t.L) : p.g;
       int64_t clo, chi, nlo, nhi;
-      clean_interval(p.g, t.stream, rr, clo, chi);
-      noisy_interval(p.g, t.stream, rr, nlo, nhi);
-      const float nlse2 = valid ? -(t.stream ? p.LSEn : p.LSEc)[(int64_t)t.head * p.g.L + r] * kLog2e : 0.f;
-      const float Dv = valid ? (t.stream ? p.Dn : p.Dc)[(int64_t)t.head * p.g.L + r] : 0.f;
+      clean_interval(gm, t.stream, rr, clo, chi);
+      noisy_interval(gm, t.stream, rr, nlo, nhi);
+      const int64_t srow = (int64_t)t.head * p.g.L + seq0 + r;  // [H, rows] statistics
+      const float nlse2 = valid ? -(t.stream ? p.LSEn : p.LSEc)[srow] * kLog2e : 0.f;
+      const float Dv = valid ? (t.stream ? p.Dn : p.Dc)[srow] : 0.f;
       const uint64_t sl2x2 = f2(p.scale_log2, p.scale_log2), nl2 = f2(nlse2, nlse2), nD2 = f2(-Dv, -Dv);
       for (int j = 0; j < t.n; ++j, ++g) {
         const bool cs = j < t.nc;
         const int64_t key0 = dq_key0(t, j);
-        const bool full = cs ? tile_full(key0, QBN, t.q.c_all_lo, t.q.c_all_hi, p.g.L)
-                             : tile_full(key0, QBN, t.q.n_all_lo, t.q.n_all_hi, p.g.L);
+        const bool full = cs ? tile_full(key0, QBN, t.q.c_all_lo, t.q.c_all_hi, seqL)
+                             : tile_full(key0, QBN, t.q.n_all_lo, t.q.n_all_hi, seqL);
         const int b = g & 1;
         // dP(j) complete (its commit follows S(j)'s MMAs)
         ok = mbar_wait(BAR(DQ_DPF), g & 1, wd, 31);
@@ -335,25 +357,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_bwd_dq_tc(const BwdMaps& m, const BwdParams& p, int num_sms, uint32_t* status,
-                             uint64_t limit_ns, cudaStream_t stream, int* launches) {
-  const int64_t n = q_items(p.g, QBM);
+template <int HD, bool VL>
+cudaError_t launch_dq_t(const BwdMaps& m, const BwdParams& p, const VarlenTabs& vt, int64_t n, int grid,
+                        uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {
+  auto k = bdlm_bwd_dq_tc_kernel<HD, VL>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<HD>::kAlloc);
+  if (e != cudaSuccess) return e;
+  k<<<grid, kThreads, DqLayout<HD>::kAlloc, stream>>>(m.Qc, m.Qn, m.dOc, m.dOn, m.Kc, m.Kn, m.Vc, m.Vn, p, vt, n,
+                                                       status, limit_ns);
+  return cudaSuccess;
+}
+
+cudaError_t launch_bwd_dq_tc(const BwdMaps& m, const BwdParams& p, const VarlenTabs* vt, int num_sms,
+                             uint32_t* status, uint64_t limit_ns, cudaStream_t stream, int* launches) {
+  const int64_t n = vt ? vt->n_q : q_items(p.g, QBM);
   if (n == 0) return cudaSuccess;
   const int grid = (int)(n < num_sms ? n : num_sms);
-  cudaError_t e;
-  if (p.d == 128) {
-    e = cudaFuncSetAttribute(bdlm_bwd_dq_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DqLayout<128>::kAlloc);
-    if (e != cudaSuccess) return e;
-    bdlm_bwd_dq_tc_kernel<128><<<grid, kThreads, DqLayout<128>::kAlloc, stream>>>(
-        m.Qc, m.Qn, m.dOc, m.dOn, m.Kc, m.Kn, m.Vc, m.Vn, p, n, status, limit_ns);
-  } else {
-    e = cudaFuncSetAttribute(bdlm_bwd_dq_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DqLayout<64>::kAlloc);
-    if (e != cudaSuccess) return e;
-    bdlm_bwd_dq_tc_kernel<64><<<grid, kThreads, DqLayout<64>::kAlloc, stream>>>(
-        m.Qc, m.Qn, m.dOc, m.dOn, m.Kc, m.Kn, m.Vc, m.Vn, p, n, status, limit_ns);
-  }
+  const VarlenTabs none{nullptr, nullptr, nullptr, 0, 0};
+  const VarlenTabs& t = vt ? *vt : none;
+  cudaError_t e = p.d == 128 ? (vt ? launch_dq_t<128, true>(m, p, t, n, grid, status, limit_ns, stream)
+                                   : launch_dq_t<128, false>(m, p, t, n, grid, status, limit_ns, stream))
+                             : (vt ? launch_dq_t<64, true>(m, p, t, n, grid, status, limit_ns, stream)
+                                   : launch_dq_t<64, false>(m, p, t, n, grid, status, limit_ns, stream));
+  if (e != cudaSuccess) return e;
   if (launches) ++*launches;
   return cudaGetLastError();
 }

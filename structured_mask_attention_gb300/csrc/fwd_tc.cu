@@ -70,21 +70,45 @@ struct ItemGeo {
   QTileRanges q;
   int nc, n;  // clean key tiles, all key tiles
   int rot;    // the clean-key sweep starts at clean tile c0 + rot
+  int64_t off, L;  // first row of the item's sequence in the packed tensors, its length
 };
 
-__device__ __forceinline__ ItemGeo item_geo(const FwdParams& p, int64_t idx) {
+// VL: packed variable-length batch (a separate instantiation, so that the
+// one-sequence kernel keeps its register budget).
+template <bool VL>
+__device__ __forceinline__ ItemGeo item_geo(const FwdParams& p, const VarlenTabs& vt, int64_t idx) {
   ItemGeo t;
-  const QItem it = q_item(p.g, BI, idx);
-  t.stream = it.stream;
-  t.head = it.head;
-  t.kvh = it.head / (p.g.Hq / p.g.Hkv);
-  t.r0 = it.qtile * BI;
-  const int64_t r1 = imin64(t.r0 + BI, p.g.L);
-  t.q = qtile_ranges(p.g, t.stream, t.r0, r1, BN);
+  Geom g = p.g;
+  int64_t qtile;
+  t.off = 0;
+  if (VL) {  // packed batch: the item and its sequence from the tables
+    const int4 e = vt.q_items[idx];
+    t.stream = e.y & 1;
+    t.head = e.y >> 1;
+    qtile = e.z;
+    t.off = vt.seq_off[e.x];
+    g = seq_geom(p.g, vt.seq_off[e.x + 1] - t.off);
+  } else {
+    const QItem it = q_item(p.g, BI, idx);
+    t.stream = it.stream;
+    t.head = it.head;
+    qtile = it.qtile;
+  }
+  t.L = g.L;
+  t.kvh = t.head / (p.g.Hq / p.g.Hkv);
+  t.r0 = qtile * BI;
+  const int64_t r1 = imin64(t.r0 + BI, g.L);
+  t.q = qtile_ranges(g, t.stream, t.r0, r1, BN);
   t.nc = (int)(t.q.c1 - t.q.c0);
   t.n = t.nc + (int)(t.q.n1 - t.q.n0);
   t.rot = sweep_rotation(idx, t.nc);
   return t;
+}
+
+// The geometry the item's rows are masked with (its sequence's, in a batch).
+template <bool VL>
+__device__ __forceinline__ Geom item_mask_geom(const FwdParams& p, const ItemGeo& t) {
+  return VL ? seq_geom(p.g, t.L) : p.g;
 }
 
 // First key of step j: the clean tiles from c0 + rot round to c0 + rot - 1,
@@ -152,12 +176,12 @@ __device__ __forceinline__ uint64_t exp_store64(const uint32_t (&a)[32], const u
   return f2_add(r, exp_store32(b, sl2x2, nm2, taddr + 16));
 }
 
-template <int HD>
+template <int HD, bool VL>
 __global__ void __launch_bounds__(kThreads, 1)
     bdlm_fwd_tc_kernel(const __grid_constant__ CUtensorMap tQc, const __grid_constant__ CUtensorMap tQn,
                        const __grid_constant__ CUtensorMap tKc, const __grid_constant__ CUtensorMap tKn,
                        const __grid_constant__ CUtensorMap tVc, const __grid_constant__ CUtensorMap tVn,
-                       const FwdParams p) {
+                       const FwdParams p, const VarlenTabs vt) {
   using LY = Layout<HD>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -209,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t rnd = 0; ok; ++rnd) {
         const int64_t idx = sched_item(p.g, rnd, cta, grid);
         if (idx >= n_items) break;
-        const ItemGeo g = item_geo(p, idx);
+        const ItemGeo g = item_geo<VL>(p, vt, idx);
         if (g.n == 0) continue;
         if (itn > 0 && !mbar_wait(BAR(B_QE), (itn - 1) & 1, wd, 1)) { ok = false; break; }
         mbar_arrive_expect_tx(BAR(B_QF), 2 * LY::kTile);
@@ -218,12 +242,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t)
 #pragma unroll
           for (int pn = 0; pn < HD / 64; ++pn)
-            tma_load_3d(sQ + t * LY::kTile + pn * kPanel, mq, BAR(B_QF), pn * 64, g.head, (int)(g.r0 + t * BM));
+            tma_load_3d(sQ + t * LY::kTile + pn * kPanel, mq, BAR(B_QF), pn * 64, g.head,
+                        (int)(g.off + g.r0 + t * BM));
         ++itn;
         for (int j = 0; j < g.n; ++j, ++kc) {
           const int st = kc & 1;
           const bool cs = j < g.nc;
-          const int key0 = (int)tile_key0(g, j);
+          const int key0 = (int)(g.off + tile_key0(g, j));  // packed-tensor row
           if (kc >= 2 && !mbar_wait(BAR(B_KE + st), ((kc >> 1) - 1) & 1, wd, 2)) { ok = false; break; }
           mbar_arrive_expect_tx(BAR(B_KF + st), LY::kTile);
 #pragma unroll
@@ -266,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t rnd = 0; ok; ++rnd) {
         const int64_t idx = sched_item(p.g, rnd, cta, grid);
         if (idx >= n_items) break;
-        const ItemGeo g = item_geo(p, idx);
+        const ItemGeo g = item_geo<VL>(p, vt, idx);
         if (g.n == 0) continue;
         if (!mbar_wait(BAR(B_QF), itn & 1, wd, 4)) { ok = false; break; }
         if (!mbar_wait(BAR(B_KF + (kc & 1)), (kc >> 1) & 1, wd, 5)) { ok = false; break; }
@@ -319,12 +344,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t rnd = 0; ok; ++rnd) {
       const int64_t idx = sched_item(p.g, rnd, cta, grid);
       if (idx >= n_items) break;
-      const ItemGeo g = item_geo(p, idx);
-      const int64_t r = g.r0 + t * BM + row;
-      const bool valid = r < p.g.L;
-      float* lse_out = (g.stream ? p.LSEn : p.LSEc) + (int64_t)g.head * p.g.L;
+      const ItemGeo g = item_geo<VL>(p, vt, idx);
+      // (one sequence: its length and offset come from the parameters, so
+      // that they occupy no registers across the loop)
+      const int64_t seqL = VL ? g.L : p.g.L, seq0 = VL ? g.off : 0;
+      const int64_t r = g.r0 + t * BM + row;  // row within the item's sequence
+      const bool valid = r < seqL;
+      float* lse_out = (g.stream ? p.LSEn : p.LSEc) + (int64_t)g.head * p.g.L + seq0;
       void* obase = g.stream ? p.On : p.Oc;
-      const int64_t oofs = (r * p.g.Hq + g.head) * HD;
+      const int64_t oofs = ((seq0 + r) * p.g.Hq + g.head) * HD;
       if (g.n == 0) {
         if (valid) {
           if (p.o_f32) {
@@ -345,15 +373,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // this row's visible key intervals
       int lo_c, hi_c, lo_n, hi_n;
       {
-        const int64_t rr = valid ? r : p.g.L - 1;
+        const int64_t rr = valid ? r : seqL - 1;
+        const Geom gm = item_mask_geom<VL>(p, g);
         int64_t a0, a1, b0, b1;
-        clean_interval(p.g, g.stream, rr, a0, a1);
-        noisy_interval(p.g, g.stream, rr, b0, b1);
+        clean_interval(gm, g.stream, rr, a0, a1);
+        noisy_interval(gm, g.stream, rr, b0, b1);
         lo_c = (int)a0; hi_c = (int)a1; lo_n = (int)b0; hi_n = (int)b1;
       }
       const int nc = g.nc, n = g.n, c0 = (int)g.q.c0, n0 = (int)g.q.n0, rot = g.rot;
-      const int call_lo = (int)g.q.c_all_lo, call_hi = (int)imin64(g.q.c_all_hi, p.g.L);
-      const int nall_lo = (int)g.q.n_all_lo, nall_hi = (int)imin64(g.q.n_all_hi, p.g.L);
+      const int call_lo = (int)g.q.c_all_lo, call_hi = (int)imin64(g.q.c_all_hi, seqL);
+      const int nall_lo = (int)g.q.n_all_lo, nall_hi = (int)imin64(g.q.n_all_hi, seqL);
       const float sl2 = p.scale_log2;
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j, ++sc) {
@@ -418,12 +447,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       ok = mbar_wait(BAR(B_OD + t), itn & 1, wd, 13);
-      const ItemGeo ge = item_geo(p, idx);
+      const ItemGeo ge = item_geo<VL>(p, vt, idx);
+      const int64_t seqL_e = VL ? ge.L : p.g.L, seq0_e = VL ? ge.off : 0;
       const int64_t re = ge.r0 + t * BM + row;
-      const bool ve = re < p.g.L;
-      float* lse_e = (ge.stream ? p.LSEn : p.LSEc) + (int64_t)ge.head * p.g.L;
+      const bool ve = re < seqL_e;
+      float* lse_e = (ge.stream ? p.LSEn : p.LSEc) + (int64_t)ge.head * p.g.L + seq0_e;
       void* obase_e = ge.stream ? p.On : p.Oc;
-      const int64_t oofs_e = (re * p.g.Hq + ge.head) * HD;
+      const int64_t oofs_e = ((seq0_e + re) * p.g.Hq + ge.head) * HD;
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -476,24 +506,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, int d, int num_sms, cudaStream_t stream,
-                       int* launches) {
+template <int HD, bool VL>
+cudaError_t launch_fwd_t(const FwdMaps& maps, const FwdParams& p, const VarlenTabs& vt, int grid,
+                         cudaStream_t stream) {
+  auto k = bdlm_fwd_tc_kernel<HD, VL>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<HD>::kAlloc);
+  if (e != cudaSuccess) return e;
+  k<<<grid, kThreads, Layout<HD>::kAlloc, stream>>>(maps.Qc, maps.Qn, maps.Kc, maps.Kn, maps.Vc, maps.Vn, p, vt);
+  return cudaSuccess;
+}
+
+cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, const VarlenTabs* vt, int d, int num_sms,
+                       cudaStream_t stream, int* launches) {
   const int64_t grid64 = p.n_items < num_sms ? p.n_items : num_sms;
   const int grid = (int)(grid64 > 0 ? grid64 : 1);
-  cudaError_t e;
-  if (d == 128) {
-    e = cudaFuncSetAttribute(bdlm_fwd_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Layout<128>::kAlloc);
-    if (e != cudaSuccess) return e;
-    bdlm_fwd_tc_kernel<128><<<grid, kThreads, Layout<128>::kAlloc, stream>>>(maps.Qc, maps.Qn, maps.Kc, maps.Kn,
-                                                                          maps.Vc, maps.Vn, p);
-  } else {
-    e = cudaFuncSetAttribute(bdlm_fwd_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Layout<64>::kAlloc);
-    if (e != cudaSuccess) return e;
-    bdlm_fwd_tc_kernel<64><<<grid, kThreads, Layout<64>::kAlloc, stream>>>(maps.Qc, maps.Qn, maps.Kc, maps.Kn,
-                                                                        maps.Vc, maps.Vn, p);
-  }
+  const VarlenTabs none{nullptr, nullptr, nullptr, 0, 0};
+  const VarlenTabs& t = vt ? *vt : none;
+  cudaError_t e = d == 128 ? (vt ? launch_fwd_t<128, true>(maps, p, t, grid, stream)
+                                 : launch_fwd_t<128, false>(maps, p, t, grid, stream))
+                           : (vt ? launch_fwd_t<64, true>(maps, p, t, grid, stream)
+                                 : launch_fwd_t<64, false>(maps, p, t, grid, stream));
+  if (e != cudaSuccess) return e;
   if (launches) ++*launches;
   return cudaGetLastError();
 }

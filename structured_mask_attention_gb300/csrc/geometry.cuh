@@ -188,6 +188,17 @@ BDLM_HD int sweep_rotation(int64_t idx, int nc) {
 // (host simulation of the snake assignment: 32 % spread at L = 16k).
 constexpr int64_t kBlockedMinTiles = 6 * kRoundItems;
 
+// The geometry of one sequence of a packed batch: rows [off, off + L) of the
+// packed tensors, all of its clean keys, its own corrupted block included.
+BDLM_HD Geom seq_geom(const Geom& all, int64_t L) {
+  Geom g = all;
+  g.L = L;
+  g.kv_begin = 0;
+  g.kv_end = L;
+  g.include_local = 1;
+  return g;
+}
+
 // Persistent-grid assignment: CTA `cta` of `grid` takes, in round r, the item
 // r*grid + cta on even rounds and r*grid + (grid-1-cta) on odd rounds.  Over
 // a longest-first list this boustrophedon order evens the CTAs' totals.

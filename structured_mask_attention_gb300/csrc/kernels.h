@@ -24,6 +24,21 @@ struct FwdParams {
   uint64_t limit_ns;
 };
 
+// Work-item tables of a packed variable-length batch, passed to the batch
+// instantiations of the kernels as a separate argument (so the one-sequence
+// kernels keep their parameter block, and their register allocation, as is).
+// Query items {sequence, stream + 2 * head, query tile, cost}, key items
+// {sequence, key stream + 2 * KV head, key tile, cost}, both in launch order,
+// and the n_seqs + 1 row offsets of the sequences.  With a batch, g.L in the
+// parameters is the total row count (the LSE / D row stride) and each item's
+// own geometry comes from its sequence.
+struct VarlenTabs {
+  const int4* q_items;
+  const int4* kv_items;
+  const int64_t* seq_off;
+  int64_t n_q, n_kv;
+};
+
 struct FwdMaps {
   CUtensorMap Qc, Qn, Kc, Kn, Vc, Vn;
 };
@@ -34,8 +49,9 @@ constexpr int kFwdTileQ = 128;
 constexpr int kFwdItemRows = 256;
 constexpr int kFwdTileK = 128;
 
-cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, int d, int num_sms, cudaStream_t stream,
-                       int* launches);
+// vt: null for one sequence.
+cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, const VarlenTabs* vt, int d, int num_sms,
+                       cudaStream_t stream, int* launches);
 
 // ------------------------------------------------------------- backward
 struct BwdParams {
@@ -56,10 +72,10 @@ constexpr int kBwdTile = 128;
 struct BwdMaps {
   CUtensorMap Qc, Qn, dOc, dOn, Kc, Kn, Vc, Vn;
 };
-cudaError_t launch_bwd_dq_tc(const BwdMaps& m, const BwdParams& p, int num_sms, uint32_t* status,
-                             uint64_t limit_ns, cudaStream_t stream, int* launches);
-cudaError_t launch_bwd_dkv_tc(const BwdMaps& m, const BwdParams& p, int num_sms, uint32_t* status,
-                              uint64_t limit_ns, cudaStream_t stream, int* launches);
+cudaError_t launch_bwd_dq_tc(const BwdMaps& m, const BwdParams& p, const VarlenTabs* vt, int num_sms,
+                             uint32_t* status, uint64_t limit_ns, cudaStream_t stream, int* launches);
+cudaError_t launch_bwd_dkv_tc(const BwdMaps& m, const BwdParams& p, const VarlenTabs* vt, int num_sms,
+                              uint32_t* status, uint64_t limit_ns, cudaStream_t stream, int* launches);
 
 // ------------------------------------------------------------- small kernels
 constexpr int kMaxParts = 32;

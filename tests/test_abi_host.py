@@ -169,3 +169,25 @@ def test_naive_schedule_lists_items_in_natural_order(lib, monkeypatch):
     keys = [(t, h, s) for (s, h, t, *_rest) in items]
     assert keys == sorted(keys)
     assert [it[2] for it in lpt][0] == max(it[2] for it in lpt)
+
+
+def test_varlen_workspace_and_validation_on_host(lib):
+    """Packed-batch sizing and argument checks need no GPU: bad offsets give a
+    zero workspace size; the entry points reject them before any launch."""
+    ws_f = m.bdlm_workspace_size_varlen(m.OP_FWD, (256, 512, 128), 4, 2, 128)
+    ws_b = m.bdlm_workspace_size_varlen(m.OP_BWD, (256, 512, 128), 4, 2, 128)
+    assert ws_f > 256 and ws_b > ws_f
+    # the backward holds D of both streams: 2 * Hq * T fp32
+    assert ws_b - ws_f >= 2 * 4 * 896 * 4
+    assert m.bdlm_workspace_size_varlen(m.OP_FWD, (256, 0), 4, 2, 128) == 0       # empty sequence
+    assert m.bdlm_workspace_size_varlen(m.OP_FWD_SHARD, (256,), 4, 2, 128) == 0   # no packed shard op
+    assert m.bdlm_workspace_size_varlen(m.OP_FWD, (256,), 4, 3, 128) == 0         # Hq % Hkv
+    lib_ = m.load_library()
+    import ctypes
+    off = (ctypes.c_int64 * 3)(0, 256, 448)
+    st = lib_.bdlm_attn_fwd_varlen(*([None] * 6), ctypes.cast(off, ctypes.c_void_p), 2, 128, 4, 2, 128, 0.1,
+                                   None, None, 0, None, None, None, 0, None)
+    assert st == 2  # 192-row sequence is not a multiple of B = 128 (checked before the pointers)
+    st = lib_.bdlm_attn_fwd_varlen(*([None] * 6), ctypes.cast(off, ctypes.c_void_p), 2, 64, 4, 2, 128, 0.1,
+                                   None, None, 0, None, None, None, 0, None)
+    assert st == 1  # null pointers
