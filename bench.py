@@ -419,8 +419,9 @@ def run_sweep(args):
     def emit(d):
         print(json.dumps(d), flush=True)
 
+    want = set(args.sweep_parts.split(","))
     # ---- configs: forward and backward separately
-    for name in ("gqa-8k", "gqa-32k", "long-128k"):
+    for name in (("gqa-8k", "gqa-32k", "long-128k") if "config" in want else ()):
         w = WORKLOADS[name]
         L, B, Hq, Hkv, d = w["L"], w["B"], w["Hq"], w["Hkv"], w["d"]
         X = make_torch(L, Hq, Hkv, d, seed=0, device=dev)
@@ -455,7 +456,7 @@ def run_sweep(args):
     w = WORKLOADS["sharded-256k"]
     L, Hq, Hkv, d, P = w["L"], w["Hq"], w["Hkv"], w["d"], w["P"]
     sc = 1.0 / math.sqrt(d)
-    for B in SHARDED_BLOCK_SIZES:
+    for B in (SHARDED_BLOCK_SIZES if "sharded" in want else ()):
         X = make_torch(L, Hq, Hkv, d, seed=B, device=dev)
         ins = [X[k] for k in names]
         step = L // P
@@ -511,6 +512,63 @@ def run_sweep(args):
         del X, ins, fu, gu, parts, mo, ml, Dc, Dn, dQc, dQn, dKc, dVc, dKn, dVn
         torch.cuda.empty_cache()
 
+    # ---- packed batches: one packed call vs one call per sequence
+    from structured_mask_attention_gb300.inputs import workload_lengths
+    for name in (("packed-128k", "batch-64x2k") if "packed" in want else ()):
+        w = WORKLOADS[name]
+        T, B, Hq, Hkv, d = w["T"], w["B"], w["Hq"], w["Hkv"], w["d"]
+        lens = workload_lengths(name)
+        offs = [0]
+        for n_ in lens:
+            offs.append(offs[-1] + n_)
+        X = make_torch(T, Hq, Hkv, d, seed=0, device=dev)
+        ins = [X[k] for k in names]
+        sc = 1.0 / math.sqrt(d)
+        wf = torch.empty(m.bdlm_workspace_size_varlen(m.OP_FWD, lens, Hq, Hkv, d), dtype=torch.uint8, device=dev)
+        wb = torch.empty(m.bdlm_workspace_size_varlen(m.OP_BWD, lens, Hq, Hkv, d), dtype=torch.uint8, device=dev)
+        f = m.bdlm_attn_fwd_varlen(*ins, lens, B, sc, workspace=wf)
+        g = m.bdlm_attn_bwd_varlen(*ins, f[0], f[1], X["dOc"], X["dOn"], f[2], f[3], lens, B, sc, workspace=wb)
+        pf = timed(lambda: m.bdlm_attn_fwd_varlen(*ins, lens, B, sc, out=f, workspace=wf))
+        pb = timed(lambda: m.bdlm_attn_bwd_varlen(*ins, f[0], f[1], X["dOc"], X["dOn"], f[2], f[3], lens, B, sc,
+                                                  out=g, workspace=wb))
+        # ablation: longest item first over the whole batch (host-built list)
+        os.environ["BDLM_VARLEN_ORDER"] = "lpt"
+        af = timed(lambda: m.bdlm_attn_fwd_varlen(*ins, lens, B, sc, out=f, workspace=wf))
+        ab = timed(lambda: m.bdlm_attn_bwd_varlen(*ins, f[0], f[1], X["dOc"], X["dOn"], f[2], f[3], lens, B, sc,
+                                                  out=g, workspace=wb))
+        os.environ.pop("BDLM_VARLEN_ORDER", None)
+        # the same sequences one call each (slices of the packed tensors)
+        sl = [(a, b_) for a, b_ in zip(offs[:-1], offs[1:])]
+        fo = [m.bdlm_attn_fwd(*[t[a:b_] for t in ins], B, sc) for (a, b_) in sl]
+        go = [m.bdlm_attn_bwd(*[t[a:b_] for t in ins], fo[i][0], fo[i][1], X["dOc"][a:b_], X["dOn"][a:b_],
+                              fo[i][2], fo[i][3], B, sc) for i, (a, b_) in enumerate(sl)]
+
+        def loop_fwd():
+            for i, (a, b_) in enumerate(sl):
+                m.bdlm_attn_fwd(*[t[a:b_] for t in ins], B, sc, out=fo[i])
+
+        def loop_bwd():
+            for i, (a, b_) in enumerate(sl):
+                m.bdlm_attn_bwd(*[t[a:b_] for t in ins], fo[i][0], fo[i][1], X["dOc"][a:b_], X["dOn"][a:b_],
+                                fo[i][2], fo[i][3], B, sc, out=go[i])
+
+        lf = timed(loop_fwd)
+        lb = timed(loop_bwd)
+        uf = sum(useful_flops(n_, B, Hq, d) for n_ in lens)
+        ptf = uf / ((pf + pb) * 1e-3) / 1e12
+        emit({"sweep": "packed", "workload": name, "T": T, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d,
+              "n_seqs": len(lens), "lens": lens,
+              "packed_fwd_ms": round(pf, 3), "packed_bwd_ms": round(pb, 3), "packed_step_ms": round(pf + pb, 3),
+              "lpt_order_step_ms": round(af + ab, 3),
+              "per_seq_fwd_ms": round(lf, 3), "per_seq_bwd_ms": round(lb, 3), "per_seq_step_ms": round(lf + lb, 3),
+              "packed_useful_tflops": round(ptf, 1),
+              "per_seq_useful_tflops": round(uf / ((lf + lb) * 1e-3) / 1e12, 1),
+              "packed_tokens_per_s": round(2 * T / ((pf + pb) * 1e-3), 1),
+              "pct_of_peak": round(100 * ptf / peak_tf, 2), "speedup": round((lf + lb) / (pf + pb), 3),
+              "peak": peak_src, "reps": reps})
+        del X, ins, f, g, fo, go, wf, wb
+        torch.cuda.empty_cache()
+
 
 # ------------------------------------------------------------------ reference arm
 def run_reference(args):
@@ -551,7 +609,10 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="measurement tables instead of the bench line: per-config fwd/bwd times, the "
                          "schedule ablation (BDLM_SCHED=naive vs longest first) and the sharded-256k "
-                         "block-size sweep with merge and preprocess bandwidth")
+                         "block-size sweep with merge and preprocess bandwidth, and packed batches "
+                         "(one packed call vs one call per sequence)")
+    ap.add_argument("--sweep-parts", default="config,sharded,packed",
+                    help="comma-separated parts of --sweep to run (config includes the schedule ablation)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -204,10 +204,14 @@ bdlm_status bdlm_attn_bwd_shard(const void* Qc, const void* Kc, const void* Vc,
  * ([Hq, T], natural log).  seq_offsets is a host array of n_seqs + 1 int64,
  * seq_offsets[0] = 0, every sequence length a positive multiple of B; a row
  * attends only within its own sequence, with the mask of the one-sequence
- * calls.  All sequences run in one launch per kernel: the work items of all
- * of them form one longest-first list (built on the host, copied into the
- * workspace, so the host array may be freed on return).  Same conventions,
- * dtypes and error behaviour as bdlm_attn_fwd / bdlm_attn_bwd.
+ * calls.  All sequences run in one launch per kernel over one work list:
+ * the sequences one after the other, longest first, each in its
+ * one-sequence order.  The offsets are copied into the workspace before the
+ * call returns (the host array may be freed then) and a small kernel expands
+ * them into the work list on the stream.  BDLM_VARLEN_ORDER=lpt instead
+ * orders all items longest first over the whole batch, built on the host (a
+ * scheduling ablation).  Same conventions, dtypes and error behaviour as
+ * bdlm_attn_fwd / bdlm_attn_bwd.
  *
  * bdlm_workspace_size_varlen: bytes of workspace for op BDLM_OP_FWD or
  * BDLM_OP_BWD (0 for another op or a bad shape). */

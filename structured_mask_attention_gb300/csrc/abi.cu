@@ -335,7 +335,7 @@ bdlm_status guarded(F&& f) {
 
 // ------------------------------------------------------------ packed batch
 // Sequence s owns rows [off[s], off[s+1]) of the packed tensors; the kernels
-// read their items from tables built here, longest first over all sequences.
+// read their items from tables in the workspace (see varlen_tables below).
 constexpr int64_t kMaxSeqs = 1 << 20;
 
 bdlm_status check_varlen(const int64_t* off, int n, int64_t B, int Hq, int Hkv, int d, int64_t* T) {
@@ -362,6 +362,16 @@ int64_t varlen_kv_count(const int64_t* off, int n, int Hkv, int tk) {
   int64_t c = 0;
   for (int s = 0; s < n; ++s) c += cdiv64(off[s + 1] - off[s], tk) * 2 * Hkv;
   return c;
+}
+
+// Order of a packed batch's items.  Default: one sequence after the other,
+// longest sequence first, each in its one-sequence order (the items running
+// together then read one sequence's keys), expanded on the device from a
+// per-sequence directory.  BDLM_VARLEN_ORDER=lpt (ablation): longest item
+// first over all sequences, tables built on the host.
+bool varlen_lpt_order() {
+  const char* s = std::getenv("BDLM_VARLEN_ORDER");
+  return s && std::strcmp(s, "lpt") == 0;
 }
 
 // {sequence, stream + 2 * head, query tile, visible key tiles}, longest first
@@ -403,17 +413,44 @@ std::vector<int4> varlen_kv_table(const Geom& all, const int64_t* off, int n, in
   return v;
 }
 
+// Directory of a packed batch, uploaded as one int64 array:
+//   [0, n]        sequence offsets (as given)
+//   [n+1, 2n+1]   first query item of each sequence in directory order (+ total)
+//   [2n+2, 3n+2]  first key item of each sequence in directory order (+ total)
+//   [3n+3, 4n+2]  sequence ids, longest first (ties: lower id first)
+std::vector<int64_t> varlen_directory(const Geom& all, const int64_t* off, int n, int tq, int tk) {
+  std::vector<int64_t> v((size_t)(4 * n + 3));
+  int64_t* o = v.data();
+  int64_t* qb = o + n + 1;
+  int64_t* kb = qb + n + 1;
+  int64_t* ord = kb + n + 1;
+  for (int s = 0; s <= n; ++s) o[s] = off[s];
+  std::vector<int> idx(n);
+  for (int s = 0; s < n; ++s) idx[s] = s;
+  std::stable_sort(idx.begin(), idx.end(),
+                   [off](int a, int b) { return off[a + 1] - off[a] > off[b + 1] - off[b]; });
+  qb[0] = kb[0] = 0;
+  for (int k = 0; k < n; ++k) {
+    const int s = idx[k];
+    const Geom g = seq_geom(all, off[s + 1] - off[s]);
+    ord[k] = s;
+    qb[k + 1] = qb[k] + q_items(g, tq);
+    kb[k + 1] = kb[k] + kv_items(g, tk);
+  }
+  return v;
+}
+
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Workspace of a packed-batch call: header, [D of both streams], offsets, item tables.
+// Workspace of a packed-batch call: header, [D of both streams], directory, item tables.
 struct VarlenLayout {
-  size_t d_bytes, off_at, q_at, kv_at, total;
+  size_t d_bytes, dir_at, q_at, kv_at, total;
 };
 VarlenLayout varlen_layout(int op, const int64_t* off, int n, int Hq, int Hkv, int64_t T) {
   VarlenLayout l;
   l.d_bytes = op == BDLM_OP_BWD ? round256(2 * (size_t)Hq * (size_t)T * sizeof(float)) : 0;
-  l.off_at = kWsHeader + l.d_bytes;
-  l.q_at = l.off_at + round256((size_t)(n + 1) * sizeof(int64_t));
+  l.dir_at = kWsHeader + l.d_bytes;
+  l.q_at = l.dir_at + round256((size_t)(4 * n + 3) * sizeof(int64_t));
   const int64_t nq = op == BDLM_OP_BWD ? varlen_q_count(off, n, Hq, kBwdTile) : varlen_q_count(off, n, Hq, kFwdItemRows);
   l.kv_at = l.q_at + round256((size_t)nq * sizeof(int4));
   const int64_t nkv = op == BDLM_OP_BWD ? varlen_kv_count(off, n, Hkv, kBwdTile) : 0;
@@ -426,6 +463,35 @@ bdlm_status upload(void* dst, const void* src, size_t bytes, cudaStream_t st) {
   // pageable source: the copy is staged before the call returns
   cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(work list)");
+  return BDLM_OK;
+}
+
+// Uploads the directory of a packed batch and fills its item tables (query
+// items with tiles of tq rows; key items too when with_kv), on the stream.
+bdlm_status varlen_tables(const Geom& all, const int64_t* off, int n, int tq, bool with_kv, const VarlenLayout& lay,
+                          char* w, cudaStream_t st, int* launches, VarlenTabs* vt) {
+  const int tk = kBwdTile;  // key tiles: 128 keys in every pass
+  const std::vector<int64_t> dir = varlen_directory(all, off, n, tq, tk);
+  BDLM_CHECK(upload(w + lay.dir_at, dir.data(), dir.size() * sizeof(int64_t), st));
+  const int64_t* d_dir = reinterpret_cast<const int64_t*>(w + lay.dir_at);
+  int4* q_tab = reinterpret_cast<int4*>(w + lay.q_at);
+  int4* kv_tab = reinterpret_cast<int4*>(w + lay.kv_at);
+  const int64_t nq = dir[2 * (size_t)n + 1], nkv = with_kv ? dir[3 * (size_t)n + 2] : 0;
+  if (varlen_lpt_order()) {
+    const std::vector<int4> qt = varlen_q_table(all, off, n, tq, tk);
+    BDLM_CHECK(upload(q_tab, qt.data(), qt.size() * sizeof(int4), st));
+    if (with_kv) {
+      const std::vector<int4> kvt = varlen_kv_table(all, off, n, tk);
+      BDLM_CHECK(upload(kv_tab, kvt.data(), kvt.size() * sizeof(int4), st));
+    }
+  } else {
+    const int64_t* ord = d_dir + 3 * (size_t)n + 3;
+    cudaError_t e = launch_varlen_items(all, d_dir, ord, d_dir + n + 1, n, nq, 0, tq, tk, q_tab, st, launches);
+    if (e == cudaSuccess && with_kv)
+      e = launch_varlen_items(all, d_dir, ord, d_dir + 2 * (size_t)n + 2, n, nkv, 1, tq, tk, kv_tab, st, launches);
+    if (e != cudaSuccess) return cuda_fail(e, "packed-batch item tables");
+  }
+  *vt = VarlenTabs{q_tab, with_kv ? kv_tab : nullptr, d_dir, nq, nkv};
   return BDLM_OK;
 }
 
@@ -742,13 +808,13 @@ bdlm_status bdlm_attn_fwd_varlen(const void* Qc, const void* Kc, const void* Vc,
     const VarlenLayout lay = varlen_layout(BDLM_OP_FWD, seq_offsets, n_seqs, Hq, Hkv, T);
     BDLM_CHECK(check_ws(workspace, ws_bytes, lay.total));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    char* w = static_cast<char*>(workspace);
-    const Geom all{T, B, Hq, Hkv, 0, T, 1};
-    const std::vector<int4> tab = varlen_q_table(all, seq_offsets, n_seqs, kFwdItemRows, kFwdTileK);
-    BDLM_CHECK(upload(w + lay.off_at, seq_offsets, (size_t)(n_seqs + 1) * sizeof(int64_t), st));
-    BDLM_CHECK(upload(w + lay.q_at, tab.data(), tab.size() * sizeof(int4), st));
-    const VarlenTabs vt{reinterpret_cast<const int4*>(w + lay.q_at), nullptr,
-                        reinterpret_cast<const int64_t*>(w + lay.off_at), (int64_t)tab.size(), 0};
+    Geom all{T, B, Hq, Hkv, 0, T, 1};
+    all.naive_order = naive_schedule();
+    VarlenTabs vt;
+    int launches = 0;
+    BDLM_CHECK(varlen_tables(all, seq_offsets, n_seqs, kFwdItemRows, false, lay, static_cast<char*>(workspace), st,
+                             &launches, &vt));
+    g_launches.fetch_add((uint64_t)launches);
     return fwd_common(Qc, Kc, Vc, Qn, Kn, Vn, T, B, Hq, Hkv, d, scale, 0, T, 1, Oc, On, o_dtype == BDLM_F32, LSEc,
                       LSEn, workspace, ws_bytes, st, &vt);
   });
@@ -776,13 +842,13 @@ bdlm_status bdlm_attn_bwd_varlen(const void* Qc, const void* Kc, const void* Vc,
     char* w = static_cast<char*>(workspace);
     float* Dc = reinterpret_cast<float*>(w + kWsHeader);
     float* Dn = Dc + (size_t)Hq * T;
-    const Geom all{T, B, Hq, Hkv, 0, T, 1};
-    const std::vector<int4> qt = varlen_q_table(all, seq_offsets, n_seqs, kBwdTile, kBwdTile);
-    const std::vector<int4> kvt = varlen_kv_table(all, seq_offsets, n_seqs, kBwdTile);
+    Geom all{T, B, Hq, Hkv, 0, T, 1};
+    all.naive_order = naive_schedule();
     BDLM_CHECK(clear_status(workspace, st));
-    BDLM_CHECK(upload(w + lay.off_at, seq_offsets, (size_t)(n_seqs + 1) * sizeof(int64_t), st));
-    BDLM_CHECK(upload(w + lay.q_at, qt.data(), qt.size() * sizeof(int4), st));
-    BDLM_CHECK(upload(w + lay.kv_at, kvt.data(), kvt.size() * sizeof(int4), st));
+    VarlenTabs vt;
+    int tab_launches = 0;
+    BDLM_CHECK(varlen_tables(all, seq_offsets, n_seqs, kBwdTile, true, lay, w, st, &tab_launches, &vt));
+    g_launches.fetch_add((uint64_t)tab_launches);
     int launches = 0;
     cudaError_t e;
     {
@@ -796,8 +862,6 @@ bdlm_status bdlm_attn_bwd_varlen(const void* Qc, const void* Kc, const void* Vc,
     BwdParams p = bwd_params(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn, T, B, Hq, Hkv, d, scale, 0, T, 1);
     p.dQc = dQc; p.dQn = dQn; p.dKc = dKc; p.dVc = dVc; p.dKn = dKn; p.dVn = dVn;
     p.g_f32 = g_dtype == BDLM_F32;
-    const VarlenTabs vt{reinterpret_cast<const int4*>(w + lay.q_at), reinterpret_cast<const int4*>(w + lay.kv_at),
-                        reinterpret_cast<const int64_t*>(w + lay.off_at), (int64_t)qt.size(), (int64_t)kvt.size()};
     bdlm_status vs = BDLM_OK;
     if (e == cudaSuccess) e = launch_backward_passes(p, info, workspace, st, &launches, &vs, &vt);
     if (vs != BDLM_OK) return vs;

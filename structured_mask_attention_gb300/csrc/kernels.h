@@ -94,6 +94,10 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, int* launche
 cudaError_t launch_preprocess(const void* O, int o_f32, const void* dO, int64_t rows, int H, int d, float* D,
                               cudaStream_t stream, int* launches);
 cudaError_t launch_watchdog(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
+// Packed-batch item table, sequence-major (kind 0: query items, 1: key items).
+cudaError_t launch_varlen_items(const Geom& all, const int64_t* off, const int64_t* order, const int64_t* beg, int n,
+                                int64_t total, int kind, int tq, int tk, int4* out, cudaStream_t stream,
+                                int* launches);
 
 // Records the message bdlm_last_error() returns on this thread.
 void set_last_error(const std::string& msg);

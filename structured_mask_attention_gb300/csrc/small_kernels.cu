@@ -1,6 +1,6 @@
 // small_kernels.cu -- HBM-bound kernels: the exact LSE merge of partial
-// attention results, the backward row statistic D, and the watchdog
-// self-test.
+// attention results, the backward row statistic D; the work-list expansion
+// of a packed batch; the watchdog self-test.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -112,6 +112,41 @@ __global__ void bdlm_watchdog_kernel(uint32_t* status, uint64_t limit_ns) {
   (void)mbar_wait(smem_u32(&bar), 0, wd, 0x7f);
 }
 
+// Item table of a packed batch in sequence-major order: the sequences in the
+// order given by `order`, each sequence's items in its one-sequence order.
+// beg[k] is the first item of the k-th sequence of that order (beg[n] = total).
+// kind 0: query items {sequence, stream + 2 * head, query tile, visible key
+// tiles} with tiles of tq rows and tk keys; kind 1: key items {sequence, key
+// stream + 2 * KV head, key tile, query rows that see it}, tiles of tk keys.
+__global__ void __launch_bounds__(256) bdlm_varlen_items_kernel(const Geom all, const int64_t* off,
+                                                                 const int64_t* order, const int64_t* beg, int n,
+                                                                 int kind, int tq, int tk, int4* out) {
+  const int64_t total = beg[n];
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    int lo = 0, hi = n - 1;  // last k with beg[k] <= idx
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (beg[mid] <= idx) lo = mid; else hi = mid - 1;
+    }
+    const int s = (int)order[lo];
+    const int64_t local = idx - beg[lo];
+    const Geom g = seq_geom(all, off[s + 1] - off[s]);
+    if (kind == 0) {
+      const QItem it = q_item(g, tq, local);
+      const int64_t r0 = it.qtile * tq, r1 = imin64(r0 + tq, g.L);
+      const QTileRanges q = qtile_ranges(g, it.stream, r0, r1, tk);
+      out[idx] = make_int4(s, it.stream + 2 * it.head, (int)it.qtile, (int)((q.c1 - q.c0) + (q.n1 - q.n0)));
+    } else {
+      const KVItem it = kv_item(g, tk, local);
+      int64_t cl, ch, nl, nh;
+      kv_tile_rows(g, it.key_stream, it.ktile * tk, imin64(it.ktile * tk + tk, g.L), cl, ch, nl, nh);
+      out[idx] = make_int4(s, it.key_stream + 2 * it.kv_head, (int)it.ktile,
+                           (int)(imax64(0, ch - cl) + imax64(0, nh - nl)));
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, int* launches) {
@@ -132,6 +167,17 @@ cudaError_t launch_preprocess(const void* O, int o_f32, const void* dO, int64_t 
   const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(dO);
   if (d == 128) bdlm_preprocess_kernel<128><<<blocks, 256, 0, stream>>>(O, o_f32, g, rows, H, D);
   else bdlm_preprocess_kernel<64><<<blocks, 256, 0, stream>>>(O, o_f32, g, rows, H, D);
+  if (launches) ++*launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_varlen_items(const Geom& all, const int64_t* off, const int64_t* order, const int64_t* beg, int n,
+                                int64_t total, int kind, int tq, int tk, int4* out, cudaStream_t stream,
+                                int* launches) {
+  if (total == 0) return cudaSuccess;
+  const int64_t blocks = (total + 255) / 256;
+  bdlm_varlen_items_kernel<<<(int)(blocks < 1024 ? blocks : 1024), 256, 0, stream>>>(all, off, order, beg, n, kind,
+                                                                                     tq, tk, out);
   if (launches) ++*launches;
   return cudaGetLastError();
 }

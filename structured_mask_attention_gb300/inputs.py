@@ -14,6 +14,11 @@ block size B, GQA with Hq query heads and Hkv key/value heads, head dim d):
 * ``long-128k``   L=131072, B=512, Hq=16, Hkv=8, d=128
 * ``sharded-256k`` L=262144, B in {128,256,512,1024}, Hq=8, Hkv=4, d=128, P=8
 * ``profile-16k`` L=16384, B=512, Hq=16, Hkv=8, d=128 (profiler captures)
+* ``packed-128k`` a packed batch of T=131072 tokens per stream, B=512, Hq=16,
+  Hkv=8, d=128, sequence lengths from ``packed_lengths`` (log-uniform between
+  2048 and 32768, multiples of B)
+* ``batch-64x2k`` a plain batch of 64 sequences of 2048 tokens, B=128, Hq=32,
+  Hkv=8, d=128
 
 Draw order: Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn (each N(0,1) in fp32), then, when
 requested, one LogNormal(0, sigma) factor per token for each of Qc, Kc, Qn, Kn,
@@ -33,10 +38,35 @@ WORKLOADS = {
     # same head layout and block size as long-128k at 1/8 of the length, for
     # profiler captures (inputs ~0.4 GB, still larger than L2)
     "profile-16k": dict(L=16384, B=512, Hq=16, Hkv=8, d=128),
+    # packed batches (per-sequence lengths; T = total tokens per stream)
+    "packed-128k": dict(T=131072, B=512, Hq=16, Hkv=8, d=128, lo=2048, hi=32768, seed=0),
+    "batch-64x2k": dict(T=131072, B=128, Hq=32, Hkv=8, d=128, lo=2048, hi=2048, seed=0),
 }
 SHARDED_BLOCK_SIZES = (128, 256, 512, 1024)
 
 NAMES = ("Qc", "Kc", "Vc", "Qn", "Kn", "Vn", "dOc", "dOn")
+
+
+def packed_lengths(T, B, lo, hi, seed=0):
+    """Sequence lengths of a packed batch of T tokens: drawn log-uniformly in
+    [lo, hi] from numpy's PCG64(seed), rounded down to multiples of B (at
+    least B), until the total would pass T; the last sequence takes the rest.
+    T, lo and hi are multiples of B."""
+    assert T % B == 0 and lo % B == 0 and hi % B == 0 and 0 < lo <= hi
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lens, left = [], T
+    while left > 0:
+        x = int(np.exp(rng.uniform(np.log(lo), np.log(hi))) // B * B) if hi > lo else lo
+        x = min(max(x, B), left)
+        lens.append(x)
+        left -= x
+    return lens
+
+
+def workload_lengths(name):
+    """Sequence lengths of a packed workload of ``WORKLOADS``."""
+    w = WORKLOADS[name]
+    return packed_lengths(w["T"], w["B"], w["lo"], w["hi"], w["seed"])
 
 
 def bf16_round(x: np.ndarray) -> np.ndarray:

@@ -191,3 +191,18 @@ def test_varlen_workspace_and_validation_on_host(lib):
     st = lib_.bdlm_attn_fwd_varlen(*([None] * 6), ctypes.cast(off, ctypes.c_void_p), 2, 64, 4, 2, 128, 0.1,
                                    None, None, 0, None, None, None, 0, None)
     assert st == 1  # null pointers
+
+
+def test_packed_lengths_mix():
+    """The packed workloads' length mix: sums to T, every length a positive
+    multiple of B within [B, hi], deterministic in the seed."""
+    from structured_mask_attention_gb300.inputs import WORKLOADS, packed_lengths, workload_lengths
+    for name in ("packed-128k", "batch-64x2k"):
+        w = WORKLOADS[name]
+        lens = workload_lengths(name)
+        assert sum(lens) == w["T"]
+        assert all(n % w["B"] == 0 and w["B"] <= n <= w["hi"] for n in lens)
+        assert all(n >= w["lo"] for n in lens[:-1])
+        assert lens == workload_lengths(name)
+    assert workload_lengths("batch-64x2k") == [2048] * 64
+    assert packed_lengths(4096, 128, 256, 1024, seed=1) != packed_lengths(4096, 128, 256, 1024, seed=2)

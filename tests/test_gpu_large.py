@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 import oracle.bdlm_oracle as orc
-from structured_mask_attention_gb300.inputs import SHARDED_BLOCK_SIZES, WORKLOADS, make_torch
+from structured_mask_attention_gb300.inputs import SHARDED_BLOCK_SIZES, WORKLOADS, make_torch, workload_lengths
 from tests.parity_util import check_lse, check_rel
 
 torch = pytest.importorskip("torch")
@@ -69,6 +69,60 @@ def _invariants(X, grads, G):
     bound = 2e-2 * math.sqrt(n) * rmsV + acc * l1V + 1e-6
     print(f"  sum dV: max |dev| / bound = {float(((sV - dO).abs() / bound).max()):.3f}")
     assert ((sV - dO).abs() <= bound).all()
+
+
+def _check_sequence(X, grads, outs, B, sc, G, kvh, rng, n_rows):
+    """Sampled oracle parity of one sequence (X, grads, outs: its slices)."""
+    Oc, On, LSEc, LSEn = outs
+    L = X["Qc"].shape[0]
+    N = L // B
+    H = _host_group(X, kvh, G)
+    hx = [H[k] for k in NAMES]
+    rows = _sample_rows(L, B, rng, n_rows)
+    for stream, O, LSE, dQ in (("c", Oc, LSEc, grads[0]), ("n", On, LSEn, grads[3])):
+        for hh in (0, G - 1):
+            h = kvh * G + hh
+            o, lse = orc.fwd_rows(*hx[:6], B, sc, stream, hh, rows)
+            check_rel(f"O{stream}[h={h}] rows", O[rows, h].float().cpu().numpy(), o)
+            check_lse(f"LSE{stream}[h={h}] rows", LSE[h, rows].cpu().numpy(), lse)
+            dq = orc.dq_rows(*hx, B, sc, stream, hh, rows)
+            check_rel(f"dQ{stream}[h={h}] rows", dQ[rows, h].float().cpu().numpy(), dq)
+    tail = sorted({N - 1, max(N - 2, 0)})
+    outc, outn = orc.dkv_tail_blocks(*hx, B, sc, 0, tail, sorted({N - 1, 0, N // 2}))
+    for (blocks, dK, dV, tag) in ((outc, grads[1], grads[2], "c"), (outn, grads[4], grads[5], "n")):
+        for j, (rk, rv) in blocks.items():
+            check_rel(f"dK{tag}[kvh={kvh}, block {j}]", dK[j * B:(j + 1) * B, kvh].float().cpu().numpy(), rk)
+            check_rel(f"dV{tag}[kvh={kvh}, block {j}]", dV[j * B:(j + 1) * B, kvh].float().cpu().numpy(), rv)
+
+
+@pytest.mark.parametrize("name", ["packed-128k", "batch-64x2k"])
+def test_packed_batch_workload(lib, name):
+    """Full-size packed batch through the packed calls: invariants over the
+    whole batch, and sampled oracle parity of the first, the longest and the
+    last sequence, each computed on that sequence alone."""
+    m = lib
+    w = WORKLOADS[name]
+    T, B, Hq, Hkv, d = w["T"], w["B"], w["Hq"], w["Hkv"], w["d"]
+    G = Hq // Hkv
+    lens = workload_lengths(name)
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(int)
+    X = make_torch(T, Hq, Hkv, d, seed=0, device="cuda")
+    ins = [X[k] for k in NAMES[:6]]
+    sc = 1.0 / math.sqrt(d)
+    outs = m.bdlm_attn_fwd_varlen(*ins, lens, B, sc)
+    grads = m.bdlm_attn_bwd_varlen(*ins, outs[0], outs[1], X["dOc"], X["dOn"], outs[2], outs[3], lens, B, sc,
+                                   g_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert all(torch.isfinite(t).all() for t in (*outs, *grads))
+    _invariants(X, grads, G)
+    rng = np.random.default_rng(T + len(lens))
+    for s in sorted({0, int(np.argmax(lens)), len(lens) - 1}):
+        a, b = int(off[s]), int(off[s + 1])
+        print(f"sequence {s}: rows [{a}, {b})")
+        Xs = {k: X[k][a:b] for k in NAMES}
+        os_ = (outs[0][a:b], outs[1][a:b], outs[2][:, a:b], outs[3][:, a:b])
+        gs = [g[a:b] for g in grads]
+        _check_sequence(Xs, gs, os_, B, sc, G, kvh=s % Hkv, rng=rng, n_rows=6)
 
 
 def _full_size_case(m, name, lognormal=0.0, groups=(0,), n_rows=12):

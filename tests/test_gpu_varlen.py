@@ -39,9 +39,14 @@ def _batch(lens, Hq, Hkv, d, seed):
     ((1024, 1024, 1024), 128, 2, 1, 128),     # equal lengths: a plain batch of 3
     ((320, 96, 640), 32, 3, 3, 64),           # ragged tails in every sequence, d = 64
     ((128,), 128, 2, 2, 128),                 # one sequence through the batch path
+    (tuple(64 * ((7 * i) % 5 + 1) for i in range(40)), 64, 2, 1, 64),  # 40 sequences, 64..320 rows
 ])
-def test_varlen_against_oracle_per_sequence(lib, lens, B, Hq, Hkv, d):
+@pytest.mark.parametrize("order", ["seq", "lpt"])
+def test_varlen_against_oracle_per_sequence(lib, lens, B, Hq, Hkv, d, order, monkeypatch):
+    """order: the default work list (sequence-major, expanded on the device)
+    and the longest-first ablation (built on the host)."""
     m = lib
+    monkeypatch.setenv("BDLM_VARLEN_ORDER", order)
     per, packed = _batch(lens, Hq, Hkv, d, seed=sum(lens) + B)
     dev = {k: to_dev(v, torch) for k, v in packed.items()}
     sc = 1.0 / math.sqrt(d)
