@@ -206,9 +206,11 @@ bdlm_status bdlm_attn_bwd_shard(const void* Qc, const void* Kc, const void* Vc,
  * attends only within its own sequence, with the mask of the one-sequence
  * calls.  All sequences run in one launch per kernel over one work list:
  * the sequences one after the other, longest first, each in its
- * one-sequence order.  The offsets are copied into the workspace before the
- * call returns (the host array may be freed then) and a small kernel expands
- * them into the work list on the stream.  BDLM_VARLEN_ORDER=lpt instead
+ * one-sequence order.  The offsets are read before the call returns (the
+ * host array may be freed then); the library's own copy reaches the
+ * workspace on the stream, and a small kernel expands it into the work list.
+ * These calls cannot be captured into a CUDA graph (BDLM_ERR_UNSUPPORTED):
+ * they copy host data that differs from call to call.  BDLM_VARLEN_ORDER=lpt instead
  * orders all items longest first over the whole batch, built on the host (a
  * scheduling ablation).  Same conventions, dtypes and error behaviour as
  * bdlm_attn_fwd / bdlm_attn_bwd.

@@ -458,9 +458,10 @@ VarlenLayout varlen_layout(int op, const int64_t* off, int n, int Hq, int Hkv, i
   return l;
 }
 
+// Host -> device copy on the stream; the caller keeps `src` alive until the
+// copy has run.
 bdlm_status upload(void* dst, const void* src, size_t bytes, cudaStream_t st) {
   if (!bytes) return BDLM_OK;
-  // pageable source: the copy is staged before the call returns
   cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(work list)");
   return BDLM_OK;
@@ -468,25 +469,50 @@ bdlm_status upload(void* dst, const void* src, size_t bytes, cudaStream_t st) {
 
 // Uploads the directory of a packed batch and fills its item tables (query
 // items with tiles of tq rows; key items too when with_kv), on the stream.
+// Host arrays of a packed-batch call, kept alive until their copies to the
+// device have run: a copy from pageable memory may still read its source
+// after cudaMemcpyAsync returns, so a host function enqueued behind the
+// copies frees them.
+struct VarlenHostArrays {
+  std::vector<int64_t> dir;
+  std::vector<int4> q, kv;
+};
+void CUDART_CB free_varlen_host_arrays(void* p) { delete static_cast<VarlenHostArrays*>(p); }
+
 bdlm_status varlen_tables(const Geom& all, const int64_t* off, int n, int tq, bool with_kv, const VarlenLayout& lay,
                           char* w, cudaStream_t st, int* launches, VarlenTabs* vt) {
   const int tk = kBwdTile;  // key tiles: 128 keys in every pass
-  const std::vector<int64_t> dir = varlen_directory(all, off, n, tq, tk);
-  BDLM_CHECK(upload(w + lay.dir_at, dir.data(), dir.size() * sizeof(int64_t), st));
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  if (cap != cudaStreamCaptureStatusNone)
+    return fail(BDLM_ERR_UNSUPPORTED, "packed-batch calls copy host arrays and cannot be captured into a graph");
+  VarlenHostArrays* h = new VarlenHostArrays;
+  h->dir = varlen_directory(all, off, n, tq, tk);
   const int64_t* d_dir = reinterpret_cast<const int64_t*>(w + lay.dir_at);
   int4* q_tab = reinterpret_cast<int4*>(w + lay.q_at);
   int4* kv_tab = reinterpret_cast<int4*>(w + lay.kv_at);
-  const int64_t nq = dir[2 * (size_t)n + 1], nkv = with_kv ? dir[3 * (size_t)n + 2] : 0;
-  if (varlen_lpt_order()) {
-    const std::vector<int4> qt = varlen_q_table(all, off, n, tq, tk);
-    BDLM_CHECK(upload(q_tab, qt.data(), qt.size() * sizeof(int4), st));
-    if (with_kv) {
-      const std::vector<int4> kvt = varlen_kv_table(all, off, n, tk);
-      BDLM_CHECK(upload(kv_tab, kvt.data(), kvt.size() * sizeof(int4), st));
+  const int64_t nq = h->dir[2 * (size_t)n + 1], nkv = with_kv ? h->dir[3 * (size_t)n + 2] : 0;
+  bdlm_status s = upload(w + lay.dir_at, h->dir.data(), h->dir.size() * sizeof(int64_t), st);
+  if (s == BDLM_OK && varlen_lpt_order()) {
+    h->q = varlen_q_table(all, off, n, tq, tk);
+    s = upload(q_tab, h->q.data(), h->q.size() * sizeof(int4), st);
+    if (s == BDLM_OK && with_kv) {
+      h->kv = varlen_kv_table(all, off, n, tk);
+      s = upload(kv_tab, h->kv.data(), h->kv.size() * sizeof(int4), st);
     }
-  } else {
+  }
+  // free the host arrays behind the copies (or at once if nothing is in flight)
+  e = cudaLaunchHostFunc(st, free_varlen_host_arrays, h);
+  if (e != cudaSuccess) {
+    cudaStreamSynchronize(st);
+    delete h;
+    return s != BDLM_OK ? s : cuda_fail(e, "cudaLaunchHostFunc");
+  }
+  if (s != BDLM_OK) return s;
+  if (!varlen_lpt_order()) {
     const int64_t* ord = d_dir + 3 * (size_t)n + 3;
-    cudaError_t e = launch_varlen_items(all, d_dir, ord, d_dir + n + 1, n, nq, 0, tq, tk, q_tab, st, launches);
+    e = launch_varlen_items(all, d_dir, ord, d_dir + n + 1, n, nq, 0, tq, tk, q_tab, st, launches);
     if (e == cudaSuccess && with_kv)
       e = launch_varlen_items(all, d_dir, ord, d_dir + 2 * (size_t)n + 2, n, nkv, 1, tq, tk, kv_tab, st, launches);
     if (e != cudaSuccess) return cuda_fail(e, "packed-batch item tables");
@@ -844,11 +870,11 @@ bdlm_status bdlm_attn_bwd_varlen(const void* Qc, const void* Kc, const void* Vc,
     float* Dn = Dc + (size_t)Hq * T;
     Geom all{T, B, Hq, Hkv, 0, T, 1};
     all.naive_order = naive_schedule();
-    BDLM_CHECK(clear_status(workspace, st));
     VarlenTabs vt;
     int tab_launches = 0;
     BDLM_CHECK(varlen_tables(all, seq_offsets, n_seqs, kBwdTile, true, lay, w, st, &tab_launches, &vt));
     g_launches.fetch_add((uint64_t)tab_launches);
+    BDLM_CHECK(clear_status(workspace, st));
     int launches = 0;
     cudaError_t e;
     {

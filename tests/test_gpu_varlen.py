@@ -77,3 +77,36 @@ def test_varlen_rejects_bad_offsets(lib):
     with pytest.raises(m.BdlmError) as e:
         m.bdlm_attn_fwd_varlen(*ins, (256, 192), 128)   # 192 is not a multiple of B = 128
     assert e.value.status == 2
+
+
+def test_varlen_refuses_graph_capture(lib):
+    """The packed calls copy host data and return BDLM_ERR_UNSUPPORTED (6)
+    inside a stream capture, before enqueuing anything."""
+    m = lib
+    lens = (256, 128)
+    per, packed = _batch(lens, 2, 1, 64, seed=5)
+    dev = {k: to_dev(v, torch) for k, v in packed.items()}
+    ins = [dev[k] for k in NAMES[:6]]
+    T = sum(lens)
+    out = (torch.empty((T, 2, 64), dtype=torch.bfloat16, device="cuda"),
+           torch.empty((T, 2, 64), dtype=torch.bfloat16, device="cuda"),
+           torch.empty((2, T), dtype=torch.float32, device="cuda"),
+           torch.empty((2, T), dtype=torch.float32, device="cuda"))
+    ws = torch.empty(m.bdlm_workspace_size_varlen(m.OP_FWD, lens, 2, 1, 64), dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    status = None
+    with torch.cuda.stream(side):
+        graph.capture_begin()
+        try:
+            m.bdlm_attn_fwd_varlen(*ins, lens, 64, out=out, workspace=ws)
+        except m.BdlmError as e:
+            status = e.status
+        finally:
+            graph.capture_end()
+    assert status == 6
+    # the library still works on the same buffers afterwards
+    m.bdlm_attn_fwd_varlen(*ins, lens, 64, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out[0].float()).all()
