@@ -112,14 +112,35 @@ def _group(Hq, Hkv):
     return Hq // Hkv
 
 
-def fwd_brute(Qc, Kc, Vc, Qn, Kn, Vn, B, scale):
+def mask_packed(seq_lens, B: int) -> np.ndarray:
+    """Explicit 2T x 2T visibility matrix of a packed batch: sequences of the
+    given lengths stored back to back (T = sum of the lengths), clean rows/keys
+    of all sequences first.  A row sees a key only inside its own sequence,
+    and there the two-stream mask of ``mask_2L`` holds with block indices
+    counted from the sequence's first token.  (Reading: the pages fix no batch
+    layout; sequences of a batch are independent problems.)"""
+    lens = [int(n) for n in seq_lens]
+    if any(n <= 0 or n % B for n in lens):
+        raise ValueError("every sequence length must be a positive multiple of B")
+    seq = np.concatenate([np.full(n, s) for s, n in enumerate(lens)])
+    pos = np.concatenate([np.arange(n) for n in lens])
+    bi = block_index(pos, B)
+    same = seq[:, None] == seq[None, :]
+    row, col = bi[:, None], bi[None, :]
+    T = len(pos)
+    return np.block([[same & (col <= row), np.zeros((T, T), dtype=bool)],
+                     [same & (col < row), same & (col == row)]])
+
+
+def fwd_brute(Qc, Kc, Vc, Qn, Kn, Vn, B, scale, mask=None):
     """Dense masked softmax attention over the combined 2L sequence with the
     explicit mask of ``mask_2L`` (abstract page: the model attends over the
-    combined clean-plus-corrupted sequence).  Tiny shapes only."""
+    combined clean-plus-corrupted sequence), or with ``mask`` when given (a
+    packed batch: ``mask_packed``).  Tiny shapes only."""
     L, Hq, d = Qc.shape
     Hkv = Kc.shape[1]
     g = _group(Hq, Hkv)
-    M = mask_2L(L, B)
+    M = mask_2L(L, B) if mask is None else mask
     O = np.zeros((2 * L, Hq, Vc.shape[2]))
     LSE = np.zeros((Hq, 2 * L))
     for h in range(Hq):
@@ -137,14 +158,14 @@ def fwd_brute(Qc, Kc, Vc, Qn, Kn, Vn, B, scale):
     return O[:L], O[L:], LSE[:, :L], LSE[:, L:]
 
 
-def bwd_brute(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, B, scale):
-    """Backward of ``fwd_brute`` with the explicit mask: the softmax-attention
-    gradient formulas of the module docstring, dense.  Returns
-    (dQc, dKc, dVc, dQn, dKn, dVn)."""
+def bwd_brute(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, B, scale, mask=None):
+    """Backward of ``fwd_brute`` with the explicit mask (``mask`` when given):
+    the softmax-attention gradient formulas of the module docstring, dense.
+    Returns (dQc, dKc, dVc, dQn, dKn, dVn)."""
     L, Hq, d = Qc.shape
     Hkv = Kc.shape[1]
     g = _group(Hq, Hkv)
-    M = mask_2L(L, B)
+    M = mask_2L(L, B) if mask is None else mask
     dQ = np.zeros((2 * L, Hq, d))
     dK = np.zeros((2 * L, Hkv, d))
     dV = np.zeros((2 * L, Hkv, Vc.shape[2]))

@@ -77,6 +77,41 @@ def test_blockwise_equals_brute(L, B, Hq, Hkv):
         np.testing.assert_allclose(x, y, rtol=0, atol=1e-12)
 
 
+# ------------------------------------------------------------------ packed batches
+def test_packed_mask_matches_hand_typed_fixture():
+    assert (orc.mask_packed((4, 2), 2) == _load_mask("mask_packed_4_2_B2.txt")).all()
+
+
+@pytest.mark.parametrize("lens,B", [((8,), 2), ((16, 8, 24), 4), ((6, 6, 6), 3), ((32, 4), 4)])
+def test_packed_mask_pairs_and_single_sequence(lens, B):
+    M = orc.mask_packed(lens, B)
+    assert M.sum() == sum(n * (n + B) for n in lens)
+    if len(lens) == 1:
+        assert (M == orc.mask_2L(lens[0], B)).all()
+
+
+@pytest.mark.parametrize("lens,B,Hq,Hkv", [((16, 8, 24), 4, 4, 2), ((6, 12), 3, 3, 1), ((8, 8, 8, 8), 8, 2, 2)])
+def test_packed_brute_equals_per_sequence(lens, B, Hq, Hkv):
+    """The packed definition (one mask over the whole batch) equals each
+    sequence computed alone: the decomposition the packed GPU tests use."""
+    T, d = sum(lens), 8
+    Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn = _rand(T, Hq, Hkv, d, seed=T + B)
+    sc = 0.35
+    M = orc.mask_packed(lens, B)
+    fwd = orc.fwd_brute(Qc, Kc, Vc, Qn, Kn, Vn, B, sc, mask=M)
+    bwd = orc.bwd_brute(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, B, sc, mask=M)
+    off = np.concatenate([[0], np.cumsum(lens)])
+    for s in range(len(lens)):
+        a, b = off[s], off[s + 1]
+        x = [t[a:b] for t in (Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn)]
+        rf = orc.fwd_blockwise(*x[:6], B, sc)
+        rb = orc.bwd_blockwise(*x, B, sc)
+        for got, ref in zip((fwd[0][a:b], fwd[1][a:b], fwd[2][:, a:b], fwd[3][:, a:b]), rf):
+            np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+        for got, ref in zip(bwd, rb):
+            np.testing.assert_allclose(got[a:b], ref, rtol=0, atol=1e-12)
+
+
 # ------------------------------------------------------------------ closed forms
 def test_zero_keys_uniform_softmax():
     """K = 0 makes every visible score 0: LSE_i = ln(#visible_i) with
