@@ -110,3 +110,32 @@ def test_varlen_refuses_graph_capture(lib):
     m.bdlm_attn_fwd_varlen(*ins, lens, 64, out=out, workspace=ws)
     torch.cuda.synchronize()
     assert torch.isfinite(out[0].float()).all()
+
+
+def test_varlen_many_sequences(lib):
+    """1536 sequences (the work-list directory and its device expansion at
+    scale): sampled sequences against the oracle, each computed alone."""
+    from structured_mask_attention_gb300.inputs import make_torch
+    m = lib
+    B, Hq, Hkv, d = 64, 2, 1, 64
+    lens = [64 * (1 + (7 * i) % 3) for i in range(1536)]  # 64, 128 or 192 tokens
+    T = sum(lens)
+    X = make_torch(T, Hq, Hkv, d, seed=11, device="cuda")
+    ins = [X[k] for k in NAMES[:6]]
+    sc = 1.0 / math.sqrt(d)
+    Oc, On, LSEc, LSEn = m.bdlm_attn_fwd_varlen(*ins, lens, B, sc)
+    grads = m.bdlm_attn_bwd_varlen(*ins, Oc, On, X["dOc"], X["dOn"], LSEc, LSEn, lens, B, sc,
+                                   g_dtype=torch.float32)
+    torch.cuda.synchronize()
+    off = np.concatenate([[0], np.cumsum(lens)])
+    for s in (0, 1, 2, 777, 1535):
+        a, b = int(off[s]), int(off[s + 1])
+        X64 = {k: to_np(X[k][a:b]) for k in NAMES}
+        ref = orc.fwd_blockwise(*[X64[k] for k in NAMES[:6]], B, sc)
+        gref = orc.bwd_blockwise(*[X64[k] for k in NAMES], B, sc)
+        check_rel(f"Oc[{s}]", to_np(Oc[a:b]), ref[0])
+        check_rel(f"On[{s}]", to_np(On[a:b]), ref[1])
+        check_lse(f"LSEc[{s}]", to_np(LSEc[:, a:b]), ref[2])
+        check_lse(f"LSEn[{s}]", to_np(LSEn[:, a:b]), ref[3])
+        for name, g, r in zip(("dQc", "dKc", "dVc", "dQn", "dKn", "dVn"), grads, gref):
+            check_rel(f"{name}[{s}]", to_np(g[a:b]), r)
