@@ -40,10 +40,11 @@ LSE and D are ``[H, L]``.  Inputs are expected to already hold the values the
 GPU sees (bf16-representable numbers), upcast to float64.
 
 Every function here is pinned by ``tests/test_oracle.py`` against things other
-than itself: a hand-typed mask fixture, closed forms, torch's fp64
-scaled-dot-product attention (and its autograd) in the cases where the mask
-reduces to textbook attention, central finite differences, exact gradient
-invariants and the Proposition-1 sharding identity.
+than itself: hand-typed mask fixtures (one sequence, and a packed batch of
+two), closed forms, torch's fp64 scaled-dot-product attention (and its
+autograd) in the cases where the mask reduces to textbook attention, central
+finite differences, exact gradient invariants and the Proposition-1 sharding
+identity.
 """
 from __future__ import annotations
 

@@ -417,3 +417,34 @@ def test_planted_mistakes_are_caught(monkeypatch):
     with pytest.raises(AssertionError):
         test_finite_differences()
     monkeypatch.setattr(orc, "bwd_partial", real_partial)
+
+
+def _planted(fn, old, new):
+    """``fn`` recompiled from its source with one edit (a planted mistake), in
+    the oracle module's namespace."""
+    import inspect
+    import textwrap
+    src = textwrap.dedent(inspect.getsource(fn))
+    assert old in src, (fn.__name__, old)
+    ns = dict(vars(orc))
+    exec(compile(src.replace(old, new), f"<planted {fn.__name__}>", "exec"), ns)
+    return ns[fn.__name__]
+
+
+@pytest.mark.parametrize("fn_name,old,new,pin", [
+    # gradient arithmetic: a sign error in dS, P in place of dS for dQ, and a
+    # dropped GQA reduction for dK (only the group's first head counted)
+    ("bwd_partial", "(dP - D[h, r][:, None])", "(dP + D[h, r][:, None])", "test_single_block_is_full_attention_per_stream"),
+    ("bwd_partial", "scale * (dS @ K)", "scale * (Pm @ K)", "test_single_block_is_full_attention_per_stream"),
+    ("bwd_partial", "+= gK[off:off + n]", "+= gK[off:off + n] * (h % g == 0)", "test_single_block_is_full_attention_per_stream"),
+    # masks: corrupted rows reading their own clean block; a packed batch whose
+    # rows see the other sequences
+    ("mask_2L", "noisy_clean = col < row", "noisy_clean = col <= row", "test_mask_matches_hand_typed_fixture"),
+    ("mask_packed", "same = seq[:, None] == seq[None, :]", "same = seq[:, None] >= 0", "test_packed_mask_matches_hand_typed_fixture"),
+])
+def test_planted_source_mistakes_are_caught(monkeypatch, fn_name, old, new, pin):
+    """Plant a mistake in the oracle's source (CPU only) and check that the
+    named pin rejects it."""
+    monkeypatch.setattr(orc, fn_name, _planted(getattr(orc, fn_name), old, new))
+    with pytest.raises(AssertionError):
+        globals()[pin]()
