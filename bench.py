@@ -349,8 +349,18 @@ def run_native(args, rank, world, local_rank):
     alg = {"bdlm_fwd_tc": 4.0 * d * pairs, "bdlm_bwd_dkv": 8.0 * d * pairs, "bdlm_bwd_dq": 6.0 * d * pairs}
     per_kernel = {}
     for k, (cnt, tot) in ktimes.items():
-        per_kernel[k] = {"launches": cnt, "ms_per_launch": round(tot / max(cnt, 1), 4),
-                         "share": round(tot / max(sum(v[1] for v in ktimes.values()), 1e-9), 4)}
+        ms_k = tot / max(cnt, 1)
+        e = {"launches": cnt, "ms_per_launch": round(ms_k, 4),
+             "share": round(tot / max(sum(v[1] for v in ktimes.values()), 1e-9), 4)}
+        if k in alg and ms_k > 0:
+            # executed FLOP per launch (recomputed products included) against the sustained peak
+            tf_k = alg[k] / (ms_k * 1e-3) / 1e12
+            e.update({"tflops": round(tf_k, 1), "frac": round(tf_k / peak_tf, 4),
+                      "traffic": committed_traffic(k)})
+        elif k == "bdlm_preprocess" and ms_k > 0:
+            # one launch per stream: reads O and dO (bf16), writes D (fp32)
+            e["gbs"] = round((2 * 2 * L * Hq * d + 4 * L * Hq) / (ms_k * 1e-3) / 1e9, 1)
+        per_kernel[k] = e
     dom = max((k for k in ktimes if k in alg), key=lambda k: ktimes[k][1])
     dom_ms = ktimes[dom][1] / ktimes[dom][0]
     achieved = alg[dom] / (dom_ms * 1e-3) / 1e12
