@@ -1,0 +1,131 @@
+// Host check of the work orders in geometry.cuh (compiled with g++ by
+// tests/test_geometry_host.py): every enumeration the kernels walk must visit
+// each work item exactly once, for blocked and unblocked lists, sharded key
+// ranges and the natural (ablation) order.  Prints one line per failure and
+// exits non-zero if any.
+#include <cstdio>
+#include <cstdlib>
+#include <vector>
+
+#include "geometry.cuh"
+
+using namespace bdlm;
+
+static int failures = 0;
+#define CHECK(cond, ...)                     \
+  do {                                       \
+    if (!(cond)) {                           \
+      ++failures;                            \
+      if (failures < 20) {                   \
+        std::printf("FAIL %s: ", #cond);     \
+        std::printf(__VA_ARGS__);            \
+        std::printf("\n");                   \
+      }                                      \
+    }                                        \
+  } while (0)
+
+// (stream, head, query tile) items of the forward / dQ lists.
+static void check_q(const Geom& g, int tq) {
+  const int64_t nqt = cdiv64(g.L, tq);
+  const int64_t n = q_items(g, tq);
+  CHECK(n == nqt * g.Hq * 2, "L=%lld tq=%d", (long long)g.L, tq);
+  std::vector<unsigned char> seen((size_t)n, 0);
+  for (int64_t i = 0; i < n; ++i) {
+    const QItem it = q_item(g, tq, i);
+    const bool ok = it.stream >= 0 && it.stream < 2 && it.head >= 0 && it.head < g.Hq && it.qtile >= 0 &&
+                    it.qtile < nqt;
+    CHECK(ok, "q item %lld out of range (L=%lld Hq=%d Hkv=%d tq=%d)", (long long)i, (long long)g.L, g.Hq, g.Hkv,
+          tq);
+    if (!ok) continue;
+    const int64_t key = (it.qtile * g.Hq + it.head) * 2 + it.stream;
+    CHECK(!seen[(size_t)key], "q item repeated (L=%lld tq=%d idx=%lld)", (long long)g.L, tq, (long long)i);
+    seen[(size_t)key] = 1;
+  }
+  // rotation of the clean-key sweep stays inside the range
+  for (int64_t i = 0; i < n; i += 97)
+    for (int nc = 1; nc < 600; nc += 37) {
+      const int r = sweep_rotation(i, nc);
+      CHECK(r >= 0 && r < nc, "rotation %d of %d", r, nc);
+    }
+}
+
+// (key stream, KV head, key tile) items of the dK/dV list.
+static void check_kv(const Geom& g, int tk) {
+  int64_t cf, cc, nn;
+  kv_tile_span(g, tk, cf, cc, nn);
+  const int64_t n = kv_items(g, tk);
+  CHECK(n == (cc + nn) * g.Hkv, "kv count L=%lld", (long long)g.L);
+  const int64_t ntile = cdiv64(g.L, tk);
+  std::vector<unsigned char> seen((size_t)(2 * g.Hkv * ntile), 0);
+  for (int64_t i = 0; i < n; ++i) {
+    const KVItem it = kv_item(g, tk, i);
+    const bool in_span = it.key_stream == 0 ? (it.ktile >= cf && it.ktile < cf + cc) : (it.ktile >= 0 && it.ktile < nn);
+    const bool ok = (it.key_stream == 0 || it.key_stream == 1) && it.kv_head >= 0 && it.kv_head < g.Hkv && in_span;
+    CHECK(ok, "kv item %lld out of range (L=%lld kv=[%lld,%lld) local=%d)", (long long)i, (long long)g.L,
+          (long long)g.kv_begin, (long long)g.kv_end, g.include_local);
+    if (!ok) continue;
+    const int64_t key = ((int64_t)it.key_stream * g.Hkv + it.kv_head) * ntile + it.ktile;
+    CHECK(!seen[(size_t)key], "kv item repeated (L=%lld idx=%lld)", (long long)g.L, (long long)i);
+    seen[(size_t)key] = 1;
+  }
+}
+
+// The persistent grid's assignment visits every list index once.
+static void check_sched(const Geom& g, int grid, int64_t rounds) {
+  std::vector<unsigned char> seen((size_t)(grid * rounds), 0);
+  for (int64_t r = 0; r < rounds; ++r)
+    for (int c = 0; c < grid; ++c) {
+      const int64_t idx = sched_item(g, r, c, grid);
+      const bool ok = idx >= r * grid && idx < (r + 1) * grid;
+      CHECK(ok, "sched round %lld cta %d -> %lld", (long long)r, c, (long long)idx);
+      if (ok) {
+        CHECK(!seen[(size_t)idx], "sched index %lld repeated", (long long)idx);
+        seen[(size_t)idx] = 1;
+      }
+    }
+}
+
+int main() {
+  const int64_t Ls[] = {96, 256, 1024, 8192, 16384, 32768, 131072, 262144};
+  const int64_t Bs[] = {32, 128, 512};
+  const int heads[][2] = {{2, 2}, {16, 8}, {32, 8}, {40, 8}, {8, 4}, {5, 1}};
+  for (int naive = 0; naive < 2; ++naive)
+    for (int64_t L : Ls)
+      for (int64_t B : Bs) {
+        if (L % B) continue;
+        for (const auto& h : heads) {
+          Geom g{L, B, h[0], h[1], 0, L, 1};
+          g.naive_order = naive;
+          for (int tq : {128, 256}) check_q(g, tq);
+          check_kv(g, 128);
+          // clean-key shards (CSBP), with and without the local block
+          const int P = 8;
+          if (L % P == 0)
+            for (int s = 0; s < P; s += 3) {
+              Geom gs = g;
+              gs.kv_begin = s * (L / P);
+              gs.kv_end = (s + 1) * (L / P);
+              gs.include_local = 0;
+              check_kv(gs, 128);
+              for (int tq : {128, 256}) check_q(gs, tq);
+            }
+          Geom gl = g;
+          gl.kv_begin = gl.kv_end = 0;  // the local partial alone
+          check_kv(gl, 128);
+          // one sequence of a packed batch
+          const Geom gp = seq_geom(g, L / 2 - (L / 2) % B > 0 ? L / 2 - (L / 2) % B : B);
+          check_kv(gp, 128);
+          check_q(gp, 128);
+        }
+        Geom g{L, B, 16, 8, 0, L, 1};
+        g.naive_order = naive;
+        check_sched(g, 152, 7);
+        check_sched(g, 37, 5);
+      }
+  if (failures) {
+    std::printf("%d failures\n", failures);
+    return 1;
+  }
+  std::printf("ok\n");
+  return 0;
+}
