@@ -85,6 +85,64 @@ static void check_sched(const Geom& g, int grid, int64_t rounds) {
     }
 }
 
+// Brute-force visibility (the mask, with the call's key restriction).
+static bool sees(const Geom& g, int s, int64_t i, int ks, int64_t j) {
+  const int64_t bi = i / g.B, bj = j / g.B;
+  if (ks == 0) {
+    if (j < g.kv_begin || j >= g.kv_end) return false;
+    return s == 0 ? bj <= bi : bj < bi;
+  }
+  return g.include_local && s == 1 && bj == bi;
+}
+
+// kv_tile_rows (the rows a key tile is read by) and qtile_ranges (the key
+// tiles a query tile reads, and the keys all its rows see) against the mask.
+static void check_ranges(const Geom& g, int t) {
+  const int64_t nt = cdiv64(g.L, t);
+  for (int ks = 0; ks < 2; ++ks)
+    for (int64_t kt = 0; kt < nt; ++kt) {
+      const int64_t j0 = kt * t, j1 = imin64(j0 + t, g.L);
+      int64_t r[4];
+      kv_tile_rows(g, ks, j0, j1, r[0], r[1], r[2], r[3]);
+      for (int s = 0; s < 2; ++s) {
+        const int64_t lo = r[2 * s], hi = r[2 * s + 1];
+        for (int64_t i = 0; i < g.L; ++i) {
+          bool any = false;
+          for (int64_t j = j0; j < j1 && !any; ++j) any = sees(g, s, i, ks, j);
+          CHECK(any == (i >= lo && i < hi), "kv_tile_rows ks=%d tile=%lld s=%d row=%lld (L=%lld B=%lld)", ks,
+                (long long)kt, s, (long long)i, (long long)g.L, (long long)g.B);
+        }
+      }
+    }
+  for (int s = 0; s < 2; ++s)
+    for (int64_t qt = 0; qt < nt; ++qt) {
+      const int64_t r0 = qt * t, r1 = imin64(r0 + t, g.L);
+      const QTileRanges q = qtile_ranges(g, s, r0, r1, t);
+      for (int ks = 0; ks < 2; ++ks)
+        for (int64_t kt = 0; kt < nt; ++kt) {
+          const int64_t j0 = kt * t, j1 = imin64(j0 + t, g.L);
+          bool any = false;
+          for (int64_t i = r0; i < r1 && !any; ++i)
+            for (int64_t j = j0; j < j1 && !any; ++j) any = sees(g, s, i, ks, j);
+          const bool listed = ks == 0 ? (kt >= q.c0 && kt < q.c1) : (kt >= q.n0 && kt < q.n1);
+          CHECK(any == listed, "qtile_ranges s=%d qtile=%lld ks=%d ktile=%lld (L=%lld B=%lld)", s, (long long)qt,
+                ks, (long long)kt, (long long)g.L, (long long)g.B);
+        }
+      // keys every row of the tile sees: exactly the stated intervals
+      for (int64_t j = 0; j < g.L; ++j) {
+        bool all_c = true, all_n = true;
+        for (int64_t i = r0; i < r1; ++i) {
+          all_c = all_c && sees(g, s, i, 0, j);
+          all_n = all_n && sees(g, s, i, 1, j);
+        }
+        CHECK(all_c == (j >= q.c_all_lo && j < q.c_all_hi), "c_all s=%d qtile=%lld key=%lld", s, (long long)qt,
+              (long long)j);
+        CHECK(all_n == (j >= q.n_all_lo && j < q.n_all_hi), "n_all s=%d qtile=%lld key=%lld", s, (long long)qt,
+              (long long)j);
+      }
+    }
+}
+
 int main() {
   const int64_t Ls[] = {96, 256, 1024, 8192, 16384, 32768, 131072, 262144};
   const int64_t Bs[] = {32, 128, 512};
@@ -121,6 +179,20 @@ int main() {
         g.naive_order = naive;
         check_sched(g, 152, 7);
         check_sched(g, 37, 5);
+      }
+  // tile ranges against the mask on small shapes: tiles smaller than,
+  // equal to and larger than the blocks, ragged tails, shards, no local block
+  for (int64_t L : {48, 96, 160, 256})
+    for (int64_t B : {1, 8, 16, 32, 48})
+      for (int t : {16, 32, 64}) {
+        if (L % B) continue;
+        for (int v = 0; v < 4; ++v) {
+          Geom g{L, B, 2, 1, 0, L, 1};
+          if (v == 1) { g.kv_begin = L / 4; g.kv_end = L / 2; }
+          if (v == 2) { g.kv_begin = L / 3; g.kv_end = L; g.include_local = 0; }
+          if (v == 3) { g.kv_begin = g.kv_end = 0; }
+          check_ranges(g, t);
+        }
       }
   if (failures) {
     std::printf("%d failures\n", failures);
