@@ -210,10 +210,11 @@ bdlm_status bdlm_attn_bwd_shard(const void* Qc, const void* Kc, const void* Vc,
  * host array may be freed then); the library's own copy reaches the
  * workspace on the stream, and a small kernel expands it into the work list.
  * These calls cannot be captured into a CUDA graph (BDLM_ERR_UNSUPPORTED):
- * they copy host data that differs from call to call.  BDLM_VARLEN_ORDER=lpt instead
- * orders all items longest first over the whole batch, built on the host (a
- * scheduling ablation).  Same conventions, dtypes and error behaviour as
- * bdlm_attn_fwd / bdlm_attn_bwd.
+ * they copy host data that differs from call to call.
+ * BDLM_VARLEN_ORDER=lpt instead orders all items longest first over the
+ * whole batch, built on the host (a scheduling ablation).  Same conventions,
+ * dtypes and error behaviour as bdlm_attn_fwd / bdlm_attn_bwd (the backward
+ * takes the forward's O and LSE of the same packed batch).
  *
  * bdlm_workspace_size_varlen: bytes of workspace for op BDLM_OP_FWD or
  * BDLM_OP_BWD (0 for another op or a bad shape). */
