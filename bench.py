@@ -579,6 +579,21 @@ def run_sweep(args):
         del X, ins, f, g, fo, go, wf, wb
         torch.cuda.empty_cache()
 
+    # ---- the fp64 oracle on the host cores: a timed sample per config,
+    # extrapolated by useful FLOP to the whole config (all heads, both streams)
+    for name in (("tiny", "gqa-8k", "gqa-32k", "long-128k", "sharded-256k") if "oracle" in want else ()):
+        w = WORKLOADS[name]
+        L, B, Hq, Hkv, d = w["L"], w["B"], w["Hq"], w["Hkv"], w["d"]
+        if name == "sharded-256k":
+            L, B = 4096, 512  # the 4096-token slice the parity tests check against the oracle
+        flops, dt, blocks, thr = oracle_sample(L, B, Hq, Hkv, d, budget_s=min(args.cpu_budget, 8.0))
+        rate = flops / dt
+        full = useful_flops(L, B, Hq, d)
+        emit({"sweep": "oracle", "workload": name, "L": L, "B": B, "Hq": Hq, "sample_blocks": blocks,
+              "sample_s": round(dt, 2), "oracle_gflops": round(rate / 1e9, 2),
+              "full_s": round(full / rate, 3 if full / rate < 10 else 1),
+              "extrapolated": blocks < L // B or Hq > 1, "threads": thr})
+
 
 # ------------------------------------------------------------------ reference arm
 def run_reference(args):
@@ -621,7 +636,7 @@ def main():
                          "schedule ablation (BDLM_SCHED=naive vs longest first) and the sharded-256k "
                          "block-size sweep with merge and preprocess bandwidth, and packed batches "
                          "(one packed call vs one call per sequence)")
-    ap.add_argument("--sweep-parts", default="config,sharded,packed",
+    ap.add_argument("--sweep-parts", default="config,sharded,packed,oracle",
                     help="comma-separated parts of --sweep to run (config includes the schedule ablation)")
     args = ap.parse_args()
     if args.warmup < 3:
