@@ -393,6 +393,24 @@ def run_native(args, rank, world, local_rank):
     return line
 
 
+def per_rank_memory(L, Hq, Hkv, d, R):
+    """Attention tensors one of R ranks holds for a fwd+bwd step (GiB), by
+    the shapes alone: bf16 Q, O, dO and fp32 dQ per query head; bf16 K, V and
+    fp32 dK, dV per KV head.  Pure BP: every rank processes the whole clean
+    sequence (replicated) plus its L / R corrupted tokens.  CSBP: its clean
+    shard and its corrupted blocks (2 L / R tokens), plus the clean K / V of
+    the other shards while they are exchanged (all-gathered: L tokens of bf16
+    K and V; a ring holds two shards)."""
+    q_tok = Hq * d * (2 + 2 + 2 + 4)
+    kv_tok = Hkv * d * (2 + 2 + 4 + 4)
+    bp = (L + L // R) * (q_tok + kv_tok)
+    csbp = 2 * (L // R) * (q_tok + kv_tok)
+    gathered = L * Hkv * d * 2 * 2
+    ring = 2 * (L // R) * Hkv * d * 2 * 2
+    g = lambda x: round(x / 2 ** 30, 2)
+    return {"pure_bp": g(bp), "csbp_allgather": g(csbp + gathered), "csbp_ring": g(csbp + ring)}
+
+
 # ------------------------------------------------------------------ sweep (measurement tables)
 def run_sweep(args):
     """Per-config timings, the schedule ablation and the sharded block-size
@@ -471,10 +489,20 @@ def run_sweep(args):
         ins = [X[k] for k in names]
         step = L // P
         bounds = [(s * step, (s + 1) * step) for s in range(P)]
+        # peak device memory of one fwd+bwd step of each schedule, inputs included
+        # (the single-device form of the pure-BP vs CSBP memory ablation)
+        torch.cuda.synchronize()
+        torch.cuda.reset_peak_memory_stats(dev)
         fu = m.bdlm_attn_fwd(*ins, B, sc)
         gu = m.bdlm_attn_bwd(*ins, fu[0], fu[1], X["dOc"], X["dOn"], fu[2], fu[3], B, sc)
+        torch.cuda.synchronize()
+        bp_peak = torch.cuda.max_memory_allocated(dev)
         un_f = timed(lambda: m.bdlm_attn_fwd(*ins, B, sc, out=fu))
         un_b = timed(lambda: m.bdlm_attn_bwd(*ins, fu[0], fu[1], X["dOc"], X["dOn"], fu[2], fu[3], B, sc, out=gu))
+        del gu
+        torch.cuda.synchronize()
+        base_mem = torch.cuda.memory_allocated(dev) - sum(t.numel() * t.element_size() for t in fu)
+        torch.cuda.reset_peak_memory_stats(dev)
         parts = [m.bdlm_attn_fwd_shard(*ins, B, lo, hi, False, sc) for (lo, hi) in bounds]
         parts.append(m.bdlm_attn_fwd_shard(*ins, B, 0, 0, True, sc))
         spec = [(lo, hi, False) for (lo, hi) in bounds] + [(0, 0, True)]
@@ -504,6 +532,13 @@ def run_sweep(args):
                 m.bdlm_attn_bwd_shard(*ins, X["dOc"], X["dOn"], ml[0], ml[1], Dc, Dn, B, lo, hi, loc,
                                       dQc, dQn, dKc, dVc, dKn, dVn, sc)
 
+        part_bwd()
+        torch.cuda.synchronize()
+        # the shard-and-merge step's peak: its partials, merged outputs, D and
+        # fp32 gradients on top of the inputs (the unsharded outputs, still
+        # allocated for the timing above, are not part of it)
+        csbp_peak = torch.cuda.max_memory_allocated(dev) - sum(t.numel() * t.element_size() for t in fu)
+        csbp_peak = max(csbp_peak, base_mem)
         sh_b = timed(part_bwd)
         # merge bytes: every non-empty (row, head, partial) O row read, all LSE_p read, O (bf16) and LSE written
         nonempty = sum(int((p_[2] > float("-inf")).sum().item() + (p_[3] > float("-inf")).sum().item())
@@ -518,8 +553,43 @@ def run_sweep(args):
               "unsharded_useful_tflops": round(useful_flops(L, B, Hq, d) / ((un_f + un_b) * 1e-3) / 1e12, 1),
               "sharded_useful_tflops": round(useful_flops(L, B, Hq, d) / (sh_tot * 1e-3) / 1e12, 1),
               "merge_share": round(mg / sh_tot, 5), "merge_gbs": round(mbytes / (mg * 1e-3) / 1e9, 1),
-              "merge_bytes": mbytes, "preprocess_gbs": round(pbytes / (pre * 1e-3) / 1e9, 1)})
-        del X, ins, fu, gu, parts, mo, ml, Dc, Dn, dQc, dQn, dKc, dVc, dKn, dVn
+              "merge_bytes": mbytes, "preprocess_gbs": round(pbytes / (pre * 1e-3) / 1e9, 1),
+              "unsharded_peak_gib": round(bp_peak / 2 ** 30, 2), "sharded_peak_gib": round(csbp_peak / 2 ** 30, 2),
+              "per_rank_gib_model_R8": per_rank_memory(L, Hq, Hkv, d, 8)})
+        del X, ins, fu, parts, mo, ml, Dc, Dn, dQc, dQn, dKc, dVc, dKn, dVn
+        torch.cuda.empty_cache()
+
+    # ---- sharded-256k: shard-and-merge vs unsharded fp32 output, production
+    # path (P rounded to bf16 against each path's running maximum) and the
+    # fixed-reference verification mode (same P in both paths)
+    for B in (SHARDED_BLOCK_SIZES if "shardcheck" in want else ()):
+        X = make_torch(L, Hq, Hkv, d, seed=B, device=dev)
+        ins = [X[k] for k in names]
+        step = L // P
+        specs = [(s * step, (s + 1) * step, False) for s in range(P)] + [(0, 0, True)]
+        u = m.bdlm_attn_fwd(*ins, B, sc, o_dtype=torch.float32)
+        res = {}
+        for mode in ("production", "fixed_reference"):
+            if mode == "production":
+                full = u
+                parts = [m.bdlm_attn_fwd_shard(*ins, B, lo, hi, loc, sc) for (lo, hi, loc) in specs]
+            else:
+                full = m.bdlm_attn_fwd_shard_refmax(*ins, B, 0, L, True, u[2], u[3], sc)
+                parts = [m.bdlm_attn_fwd_shard_refmax(*ins, B, lo, hi, loc, u[2], u[3], sc) for (lo, hi, loc) in specs]
+            oc, lc = m.bdlm_lse_merge([p_[0] for p_ in parts], [p_[2] for p_ in parts], o_dtype=torch.float32)
+            on, ln = m.bdlm_lse_merge([p_[1] for p_ in parts], [p_[3] for p_ in parts], o_dtype=torch.float32)
+            del parts
+            res[mode] = (max((oc - full[0]).abs().max().item(), (on - full[1]).abs().max().item()),
+                         max((lc - full[2]).abs().max().item(), (ln - full[3]).abs().max().item()))
+            del full, oc, on, lc, ln
+        omax = max(u[0].abs().max().item(), u[1].abs().max().item())
+        vmax = max(X["Vc"].abs().max().item(), X["Vn"].abs().max().item())
+        emit({"sweep": "shardcheck", "workload": "sharded-256k", "B": B, "P": P,
+              "production_max_abs_dO": res["production"][0], "production_max_abs_dLSE": res["production"][1],
+              "fixed_reference_max_abs_dO": res["fixed_reference"][0],
+              "fixed_reference_max_abs_dLSE": res["fixed_reference"][1],
+              "max_abs_O": omax, "max_abs_V": vmax})
+        del X, ins, u
         torch.cuda.empty_cache()
 
     # ---- packed batches: one packed call vs one call per sequence
@@ -636,8 +706,10 @@ def main():
                          "schedule ablation (BDLM_SCHED=naive vs longest first) and the sharded-256k "
                          "block-size sweep with merge and preprocess bandwidth, and packed batches "
                          "(one packed call vs one call per sequence)")
-    ap.add_argument("--sweep-parts", default="config,sharded,packed,oracle",
-                    help="comma-separated parts of --sweep to run (config includes the schedule ablation)")
+    ap.add_argument("--sweep-parts", default="config,sharded,shardcheck,packed,oracle",
+                    help="comma-separated parts of --sweep to run (config includes the schedule ablation; "
+                         "shardcheck: sharded vs unsharded fp32 output differences, production path and "
+                         "fixed-reference mode)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

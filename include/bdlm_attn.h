@@ -60,7 +60,7 @@ typedef enum {
   BDLM_ERR_ALIGN = 3,       /* a pointer not 16-byte aligned */
   BDLM_ERR_WORKSPACE = 4,   /* workspace missing or smaller than bdlm_workspace_size */
   BDLM_ERR_CUDA = 5,        /* a CUDA runtime/driver call or launch failed */
-  BDLM_ERR_UNSUPPORTED = 6, /* device is not sm_103 / sm_100 family */
+  BDLM_ERR_UNSUPPORTED = 6, /* device is not sm_103; or a packed-batch call inside CUDA-graph capture */
   BDLM_ERR_TIMEOUT = 7      /* a device-side bounded wait expired */
 } bdlm_status;
 
@@ -105,6 +105,31 @@ bdlm_status bdlm_attn_fwd_shard(const void* Qc, const void* Kc, const void* Vc,
                                 int64_t kv_begin, int64_t kv_end, int include_local,
                                 float* Op_c, float* Op_n, float* LSEp_c, float* LSEp_n,
                                 void* workspace, size_t ws_bytes, bdlm_stream stream);
+
+/* Verification mode of the partial forward, for checking that
+ * shard-and-merge reproduces the unsharded result up to floating-point
+ * reduction order (Proposition 1; evolve.pub FAQ "Does CSBP change training
+ * results?").  The production kernels round the probabilities P to bf16
+ * before the P.V product relative to each row's running maximum, which
+ * differs between a shard and the whole key range, so their fp32 outputs
+ * also differ by that rounding.  This call is bdlm_attn_fwd_shard with one
+ * change: every row forms P = exp(scale q.k - Mref) against a fixed reference
+ * Mref supplied by the caller, with no rescaling.  Called for the whole key
+ * range (kv_begin = 0, kv_end = L, include_local = 1) it gives the unsharded
+ * result; called per shard with the same Mref, every (row, key) probability
+ * is rounded identically in both, and only fp32 summation order differs.
+ * Mref_c, Mref_n: [Hq, L] fp32, natural log, finite, and at least the row's
+ * largest scaled score over the keys of the call (the LSE of the unsharded
+ * forward qualifies); a smaller value can overflow P.  Same outputs, layout
+ * and errors as bdlm_attn_fwd_shard; same speed class (one extra load per
+ * row).  Not for training: use the production calls. */
+bdlm_status bdlm_attn_fwd_shard_refmax(const void* Qc, const void* Kc, const void* Vc,
+                                       const void* Qn, const void* Kn, const void* Vn,
+                                       int64_t L, int64_t B, int Hq, int Hkv, int d, float scale,
+                                       int64_t kv_begin, int64_t kv_end, int include_local,
+                                       const float* Mref_c, const float* Mref_n,
+                                       float* Op_c, float* Op_n, float* LSEp_c, float* LSEp_n,
+                                       void* workspace, size_t ws_bytes, bdlm_stream stream);
 
 /* Exact merge of partial attention results over disjoint key sets
  * (Proposition 1 / evolve.pub FAQ "Does CSBP change training results?"):
@@ -154,9 +179,11 @@ bdlm_status bdlm_attn_bwd(const void* Qc, const void* Kc, const void* Vc,
  *    nothing, and bdlm_last_error() names the limit.
  *  - The array is created when the library's module is loaded on a device
  *    and every GPU that loads it holds it until the process exits.  The first
- *    call on a device also looks up the array's device address (once per
- *    device, with that device current); make that first call before any
- *    stream capture.
+ *    call on a device looks up the array's device address with that device
+ *    current (and looks it up again after the device's context was
+ *    re-created, e.g. by cudaDeviceReset); that lookup may load the
+ *    library's device code, so make the first call before any stream
+ *    capture.
  *  - Every call shares the one array per device and leaves its contents
  *    behind; each call clears the status word and rewrites D before use.
  *    Calls that overlap on the GPU (different streams, no ordering) race on
@@ -165,8 +192,9 @@ bdlm_status bdlm_attn_bwd(const void* Qc, const void* Kc, const void* Vc,
  *    per-kernel timing enabled (bdlm_timing_enable), launches also record
  *    CUDA events from a pool the library creates on first use: keep timing
  *    off when no allocation at all is allowed.
- * Kernel status (watchdog) is not reported through this call's return value;
- * errors of the launches themselves are. */
+ * Kernel status (a device wait that ran out of time) goes to the array's
+ * status word, not to this call's return value, which reports argument and
+ * launch errors: read it with bdlm_sync_status_noalloc. */
 bdlm_status bdlm_attn_bwd_noalloc(const void* Qc, const void* Kc, const void* Vc,
                                   const void* Qn, const void* Kn, const void* Vn,
                                   const void* Oc, const void* On, const void* dOc, const void* dOn,
@@ -174,6 +202,19 @@ bdlm_status bdlm_attn_bwd_noalloc(const void* Qc, const void* Kc, const void* Vc
                                   int64_t L, int64_t B, int Hq, int Hkv, int d, float scale,
                                   void* dQc, void* dKc, void* dVc, void* dQn, void* dKn, void* dVn,
                                   bdlm_dtype g_dtype, bdlm_stream stream);
+
+/* bdlm_sync_status for the array of bdlm_attn_bwd_noalloc on the current
+ * device: waits for `stream`, reads and clears the array's status word, and
+ * returns BDLM_ERR_TIMEOUT if a kernel of an earlier allocation-free call
+ * gave up on a device wait, BDLM_ERR_CUDA on a stream error, else BDLM_OK.
+ * Allocates nothing. */
+bdlm_status bdlm_sync_status_noalloc(bdlm_stream stream);
+
+/* bdlm_watchdog_selftest run on the status word of the allocation-free
+ * array (see bdlm_watchdog_selftest below): a wait nobody ends runs out after
+ * limit_us microseconds and the call returns BDLM_ERR_TIMEOUT, read back
+ * through bdlm_sync_status_noalloc.  Allocates nothing. */
+bdlm_status bdlm_watchdog_selftest_noalloc(uint32_t limit_us, bdlm_stream stream);
 
 /* Gradient contribution of one context shard, given the MERGED forward
  * statistics LSEc/LSEn and D (from bdlm_bwd_preprocess on the merged O):

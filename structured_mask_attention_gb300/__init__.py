@@ -18,9 +18,11 @@ import re
 
 __all__ = [
     "BdlmError", "load_library", "bdlm_workspace_size", "bdlm_attn_fwd", "bdlm_attn_fwd_shard",
+    "bdlm_attn_fwd_shard_refmax",
     "bdlm_lse_merge", "bdlm_bwd_preprocess", "bdlm_attn_bwd", "bdlm_attn_bwd_noalloc", "bdlm_attn_bwd_shard",
     "bdlm_worklist", "bdlm_workspace_size_varlen", "bdlm_attn_fwd_varlen", "bdlm_attn_bwd_varlen",
-    "bdlm_sync_status", "bdlm_watchdog_selftest", "bdlm_kernel_launches", "bdlm_last_error",
+    "bdlm_sync_status", "bdlm_watchdog_selftest", "bdlm_sync_status_noalloc", "bdlm_watchdog_selftest_noalloc",
+    "bdlm_kernel_launches", "bdlm_last_error",
     "bdlm_version", "bdlm_timing_enable", "bdlm_timing_report", "header_functions", "LIB_PATH",
     "HEADER_PATH",
 ]
@@ -54,6 +56,8 @@ _SIGS = {
     "bdlm_attn_fwd": (_I, [_P] * 6 + [_I64, _I64, _I, _I, _I, _F, _P, _P, _I, _P, _P, _P, _SZ, _P]),
     "bdlm_attn_fwd_shard": (_I, [_P] * 6 + [_I64, _I64, _I, _I, _I, _F, _I64, _I64, _I, _P, _P, _P, _P, _P,
                                             _SZ, _P]),
+    "bdlm_attn_fwd_shard_refmax": (_I, [_P] * 6 + [_I64, _I64, _I, _I, _I, _F, _I64, _I64, _I, _P, _P, _P, _P, _P,
+                                                   _P, _P, _SZ, _P]),
     "bdlm_lse_merge": (_I, [_I, _P, _P, _I64, _I, _I, _P, _I, _P, _P]),
     "bdlm_bwd_preprocess": (_I, [_P, _I, _P, _I64, _I, _I, _P, _P]),
     "bdlm_attn_bwd": (_I, [_P] * 12 + [_I64, _I64, _I, _I, _I, _F] + [_P] * 6 + [_I, _P, _SZ, _P]),
@@ -65,6 +69,8 @@ _SIGS = {
     "bdlm_attn_fwd_varlen": (_I, [_P] * 6 + [_P, _I, _I64, _I, _I, _I, _F, _P, _P, _I, _P, _P, _P, _SZ, _P]),
     "bdlm_attn_bwd_varlen": (_I, [_P] * 12 + [_P, _I, _I64, _I, _I, _I, _F] + [_P] * 6 + [_I, _P, _SZ, _P]),
     "bdlm_sync_status": (_I, [_P, _P]),
+    "bdlm_sync_status_noalloc": (_I, [_P]),
+    "bdlm_watchdog_selftest_noalloc": (_I, [ctypes.c_uint32, _P]),
     "bdlm_watchdog_selftest": (_I, [_P, _SZ, ctypes.c_uint32, _P]),
     "bdlm_kernel_launches": (ctypes.c_uint64, []),
     "bdlm_timing_enable": (_I, [_I]),
@@ -225,6 +231,32 @@ def bdlm_attn_fwd_shard(Qc, Kc, Vc, Qn, Kn, Vn, B: int, kv_begin: int, kv_end: i
     return out
 
 
+def bdlm_attn_fwd_shard_refmax(Qc, Kc, Vc, Qn, Kn, Vn, B: int, kv_begin: int, kv_end: int, include_local: bool,
+                               Mref_c, Mref_n, scale: float | None = None, out=None, workspace=None, stream=None):
+    """Verification mode of ``bdlm_attn_fwd_shard``: every row's probabilities
+    are formed against the fixed reference ``Mref_c`` / ``Mref_n`` ([Hq, L]
+    fp32, natural log, e.g. the unsharded forward's LSE) instead of its
+    running maximum.  Returns (Op_c, Op_n, LSEp_c, LSEp_n), fp32."""
+    torch = _torch()
+    _check_inputs(Qc, Kc, Vc, Qn, Kn, Vn)
+    L, Hq, Hkv, d = _shape(Qc, Kc)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    for t in (Mref_c, Mref_n):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.float32 or tuple(t.shape) != (Hq, L):
+            raise ValueError("Mref must be a contiguous float32 CUDA tensor of shape [Hq, L]")
+    if out is None:
+        out = (torch.empty((L, Hq, d), dtype=torch.float32, device=Qc.device),
+               torch.empty((L, Hq, d), dtype=torch.float32, device=Qc.device),
+               torch.empty((Hq, L), dtype=torch.float32, device=Qc.device),
+               torch.empty((Hq, L), dtype=torch.float32, device=Qc.device))
+    ws = _workspace(OP_FWD_SHARD, L, B, Hq, Hkv, d, Qc.device, workspace)
+    _check(load_library().bdlm_attn_fwd_shard_refmax(
+        _ptr(Qc), _ptr(Kc), _ptr(Vc), _ptr(Qn), _ptr(Kn), _ptr(Vn), L, B, Hq, Hkv, d, scale,
+        kv_begin, kv_end, int(bool(include_local)), _ptr(Mref_c), _ptr(Mref_n), *[_ptr(t) for t in out],
+        _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
 def bdlm_lse_merge(O_parts, LSE_parts, o_dtype=None, out=None, lse_out=None, write_lse: bool = True,
                    stream=None):
     """Exact LSE merge of fp32 partials [rows, H, d] / [H, rows].
@@ -274,10 +306,14 @@ def bdlm_attn_bwd(Qc, Kc, Vc, Qn, Kn, Vn, Oc, On, dOc, dOn, LSEc, LSEn, B: int, 
 
 
 def bdlm_attn_bwd_noalloc(Qc, Kc, Vc, Qn, Kn, Vn, Oc, On, dOc, dOn, LSEc, LSEn, B: int,
-                          scale: float | None = None, g_dtype=None, out=None, stream=None):
+                          scale: float | None = None, g_dtype=None, out=None, stream=None,
+                          check_status: bool = True):
     """bdlm_attn_bwd without a workspace argument, for callers that cannot
     allocate device memory: the library uses its own fixed-size device array
-    (Hq * L <= 4194272).  Returns (dQc, dKc, dVc, dQn, dKn, dVn)."""
+    (Hq * L <= 4194272).  With ``check_status`` (the default) the call waits
+    for the stream and raises BdlmError(BDLM_ERR_TIMEOUT) if a kernel gave up
+    on a device wait (``bdlm_sync_status_noalloc``); pass False to keep the
+    call asynchronous and check later.  Returns (dQc, dKc, dVc, dQn, dKn, dVn)."""
     torch = _torch()
     _check_inputs(Qc, Kc, Vc, Qn, Kn, Vn, Oc, On, dOc, dOn)
     L, Hq, Hkv, d = _shape(Qc, Kc)
@@ -291,6 +327,8 @@ def bdlm_attn_bwd_noalloc(Qc, Kc, Vc, Qn, Kn, Vn, Oc, On, dOc, dOn, LSEc, LSEn, 
         _ptr(Qc), _ptr(Kc), _ptr(Vc), _ptr(Qn), _ptr(Kn), _ptr(Vn), _ptr(Oc), _ptr(On), _ptr(dOc), _ptr(dOn),
         _ptr(LSEc), _ptr(LSEn), L, B, Hq, Hkv, d, scale, _ptr(dQc), _ptr(dKc), _ptr(dVc), _ptr(dQn), _ptr(dKn),
         _ptr(dVn), _dt(g_dtype), _stream(stream)))
+    if check_status:
+        bdlm_sync_status_noalloc(stream)
     return out
 
 
@@ -404,6 +442,18 @@ def bdlm_sync_status(workspace, stream=None):
     """Synchronises and raises BdlmError(BDLM_ERR_TIMEOUT) if a kernel's
     bounded wait expired since the last call on this workspace."""
     _check(load_library().bdlm_sync_status(_ptr(workspace), _stream(stream)))
+
+
+def bdlm_sync_status_noalloc(stream=None):
+    """Synchronises and raises BdlmError(BDLM_ERR_TIMEOUT) if a kernel of an
+    allocation-free call gave up on a device wait since the last check."""
+    _check(load_library().bdlm_sync_status_noalloc(_stream(stream)))
+
+
+def bdlm_watchdog_selftest_noalloc(limit_us: int = 20000, stream=None) -> int:
+    """The watchdog self-test on the allocation-free array's status word;
+    returns the status code (7 = the wait ran out and was reported)."""
+    return int(load_library().bdlm_watchdog_selftest_noalloc(limit_us, _stream(stream)))
 
 
 def bdlm_watchdog_selftest(workspace, limit_us: int = 20000, stream=None) -> int:

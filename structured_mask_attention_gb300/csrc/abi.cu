@@ -243,7 +243,8 @@ bdlm_status finish(cudaError_t e, int launches, const char* what) {
 bdlm_status fwd_common(const void* Qc, const void* Kc, const void* Vc, const void* Qn, const void* Kn,
                        const void* Vn, int64_t L, int64_t B, int Hq, int Hkv, int d, float scale, int64_t kv_begin,
                        int64_t kv_end, int include_local, void* Oc, void* On, int o_f32, float* LSEc, float* LSEn,
-                       void* ws, size_t ws_bytes, cudaStream_t st, const VarlenTabs* vt = nullptr) {
+                       void* ws, size_t ws_bytes, cudaStream_t st, const VarlenTabs* vt = nullptr,
+                       const FwdRef* ref = nullptr) {
   DeviceInfo info;
   BDLM_CHECK(device_info(info));
   EncodeTiledFn enc;
@@ -258,6 +259,7 @@ bdlm_status fwd_common(const void* Qc, const void* Kc, const void* Vc, const voi
   FwdParams p;
   p.g = Geom{L, B, Hq, Hkv, kv_begin, kv_end, include_local ? 1 : 0};
   p.g.naive_order = naive_schedule();
+  p.g.round_items = info.sms;  // the persistent grid: one CTA per SM
   p.scale_log2 = scale * 1.4426950408889634f;
   p.Oc = Oc;
   p.On = On;
@@ -270,7 +272,7 @@ bdlm_status fwd_common(const void* Qc, const void* Kc, const void* Vc, const voi
   BDLM_CHECK(clear_status(ws, st));
   int launches = 0;
   ScopedKernelTimer tm(K_FWD, st);
-  cudaError_t e = launch_fwd(maps, p, vt, d, info.sms, st, &launches);
+  cudaError_t e = launch_fwd(maps, p, vt, ref, d, info.sms, st, &launches);
   tm.stop();
   return finish(e, launches, "forward launch");
 }
@@ -278,10 +280,11 @@ bdlm_status fwd_common(const void* Qc, const void* Kc, const void* Vc, const voi
 BwdParams bwd_params(const void* Qc, const void* Kc, const void* Vc, const void* Qn, const void* Kn, const void* Vn,
                      const void* dOc, const void* dOn, const float* LSEc, const float* LSEn, const float* Dc,
                      const float* Dn, int64_t L, int64_t B, int Hq, int Hkv, int d, float scale, int64_t kv_begin,
-                     int64_t kv_end, int include_local) {
+                     int64_t kv_end, int include_local, int num_sms) {
   BwdParams p;
   p.g = Geom{L, B, Hq, Hkv, kv_begin, kv_end, include_local ? 1 : 0};
   p.g.naive_order = naive_schedule();
+  p.g.round_items = num_sms;  // the persistent grid: one CTA per SM
   p.d = d;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -576,6 +579,27 @@ bdlm_status bdlm_attn_fwd_shard(const void* Qc, const void* Kc, const void* Vc, 
   });
 }
 
+bdlm_status bdlm_attn_fwd_shard_refmax(const void* Qc, const void* Kc, const void* Vc, const void* Qn,
+                                       const void* Kn, const void* Vn, int64_t L, int64_t B, int Hq, int Hkv, int d,
+                                       float scale, int64_t kv_begin, int64_t kv_end, int include_local,
+                                       const float* Mref_c, const float* Mref_n, float* Op_c, float* Op_n,
+                                       float* LSEp_c, float* LSEp_n, void* workspace, size_t ws_bytes,
+                                       bdlm_stream stream) {
+  return guarded([&]() -> bdlm_status {
+    BDLM_CHECK(check_shape(L, B, Hq, Hkv, d));
+    BDLM_CHECK(check_scale(scale));
+    if (kv_begin < 0 || kv_end < kv_begin || kv_end > L)
+      return fail(BDLM_ERR_SHAPE, "clean key range [%lld, %lld) is not inside [0, %lld)", (long long)kv_begin,
+                  (long long)kv_end, (long long)L);
+    BDLM_CHECK(check_ptrs("bdlm_attn_fwd_shard_refmax(Qc,Kc,Vc,Qn,Kn,Vn,Mref_c,Mref_n,Op_c,Op_n,LSEp_c,LSEp_n)",
+                          {Qc, Kc, Vc, Qn, Kn, Vn, Mref_c, Mref_n, Op_c, Op_n, LSEp_c, LSEp_n}));
+    BDLM_CHECK(check_ws(workspace, ws_bytes, bdlm_workspace_size(BDLM_OP_FWD_SHARD, L, B, Hq, Hkv, d, 1)));
+    const FwdRef ref{Mref_c, Mref_n};
+    return fwd_common(Qc, Kc, Vc, Qn, Kn, Vn, L, B, Hq, Hkv, d, scale, kv_begin, kv_end, include_local, Op_c, Op_n,
+                      1, LSEp_c, LSEp_n, workspace, ws_bytes, static_cast<cudaStream_t>(stream), nullptr, &ref);
+  });
+}
+
 bdlm_status bdlm_lse_merge(int n_parts, const float* const* O_parts, const float* const* LSE_parts, int64_t rows,
                            int H, int d, void* O, bdlm_dtype o_dtype, float* LSE, bdlm_stream stream) {
   return guarded([&]() -> bdlm_status {
@@ -623,7 +647,7 @@ bdlm_status bdlm_bwd_preprocess(const void* O, bdlm_dtype o_dtype, const void* d
     int launches = 0;
     ScopedKernelTimer tm(K_PREP, static_cast<cudaStream_t>(stream));
     cudaError_t e = launch_preprocess(O, o_dtype == BDLM_F32, dO, rows, H, d, D, static_cast<cudaStream_t>(stream),
-                                      &launches);
+                                      &launches, info.sms);
     tm.stop();
     return finish(e, launches, "preprocess launch");
   });
@@ -652,13 +676,14 @@ bdlm_status bdlm_attn_bwd(const void* Qc, const void* Kc, const void* Vc, const 
     cudaError_t e;
     {
       ScopedKernelTimer tm(K_PREP, st);
-      e = launch_preprocess(Oc, 0, dOc, L, Hq, d, Dc, st, &launches);
+      e = launch_preprocess(Oc, 0, dOc, L, Hq, d, Dc, st, &launches, info.sms);
     }
     if (e == cudaSuccess) {
       ScopedKernelTimer tm(K_PREP, st);
-      e = launch_preprocess(On, 0, dOn, L, Hq, d, Dn, st, &launches);
+      e = launch_preprocess(On, 0, dOn, L, Hq, d, Dn, st, &launches, info.sms);
     }
-    BwdParams p = bwd_params(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn, L, B, Hq, Hkv, d, scale, 0, L, 1);
+    BwdParams p = bwd_params(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn, L, B, Hq, Hkv, d, scale, 0, L, 1,
+                             info.sms);
     p.dQc = dQc; p.dQn = dQn; p.dKc = dKc; p.dVc = dVc; p.dKn = dKn; p.dVn = dVn;
     p.g_f32 = g_dtype == BDLM_F32;
     bdlm_status vs = BDLM_OK;
@@ -690,7 +715,7 @@ bdlm_status bdlm_attn_bwd_shard(const void* Qc, const void* Kc, const void* Vc, 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     BDLM_CHECK(clear_status(workspace, st));
     BwdParams p = bwd_params(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn, L, B, Hq, Hkv, d, scale, kv_begin,
-                             kv_end, include_local);
+                             kv_end, include_local, info.sms);
     p.dQc = dQc_acc; p.dQn = dQn_acc; p.dKc = dKc; p.dVc = dVc; p.dKn = dKn; p.dVn = dVn;
     p.g_f32 = 1;
     p.dq_accumulate = 1;
@@ -833,9 +858,12 @@ bdlm_status bdlm_attn_fwd_varlen(const void* Qc, const void* Kc, const void* Vc,
                           {Qc, Kc, Vc, Qn, Kn, Vn, Oc, On, LSEc, LSEn}));
     const VarlenLayout lay = varlen_layout(BDLM_OP_FWD, seq_offsets, n_seqs, Hq, Hkv, T);
     BDLM_CHECK(check_ws(workspace, ws_bytes, lay.total));
+    DeviceInfo info;
+    BDLM_CHECK(device_info(info));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Geom all{T, B, Hq, Hkv, 0, T, 1};
     all.naive_order = naive_schedule();
+    all.round_items = info.sms;
     VarlenTabs vt;
     int launches = 0;
     BDLM_CHECK(varlen_tables(all, seq_offsets, n_seqs, kFwdItemRows, false, lay, static_cast<char*>(workspace), st,
@@ -870,6 +898,7 @@ bdlm_status bdlm_attn_bwd_varlen(const void* Qc, const void* Kc, const void* Vc,
     float* Dn = Dc + (size_t)Hq * T;
     Geom all{T, B, Hq, Hkv, 0, T, 1};
     all.naive_order = naive_schedule();
+    all.round_items = info.sms;
     VarlenTabs vt;
     int tab_launches = 0;
     BDLM_CHECK(varlen_tables(all, seq_offsets, n_seqs, kBwdTile, true, lay, w, st, &tab_launches, &vt));
@@ -879,13 +908,14 @@ bdlm_status bdlm_attn_bwd_varlen(const void* Qc, const void* Kc, const void* Vc,
     cudaError_t e;
     {
       ScopedKernelTimer tm(K_PREP, st);
-      e = launch_preprocess(Oc, 0, dOc, T, Hq, d, Dc, st, &launches);
+      e = launch_preprocess(Oc, 0, dOc, T, Hq, d, Dc, st, &launches, info.sms);
     }
     if (e == cudaSuccess) {
       ScopedKernelTimer tm(K_PREP, st);
-      e = launch_preprocess(On, 0, dOn, T, Hq, d, Dn, st, &launches);
+      e = launch_preprocess(On, 0, dOn, T, Hq, d, Dn, st, &launches, info.sms);
     }
-    BwdParams p = bwd_params(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn, T, B, Hq, Hkv, d, scale, 0, T, 1);
+    BwdParams p = bwd_params(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn, T, B, Hq, Hkv, d, scale, 0, T, 1,
+                             info.sms);
     p.dQc = dQc; p.dQn = dQn; p.dKc = dKc; p.dVc = dVc; p.dKn = dKn; p.dVn = dVn;
     p.g_f32 = g_dtype == BDLM_F32;
     bdlm_status vs = BDLM_OK;

@@ -32,6 +32,12 @@
 // Every MMA is M = 128, N = 128 (N = d for PV).  Only key tiles some row of
 // the item can see are visited; a per-row interval test masks the tiles that
 // are not fully visible.
+//
+// A separate instantiation (FIXREF) serves verification: each row takes a
+// fixed reference M_ref from the caller in place of its running maximum, so
+// P = exp(scale q.k - M_ref) needs no rescaling and is rounded to bf16 the
+// same way in every call that sees the same key tile for that row (the
+// sharded and unsharded paths then differ only by fp32 summation order).
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -46,6 +52,7 @@ constexpr int BN = kFwdTileK;      // keys per step (128)
 constexpr int kThreads = 320;
 constexpr int kPanel = 128 * 128;  // 128 rows x 128 bytes (64 bf16)
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 enum { B_QF = 0, B_QE = 1, B_KF = 2, B_KE = 4, B_VF = 6, B_VE = 8, B_SF = 10, B_PF = 12, B_OD = 14, B_OE = 16,
@@ -176,12 +183,12 @@ __device__ __forceinline__ uint64_t exp_store64(const uint32_t (&a)[32], const u
   return f2_add(r, exp_store32(b, sl2x2, nm2, taddr + 16));
 }
 
-template <int HD, bool VL>
+template <int HD, bool VL, bool FIXREF>
 __global__ void __launch_bounds__(kThreads, 1)
     bdlm_fwd_tc_kernel(const __grid_constant__ CUtensorMap tQc, const __grid_constant__ CUtensorMap tQn,
                        const __grid_constant__ CUtensorMap tKc, const __grid_constant__ CUtensorMap tKn,
                        const __grid_constant__ CUtensorMap tVc, const __grid_constant__ CUtensorMap tVn,
-                       const FwdParams p, const VarlenTabs vt) {
+                       const FwdParams p, const VarlenTabs vt, const FwdRef ref) {
   using LY = Layout<HD>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -385,6 +392,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nall_lo = (int)g.q.n_all_lo, nall_hi = (int)imin64(g.q.n_all_hi, seqL);
       const float sl2 = p.scale_log2;
       float m_ref = -INFINITY, l = 0.f;
+      if (FIXREF) {
+        // the caller's reference, natural log -> the kernel's log2 units
+        const float* rp = g.stream ? ref.n : ref.c;
+        const float mr = valid ? rp[(int64_t)g.head * p.g.L + r] * kLog2e : 0.f;
+        m_ref = fabsf(mr) < INFINITY ? mr : 0.f;
+      }
       for (int j = 0; j < n; ++j, ++sc) {
         const bool cs = j < nc;
         const int key0 = (cs ? c0 + clean_step(j, rot, nc) : n0 + (j - nc)) * BN;
@@ -409,7 +422,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mx2 = mx * sl2;
         bool rescale = false;
         float alpha = 1.f, m_use = m_ref;
-        if (m_ref == -INFINITY) {
+        if (FIXREF) {
+          // fixed reference: no rescaling
+        } else if (m_ref == -INFINITY) {
           m_use = mx2;  // first visible keys of this row (O holds zeros so far)
         } else if (mx2 > m_ref + kRescaleThreshold) {
           m_use = mx2;
@@ -506,26 +521,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <int HD, bool VL>
-cudaError_t launch_fwd_t(const FwdMaps& maps, const FwdParams& p, const VarlenTabs& vt, int grid,
+template <int HD, bool VL, bool FIXREF>
+cudaError_t launch_fwd_t(const FwdMaps& maps, const FwdParams& p, const VarlenTabs& vt, const FwdRef& ref, int grid,
                          cudaStream_t stream) {
-  auto k = bdlm_fwd_tc_kernel<HD, VL>;
+  auto k = bdlm_fwd_tc_kernel<HD, VL, FIXREF>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<HD>::kAlloc);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreads, Layout<HD>::kAlloc, stream>>>(maps.Qc, maps.Qn, maps.Kc, maps.Kn, maps.Vc, maps.Vn, p, vt);
+  k<<<grid, kThreads, Layout<HD>::kAlloc, stream>>>(maps.Qc, maps.Qn, maps.Kc, maps.Kn, maps.Vc, maps.Vn, p, vt,
+                                                    ref);
   return cudaSuccess;
 }
 
-cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, const VarlenTabs* vt, int d, int num_sms,
-                       cudaStream_t stream, int* launches) {
+cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, const VarlenTabs* vt, const FwdRef* ref, int d,
+                       int num_sms, cudaStream_t stream, int* launches) {
   const int64_t grid64 = p.n_items < num_sms ? p.n_items : num_sms;
   const int grid = (int)(grid64 > 0 ? grid64 : 1);
   const VarlenTabs none{nullptr, nullptr, nullptr, 0, 0};
   const VarlenTabs& t = vt ? *vt : none;
-  cudaError_t e = d == 128 ? (vt ? launch_fwd_t<128, true>(maps, p, t, grid, stream)
-                                 : launch_fwd_t<128, false>(maps, p, t, grid, stream))
-                           : (vt ? launch_fwd_t<64, true>(maps, p, t, grid, stream)
-                                 : launch_fwd_t<64, false>(maps, p, t, grid, stream));
+  const FwdRef noref{nullptr, nullptr};
+  cudaError_t e;
+  if (ref) {  // verification mode: one sequence only
+    if (vt) return cudaErrorInvalidValue;
+    e = d == 128 ? launch_fwd_t<128, false, true>(maps, p, t, *ref, grid, stream)
+                 : launch_fwd_t<64, false, true>(maps, p, t, *ref, grid, stream);
+  } else {
+    e = d == 128 ? (vt ? launch_fwd_t<128, true, false>(maps, p, t, noref, grid, stream)
+                       : launch_fwd_t<128, false, false>(maps, p, t, noref, grid, stream))
+                 : (vt ? launch_fwd_t<64, true, false>(maps, p, t, noref, grid, stream)
+                       : launch_fwd_t<64, false, false>(maps, p, t, noref, grid, stream));
+  }
   if (e != cudaSuccess) return e;
   if (launches) ++*launches;
   return cudaGetLastError();

@@ -32,6 +32,7 @@ struct Geom {
   int64_t kv_begin, kv_end;  // clean key range of this call
   int include_local;         // corrupted rows also read their own block
   int naive_order = 0;       // 1: items in natural order, round-robin over the grid
+  int round_items = 152;     // CTAs of the persistent grid (the device's SM count): items per block and KV head
 };
 
 BDLM_HD int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
@@ -117,7 +118,8 @@ BDLM_HD bool tile_full(int64_t j0, int tk, int64_t all_lo, int64_t all_hi, int64
 // query tiles (at least kBlockedMinQBlocks blocks) they go in blocks of
 // q_block() tiles, and inside a block the items of one KV head (its query
 // heads, both streams) come together, one KV head after the other: such a
-// block is about one round of a 152-CTA persistent grid, whose key sweeps
+// block is about one round of the persistent grid (g.round_items CTAs, one
+// per SM), whose key sweeps
 // then read one head's K and V, which fit in L2, instead of every head's.
 // Otherwise, inside one query-tile index the two streams of one head are
 // adjacent, then the heads.  (The kernels also start each item's clean-key
@@ -128,14 +130,13 @@ struct QItem {
   int64_t qtile;
 };
 
-constexpr int kRoundItems = 152;        // items per block and KV head, about one grid round
 constexpr int64_t kBlockedMinQBlocks = 6;
 
 BDLM_HD int64_t q_items(const Geom& g, int tq) { return cdiv64(g.L, tq) * g.Hq * 2; }
 
 BDLM_HD int64_t q_block(const Geom& g) {
   const int64_t per_kv = (int64_t)(g.Hq / g.Hkv) * 2;  // items per query tile and KV head
-  const int64_t qb = kRoundItems / per_kv;
+  const int64_t qb = g.round_items / per_kv;
   return qb > 0 ? qb : 1;
 }
 
@@ -183,10 +184,11 @@ BDLM_HD int sweep_rotation(int64_t idx, int nc) {
   return nc > 0 ? (int)((uint32_t)idx % (uint32_t)nc) : 0;
 }
 
-// Below this many key tiles per key stream the dK/dV list stays tile-major:
-// blocks then cover tiles of very different lengths and unbalance the grid
-// (host simulation of the snake assignment: 32 % spread at L = 16k).
-constexpr int64_t kBlockedMinTiles = 6 * kRoundItems;
+// Below this many key tiles per key stream (six grid rounds) the dK/dV list
+// stays tile-major: blocks then cover tiles of very different lengths and
+// unbalance the grid (host simulation of the snake assignment: 32 % spread
+// at L = 16k).
+BDLM_HD int64_t kv_blocked_min_tiles(const Geom& g) { return 6 * (int64_t)g.round_items; }
 
 // The geometry of one sequence of a packed batch: rows [off, off + L) of the
 // packed tensors, all of its clean keys, its own corrupted block included.
@@ -216,11 +218,11 @@ BDLM_HD int64_t sched_item(const Geom& g, int64_t round, int cta, int grid) {
 // dK/dV work items: (key stream, key/value head, key tile).  Clean key tiles
 // first in increasing position (a clean key is read by every later row, so
 // earlier tiles carry more work), then corrupted key tiles (each read only by
-// its own block's rows).  A long range (at least kBlockedMinTiles tiles) goes
-// in blocks of kRoundItems tiles with one KV head after the other inside a
-// block, so the items running together read one head's Q and dO; a short
-// range goes tile by tile with the KV heads inside.  Only tiles that
-// intersect this call's keys count.
+// its own block's rows).  A long range (at least kv_blocked_min_tiles) goes
+// in blocks of g.round_items tiles (one grid round) with one KV head after
+// the other inside a block, so the items running together read one head's Q
+// and dO; a short range goes tile by tile with the KV heads inside.  Only
+// tiles that intersect this call's keys count.
 struct KVItem {
   int key_stream, kv_head;
   int64_t ktile;
@@ -255,18 +257,19 @@ BDLM_HD KVItem kv_item(const Geom& g, int tk, int64_t idx) {
     count = nc;
     it.key_stream = 1;
   }
-  if (count < kBlockedMinTiles || g.naive_order) {
+  if (count < kv_blocked_min_tiles(g) || g.naive_order) {
     // short range: tile-major, KV head minor (rounds of similar lengths)
     it.kv_head = (int)(i % g.Hkv);
     it.ktile = base + i / g.Hkv;
     return it;
   }
-  // long range: blocks of kRoundItems tiles, one KV head after the other
+  // long range: blocks of g.round_items tiles, one KV head after the other
   // inside a block; a block of one head is one grid round, and the snake
   // assignment pairs each round's long items with the next round's short ones
-  const int64_t bi = i / ((int64_t)kRoundItems * g.Hkv);
-  const int64_t t0 = bi * kRoundItems;
-  const int64_t nb = imin64(kRoundItems, count - t0);
+  const int64_t R = g.round_items;
+  const int64_t bi = i / (R * g.Hkv);
+  const int64_t t0 = bi * R;
+  const int64_t nb = imin64(R, count - t0);
   const int64_t r = i - t0 * g.Hkv;
   it.kv_head = (int)(r / nb);
   it.ktile = base + t0 + r % nb;

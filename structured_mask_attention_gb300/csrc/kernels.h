@@ -43,15 +43,25 @@ struct FwdMaps {
   CUtensorMap Qc, Qn, Kc, Kn, Vc, Vn;
 };
 
+// Per-row reference of the fixed-reference verification mode: [Hq, L] fp32,
+// natural-log units, one array per stream.  When given, every row forms its
+// probabilities as exp(scale q.k - M_ref) against this fixed value instead of
+// its running maximum (no rescaling), so two calls that see the same key tile
+// for the same row round the same probabilities to bf16.  Null: production.
+struct FwdRef {
+  const float* c;
+  const float* n;
+};
+
 // Tile sizes of the tensor-core forward: items of 256 query rows (two
 // 128-row sub-tiles sharing their key tiles), 128 keys per step.
 constexpr int kFwdTileQ = 128;
 constexpr int kFwdItemRows = 256;
 constexpr int kFwdTileK = 128;
 
-// vt: null for one sequence.
-cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, const VarlenTabs* vt, int d, int num_sms,
-                       cudaStream_t stream, int* launches);
+// vt: null for one sequence.  ref: null for the production kernel (see FwdRef).
+cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, const VarlenTabs* vt, const FwdRef* ref, int d,
+                       int num_sms, cudaStream_t stream, int* launches);
 
 // ------------------------------------------------------------- backward
 struct BwdParams {
@@ -92,7 +102,7 @@ struct MergeParams {
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, int* launches);
 cudaError_t launch_preprocess(const void* O, int o_f32, const void* dO, int64_t rows, int H, int d, float* D,
-                              cudaStream_t stream, int* launches);
+                              cudaStream_t stream, int* launches, int num_sms);
 cudaError_t launch_watchdog(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 // Packed-batch item table, sequence-major (kind 0: query items, 1: key items).
 cudaError_t launch_varlen_items(const Geom& all, const int64_t* off, const int64_t* order, const int64_t* beg, int n,

@@ -66,35 +66,72 @@ __global__ void __launch_bounds__(256) bdlm_merge_kernel(const MergeParams p) {
 }
 
 // D_i = sum_d dO_i * O_i, [H, rows] fp32 (the row statistic of the
-// softmax-attention backward).  One warp per (head, row).
-template <int HD>
-__global__ void __launch_bounds__(256) bdlm_preprocess_kernel(const void* O, int o_f32, const __nv_bfloat16* dO,
-                                                              int64_t rows, int H, float* D) {
-  const int64_t wid = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+// softmax-attention backward).  O and dO are [rows, H, HD]: one (row, head)
+// pair is HD contiguous elements, and consecutive pairs are contiguous, so
+// the pairs are read as one stream of 16-byte chunks.  A pair's HD / 8 chunks
+// go to HD / 8 consecutive lanes (two pairs per warp at HD = 128, four at 64),
+// each warp takes kUnroll groups of pairs per pass with all their loads
+// issued before the first use, and the lanes of a pair reduce by shuffles.
+template <int HD, bool OF32>
+__global__ void __launch_bounds__(256) bdlm_preprocess_kernel(const void* __restrict__ O,
+                                                              const __nv_bfloat16* __restrict__ dO, int64_t rows,
+                                                              int H, float* __restrict__ D) {
+  constexpr int kCh = HD / 8;            // 16-byte chunks of bf16 per pair
+  constexpr int kPairs = 32 / kCh;       // pairs per warp per group
+  constexpr int kUnroll = 4;             // groups per warp per pass
   const int lane = threadIdx.x & 31;
-  if (wid >= rows * H) return;
-  const int h = (int)(wid / rows);
-  const int64_t r = wid % rows;
-  constexpr int PER = HD / 32;
-  const int64_t off = (r * H + h) * HD + lane * PER;
-  float o[PER], g[PER];
-  if (o_f32) {
-    const float* src = static_cast<const float*>(O) + off;
+  const int64_t npairs = rows * H;
+  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int sub = lane / kCh, ch = lane % kCh;
+  for (int64_t g0 = warp0 * kUnroll; g0 * kPairs < npairs; g0 += nwarps * kUnroll) {
+    uint4 o[kUnroll][OF32 ? 2 : 1], g[kUnroll];
+    int64_t pr[kUnroll];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) o[i] = src[i];
-  } else {
-    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(O) + off;
+    for (int u = 0; u < kUnroll; ++u) {
+      pr[u] = (g0 + u) * kPairs + sub;
+      const bool v = pr[u] < npairs;
+      const int64_t e = (v ? pr[u] : 0) * HD + ch * 8;  // first element of this lane's chunk
+      g[u] = v ? __ldg(reinterpret_cast<const uint4*>(dO + e)) : make_uint4(0u, 0u, 0u, 0u);
+      if (OF32) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const float*>(O) + e);
+        o[u][0] = v ? __ldg(src) : make_uint4(0u, 0u, 0u, 0u);
+        o[u][OF32 ? 1 : 0] = v ? __ldg(src + 1) : make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        o[u][0] = v ? __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(O) + e))
+                    : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
 #pragma unroll
-    for (int i = 0; i < PER; ++i) o[i] = __bfloat162float(src[i]);
+    for (int u = 0; u < kUnroll; ++u) {
+      const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(&g[u]);
+      float acc = 0.f;
+      if (OF32) {
+        const float* of = reinterpret_cast<const float*>(&o[u][0]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 gf = __bfloat1622float2(gp[k]);
+          acc = fmaf(of[2 * k], gf.x, acc);
+          acc = fmaf(of[2 * k + 1], gf.y, acc);
+        }
+      } else {
+        const __nv_bfloat162* op = reinterpret_cast<const __nv_bfloat162*>(&o[u][0]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 of = __bfloat1622float2(op[k]), gf = __bfloat1622float2(gp[k]);
+          acc = fmaf(of.x, gf.x, acc);
+          acc = fmaf(of.y, gf.y, acc);
+        }
+      }
+#pragma unroll
+      for (int k = kCh / 2; k > 0; k >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, k);
+      if (ch == 0 && pr[u] < npairs) {
+        const int64_t r = pr[u] / H;
+        const int h = (int)(pr[u] - r * H);
+        D[(int64_t)h * rows + r] = acc;
+      }
+    }
   }
-#pragma unroll
-  for (int i = 0; i < PER; ++i) g[i] = __bfloat162float(dO[off + i]);
-  float acc = 0.f;
-#pragma unroll
-  for (int i = 0; i < PER; ++i) acc = fmaf(o[i], g[i], acc);
-#pragma unroll
-  for (int k = 16; k > 0; k >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, k);
-  if (lane == 0) D[(int64_t)h * rows + r] = acc;
 }
 
 // Waits on an mbarrier that nobody arrives on, through the same bounded wait
@@ -160,13 +197,24 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, int* launche
 }
 
 cudaError_t launch_preprocess(const void* O, int o_f32, const void* dO, int64_t rows, int H, int d, float* D,
-                              cudaStream_t stream, int* launches) {
-  const int64_t warps = rows * H;
-  if (warps == 0) return cudaSuccess;
-  const unsigned blocks = (unsigned)((warps + 7) / 8);
+                              cudaStream_t stream, int* launches, int num_sms) {
+  const int64_t pairs = rows * H;
+  if (pairs == 0) return cudaSuccess;
+  // 8 warps per block, each taking 4 groups of 32 / (d / 8) pairs per pass;
+  // at most 8 resident blocks per SM, grid-stride beyond that
+  const int64_t per_block = 8 * 4 * (32 / (d / 8));
+  int64_t blocks = (pairs + per_block - 1) / per_block;
+  const int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 152) * 8;
+  if (blocks > cap) blocks = cap;
   const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(dO);
-  if (d == 128) bdlm_preprocess_kernel<128><<<blocks, 256, 0, stream>>>(O, o_f32, g, rows, H, D);
-  else bdlm_preprocess_kernel<64><<<blocks, 256, 0, stream>>>(O, o_f32, g, rows, H, D);
+  const unsigned nb = (unsigned)blocks;
+  if (d == 128) {
+    if (o_f32) bdlm_preprocess_kernel<128, true><<<nb, 256, 0, stream>>>(O, g, rows, H, D);
+    else bdlm_preprocess_kernel<128, false><<<nb, 256, 0, stream>>>(O, g, rows, H, D);
+  } else {
+    if (o_f32) bdlm_preprocess_kernel<64, true><<<nb, 256, 0, stream>>>(O, g, rows, H, D);
+    else bdlm_preprocess_kernel<64, false><<<nb, 256, 0, stream>>>(O, g, rows, H, D);
+  }
   if (launches) ++*launches;
   return cudaGetLastError();
 }

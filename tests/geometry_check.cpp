@@ -143,6 +143,44 @@ static void check_ranges(const Geom& g, int t) {
     }
 }
 
+// Per-CTA totals of the persistent assignment over a work list, with the
+// list's own costs (visible key tiles of a query item; query rows reading a
+// key tile): the boustrophedon order over a longest-first (or blocked) list
+// keeps every CTA within `slack` items' worth of the mean.
+static void check_balance(const Geom& g, int grid, bool kv, double max_over_mean) {
+  const int tq = 256, tk = 128;
+  const int64_t n = kv ? kv_items(g, tk) : q_items(g, tq);
+  std::vector<double> tot((size_t)grid, 0.0);
+  double cmax = 0.0, sum = 0.0;
+  for (int64_t r = 0; r * grid < n; ++r)
+    for (int c = 0; c < grid; ++c) {
+      const int64_t idx = sched_item(g, r, c, grid);
+      if (idx >= n) continue;
+      double cost;
+      if (kv) {
+        const KVItem it = kv_item(g, tk, idx);
+        int64_t cl, ch, nl, nh;
+        kv_tile_rows(g, it.key_stream, it.ktile * tk, imin64(it.ktile * tk + tk, g.L), cl, ch, nl, nh);
+        cost = (double)(imax64(0, ch - cl) + imax64(0, nh - nl));
+      } else {
+        const QItem it = q_item(g, tq, idx);
+        const int64_t r0 = it.qtile * tq;
+        const QTileRanges q = qtile_ranges(g, it.stream, r0, imin64(r0 + tq, g.L), tk);
+        cost = (double)((q.c1 - q.c0) + (q.n1 - q.n0));
+      }
+      tot[(size_t)c] += cost;
+      cmax = cost > cmax ? cost : cmax;
+      sum += cost;
+    }
+  double mx = 0.0, mn = 1e300;
+  for (double t : tot) { mx = t > mx ? t : mx; mn = t < mn ? t : mn; }
+  const double mean = sum / grid;
+  CHECK(mx <= mean * max_over_mean, "balance %s grid=%d L=%lld: max %.0f mean %.0f (ratio %.4f)", kv ? "kv" : "q",
+        grid, (long long)g.L, mx, mean, mx / mean);
+  CHECK(mx - mn <= 2 * cmax, "spread %s grid=%d L=%lld: max %.0f min %.0f item %.0f", kv ? "kv" : "q", grid,
+        (long long)g.L, mx, mn, cmax);
+}
+
 int main() {
   const int64_t Ls[] = {96, 256, 1024, 8192, 16384, 32768, 131072, 262144};
   const int64_t Bs[] = {32, 128, 512};
@@ -179,6 +217,28 @@ int main() {
         g.naive_order = naive;
         check_sched(g, 152, 7);
         check_sched(g, 37, 5);
+      }
+  // the work-order blocking follows the grid: one round of the persistent
+  // grid per block, for devices of 132, 148 and 152 SMs
+  for (int grid : {132, 148, 152})
+    for (int64_t L : {16384, 32768, 131072, 262144})
+      for (const auto& h : heads) {
+        const int64_t B = 512;
+        Geom g{L, B, h[0], h[1], 0, L, 1};
+        g.round_items = grid;
+        for (int tq : {128, 256}) check_q(g, tq);
+        check_kv(g, 128);
+        Geom gs = g;
+        gs.kv_begin = L / 8;
+        gs.kv_end = L / 4;
+        gs.include_local = 0;
+        check_kv(gs, 128);
+        check_q(gs, 128);
+        check_sched(g, grid, 9);
+        if (L >= 131072) {
+          check_balance(g, grid, false, 1.02);
+          check_balance(g, grid, true, 1.05);
+        }
       }
   // tile ranges against the mask on small shapes: tiles smaller than,
   // equal to and larger than the blocks, ragged tails, shards, no local block

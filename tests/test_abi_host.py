@@ -206,3 +206,18 @@ def test_packed_lengths_mix():
         assert lens == workload_lengths(name)
     assert workload_lengths("batch-64x2k") == [2048] * 64
     assert packed_lengths(4096, 128, 256, 1024, seed=1) != packed_lengths(4096, 128, 256, 1024, seed=2)
+
+
+def test_noalloc_size_limit_edge_on_host(lib):
+    """The allocation-free backward's array holds 256 + 8 * Hq * L bytes for
+    Hq * L up to 4194272: at exactly the limit the size check passes and the
+    null pointers are what is rejected (BDLM_ERR_INVALID_ARG); one block more
+    is rejected by the size check (BDLM_ERR_WORKSPACE).  Both are decided on
+    the host before any device call."""
+    f = lib.bdlm_attn_bwd_noalloc
+    st = f(*([None] * 12), 4194272, 32, 1, 1, 128, 0.088, *([None] * 6), 0, None)
+    assert st == 1, (st, m.bdlm_last_error())
+    assert "null pointer" in m.bdlm_last_error()
+    st = f(*([None] * 12), 4194304, 32, 1, 1, 128, 0.088, *([None] * 6), 0, None)
+    assert st == 4, (st, m.bdlm_last_error())
+    assert "4194272" in m.bdlm_last_error()

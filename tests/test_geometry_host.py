@@ -2,7 +2,9 @@
 kernels' own geometry header (tile ranges, item orders, grid assignment)
 with g++ and checks that every enumeration visits each item exactly once,
 for blocked and unblocked lists, sharded key ranges, one sequence of a packed
-batch and the natural-order ablation."""
+batch and the natural-order ablation; and, for persistent grids of 132, 148
+and 152 CTAs (the blocking follows the grid), that the assignment keeps the
+per-CTA work within 2 % (query items) and 5 % (key items) of the mean."""
 from __future__ import annotations
 
 import os
