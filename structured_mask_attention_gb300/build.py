@@ -6,10 +6,13 @@ library is plain C ABI (include/bdlm_attn.h).
 """
 from __future__ import annotations
 
+import json
 import os
+import platform
 import shutil
 import subprocess
 import sys
+import time
 from concurrent.futures import ThreadPoolExecutor
 
 PKG = os.path.dirname(os.path.abspath(__file__))
@@ -49,20 +52,21 @@ def build(verbose: bool = False, ptxas_verbose: bool = False, force: bool = Fals
         o = os.path.join(OBJ, src + ".o")
         if (not force and not ptxas_verbose and os.path.exists(o)
                 and os.path.getmtime(o) >= max(os.path.getmtime(s), newest_header)):
-            return o, ""
+            return o, "", False
         cmd = [cc] + _flags(ptxas_verbose) + ["-c", s, "-o", o]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
-        return o, r.stderr
+        return o, r.stderr, True
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         results = list(ex.map(compile_one, SOURCES))
     if verbose or ptxas_verbose:
-        for (o, log) in results:
+        for (o, log, _) in results:
             if log:
                 sys.stderr.write(log)
-    objs = [o for (o, _) in results]
+    objs = [o for (o, _, _) in results]
+    linked = False
     if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
         tmp = LIB + ".tmp"
         cmd = [cc] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcudart_static", "-ldl", "-lpthread", "-lrt"]
@@ -70,6 +74,18 @@ def build(verbose: bool = False, ptxas_verbose: bool = False, force: bool = Fals
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, LIB)
+        linked = True
+    # what this call did, for the record: which objects were compiled here
+    # and which were reused (up to date with their sources and headers)
+    record = {"compiled": [os.path.basename(o) for (o, _, c) in results if c],
+              "reused": [os.path.basename(o) for (o, _, c) in results if not c],
+              "linked": linked, "nvcc": cc, "arch": ARCH[1], "machine": platform.machine(),
+              "time": time.strftime("%Y-%m-%dT%H:%M:%S")}
+    with open(os.path.join(OBJ, "build_record.json"), "w") as fh:
+        json.dump(record, fh, indent=1)
+    print(f"bdlm build: compiled {len(record['compiled'])}, reused {len(record['reused'])} of {len(SOURCES)} "
+          f"sources; {'linked' if linked else 'library up to date'} ({record['machine']}, {ARCH[1]})",
+          file=sys.stderr)
     return LIB
 
 
