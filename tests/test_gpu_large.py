@@ -56,7 +56,10 @@ def _invariants(X, grads, G):
     bf16 rounding of P and dS, random across ~sqrt(n) keys, and the tensor
     cores' fp32 accumulation over ~10^4 MMA steps per gradient element, which
     truncates and shrinks each element by up to ~1e-3 relative (measured
-    shrinkage of the dV sums: 2e-4 to 7e-4 at L = 32768)."""
+    shrinkage of the dV sums: 2e-4 to 7e-4 at L = 32768).  The longest
+    accumulations are also compared with the oracle directly (every key of a
+    KV group at L = 32768; clean blocks 0 and N/2, read by the most rows, at
+    L = 131072), at the parity tolerance."""
     dQc, dKc, dVc, dQn, dKn, dVn = [g.double() for g in grads]
     Hkv = dKc.shape[1]
     n = 2 * dKc.shape[0]
