@@ -235,6 +235,47 @@ bdlm_status bdlm_attn_bwd_shard(const void* Qc, const void* Kc, const void* Vc,
                                 float* dKc, float* dVc, float* dKn, float* dVn,
                                 void* workspace, size_t ws_bytes, bdlm_stream stream);
 
+/* ---- One rank's rows (multi-rank CSBP) -----------------------------------
+ * A rank of a context-sharded deployment (evolve.pub FAQ on CSBP: ranks own
+ * complete corrupted blocks and a shard of the clean context; only clean K/V
+ * and their gradients cross ranks) computes its own query rows only.  These
+ * two calls are bdlm_attn_fwd_shard and bdlm_attn_bwd_shard restricted to
+ * the clean rows [rows_c_begin, rows_c_end) and the corrupted rows
+ * [rows_n_begin, rows_n_end) (0 <= begin <= end <= L; any boundaries, most
+ * naturally whole blocks).  Other rows are neither computed into the
+ * results nor written.
+ *  - bdlm_attn_fwd_shard_rows writes Op/LSEp of those rows only (rows with no
+ *    visible key: O = 0, LSE = -inf), against clean keys [kv_begin, kv_end)
+ *    and, with include_local, the rows' own corrupted blocks.
+ *  - bdlm_attn_bwd_shard_rows ADDS the contributions of those rows: dQ of
+ *    the rows into dQc_acc / dQn_acc, and dK, dV of the call's keys (clean
+ *    [kv_begin, kv_end), plus every corrupted key with include_local) into
+ *    dKc_acc, dVc_acc, dKn_acc, dVn_acc (all fp32, zeroed by the caller
+ *    before the first call).  LSE and D are the merged, full-row statistics.
+ *    Contributions of disjoint row sets to the same keys add up to the
+ *    gradient of all rows; on one stream in a fixed order the sums are
+ *    deterministic. */
+bdlm_status bdlm_attn_fwd_shard_rows(const void* Qc, const void* Kc, const void* Vc,
+                                     const void* Qn, const void* Kn, const void* Vn,
+                                     int64_t L, int64_t B, int Hq, int Hkv, int d, float scale,
+                                     int64_t kv_begin, int64_t kv_end, int include_local,
+                                     int64_t rows_c_begin, int64_t rows_c_end,
+                                     int64_t rows_n_begin, int64_t rows_n_end,
+                                     float* Op_c, float* Op_n, float* LSEp_c, float* LSEp_n,
+                                     void* workspace, size_t ws_bytes, bdlm_stream stream);
+
+bdlm_status bdlm_attn_bwd_shard_rows(const void* Qc, const void* Kc, const void* Vc,
+                                     const void* Qn, const void* Kn, const void* Vn,
+                                     const void* dOc, const void* dOn,
+                                     const float* LSEc, const float* LSEn, const float* Dc, const float* Dn,
+                                     int64_t L, int64_t B, int Hq, int Hkv, int d, float scale,
+                                     int64_t kv_begin, int64_t kv_end, int include_local,
+                                     int64_t rows_c_begin, int64_t rows_c_end,
+                                     int64_t rows_n_begin, int64_t rows_n_end,
+                                     float* dQc_acc, float* dQn_acc,
+                                     float* dKc_acc, float* dVc_acc, float* dKn_acc, float* dVn_acc,
+                                     void* workspace, size_t ws_bytes, bdlm_stream stream);
+
 /* ---- Packed variable-length batch (batch > 1) ---------------------------
  * Several independent two-stream problems in one call, for batches of
  * sequences (the pages tune the batch size alongside the parallelism:

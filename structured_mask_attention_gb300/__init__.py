@@ -18,7 +18,7 @@ import re
 
 __all__ = [
     "BdlmError", "load_library", "bdlm_workspace_size", "bdlm_attn_fwd", "bdlm_attn_fwd_shard",
-    "bdlm_attn_fwd_shard_refmax",
+    "bdlm_attn_fwd_shard_refmax", "bdlm_attn_fwd_shard_rows", "bdlm_attn_bwd_shard_rows",
     "bdlm_lse_merge", "bdlm_bwd_preprocess", "bdlm_attn_bwd", "bdlm_attn_bwd_noalloc", "bdlm_attn_bwd_shard",
     "bdlm_worklist", "bdlm_workspace_size_varlen", "bdlm_attn_fwd_varlen", "bdlm_attn_bwd_varlen",
     "bdlm_sync_status", "bdlm_watchdog_selftest", "bdlm_sync_status_noalloc", "bdlm_watchdog_selftest_noalloc",
@@ -64,6 +64,10 @@ _SIGS = {
     "bdlm_attn_bwd_shard": (_I, [_P] * 12 + [_I64, _I64, _I, _I, _I, _F, _I64, _I64, _I] + [_P] * 6
                             + [_P, _SZ, _P]),
     "bdlm_attn_bwd_noalloc": (_I, [_P] * 12 + [_I64, _I64, _I, _I, _I, _F] + [_P] * 6 + [_I, _P]),
+    "bdlm_attn_fwd_shard_rows": (_I, [_P] * 6 + [_I64, _I64, _I, _I, _I, _F, _I64, _I64, _I] + [_I64] * 4
+                                 + [_P] * 5 + [_SZ, _P]),
+    "bdlm_attn_bwd_shard_rows": (_I, [_P] * 12 + [_I64, _I64, _I, _I, _I, _F, _I64, _I64, _I] + [_I64] * 4
+                                 + [_P] * 7 + [_SZ, _P]),
     "bdlm_worklist": (_I64, [_I64, _I64, _I, _I, _I, _I, _I64, _I64, _I, _P, _I64]),
     "bdlm_workspace_size_varlen": (_SZ, [_I, _P, _I, _I, _I, _I]),
     "bdlm_attn_fwd_varlen": (_I, [_P] * 6 + [_P, _I, _I64, _I, _I, _I, _F, _P, _P, _I, _P, _P, _P, _SZ, _P]),
@@ -346,6 +350,47 @@ def bdlm_attn_bwd_shard(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn, B:
         _ptr(Dc), _ptr(Dn), L, B, Hq, Hkv, d, scale, kv_begin, kv_end, int(bool(include_local)),
         _ptr(dQc_acc), _ptr(dQn_acc), _ptr(dKc), _ptr(dVc), _ptr(dKn), _ptr(dVn), _ptr(ws), ws.numel(),
         _stream(stream)))
+
+
+def bdlm_attn_fwd_shard_rows(Qc, Kc, Vc, Qn, Kn, Vn, B: int, kv_begin: int, kv_end: int, include_local: bool,
+                             rows_c, rows_n, scale: float | None = None, out=None, workspace=None, stream=None):
+    """One rank's rows of the partial forward: clean rows ``rows_c`` =
+    (begin, end) and corrupted rows ``rows_n``, against clean keys
+    [kv_begin, kv_end) (+ the rows' own corrupted blocks if include_local).
+    Only those rows of the fp32 outputs are written.  Returns
+    (Op_c, Op_n, LSEp_c, LSEp_n)."""
+    torch = _torch()
+    _check_inputs(Qc, Kc, Vc, Qn, Kn, Vn)
+    L, Hq, Hkv, d = _shape(Qc, Kc)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    if out is None:
+        out = (torch.zeros((L, Hq, d), dtype=torch.float32, device=Qc.device),
+               torch.zeros((L, Hq, d), dtype=torch.float32, device=Qc.device),
+               torch.full((Hq, L), float("-inf"), dtype=torch.float32, device=Qc.device),
+               torch.full((Hq, L), float("-inf"), dtype=torch.float32, device=Qc.device))
+    ws = _workspace(OP_FWD_SHARD, L, B, Hq, Hkv, d, Qc.device, workspace)
+    _check(load_library().bdlm_attn_fwd_shard_rows(
+        _ptr(Qc), _ptr(Kc), _ptr(Vc), _ptr(Qn), _ptr(Kn), _ptr(Vn), L, B, Hq, Hkv, d, scale,
+        kv_begin, kv_end, int(bool(include_local)), int(rows_c[0]), int(rows_c[1]), int(rows_n[0]), int(rows_n[1]),
+        *[_ptr(t) for t in out], _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def bdlm_attn_bwd_shard_rows(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn, B: int, kv_begin: int,
+                             kv_end: int, include_local: bool, rows_c, rows_n, dQc_acc, dQn_acc, dKc_acc, dVc_acc,
+                             dKn_acc, dVn_acc, scale: float | None = None, workspace=None, stream=None):
+    """One rank's rows of the sharded backward: adds the rows' dQ and their
+    contributions to the call's keys' dK, dV into the fp32 accumulators."""
+    _check_inputs(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn)
+    L, Hq, Hkv, d = _shape(Qc, Kc)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    ws = _workspace(OP_BWD_SHARD, L, B, Hq, Hkv, d, Qc.device, workspace)
+    _check(load_library().bdlm_attn_bwd_shard_rows(
+        _ptr(Qc), _ptr(Kc), _ptr(Vc), _ptr(Qn), _ptr(Kn), _ptr(Vn), _ptr(dOc), _ptr(dOn), _ptr(LSEc), _ptr(LSEn),
+        _ptr(Dc), _ptr(Dn), L, B, Hq, Hkv, d, scale, kv_begin, kv_end, int(bool(include_local)),
+        int(rows_c[0]), int(rows_c[1]), int(rows_n[0]), int(rows_n[1]),
+        _ptr(dQc_acc), _ptr(dQn_acc), _ptr(dKc_acc), _ptr(dVc_acc), _ptr(dKn_acc), _ptr(dVn_acc),
+        _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def bdlm_worklist(L: int, B: int, Hq: int, Hkv: int, tile_q: int = 256, tile_k: int = 128,

@@ -10,11 +10,13 @@ App. I / Table 5 per the review's Strengths):
   blocks; rank r owns clean shard r: its clean query rows and its clean keys
   and values.
 * Every corrupted block is owned whole by one rank (block parallelism): its
-  queries, keys, values and their gradients never leave that rank.  Blocks
-  are dealt to ranks longest first onto the least-loaded rank, counting each
-  rank's clean rows as load it already carries (the work of a block of
-  either stream grows with its index: block j has B rows that each read
-  (j + 1) B keys).
+  queries, keys, values and their gradients never leave that rank.  The
+  work of a block of either stream grows with its index (block j has B rows
+  that each read (j + 1) B keys), so rank r, whose clean shard is the r-th
+  slice of blocks, takes the mirror slice of corrupted blocks, the
+  (R - 1 - r)-th: every rank then carries the same work,
+  B^2 ((R - 1) n^2 + n (n + 1)) for n = L / (B R) blocks per slice (the
+  load balancing of App. I), and both of its row sets are contiguous.
 * Forward on rank r: for every clean shard s in order 0..R-1 a partial
   (O_s, LSE_s) of the rank's rows against shard s's keys, then the local
   partial (corrupted rows against their own block), merged exactly by
@@ -48,11 +50,15 @@ object passed in by the caller:
   ``sum_to_owner(x, owner) -> x or None`` (the sum over ranks, on the owner).
 
 On GB300s the compute object is the library's tensor-core kernels
-restricted to a rank's rows and the transport is NCCL over NVLink (no TMA
-multicast, and no kernel reads a peer's memory: shards are copied into local
-HBM first).  That GPU path is not built (the kernels take whole sequences),
-so the plan and the driver are exercised on the CPU with gloo ranks and the
-fp64 oracle as the compute object (tests/test_csbp_ranks.py), and are
+restricted to a rank's rows (`bdlm_attn_fwd_shard_rows`,
+`bdlm_attn_bwd_shard_rows`: row ranges per stream, gradients accumulated
+over calls) and the transport is NCCL over NVLink (no TMA multicast, and no
+kernel reads a peer's memory: shards are copied into local HBM first).  The
+row-restricted kernels are checked on one GPU with every rank's calls made
+in turn (tests/test_gpu_csbp_rows.py); the plan and this driver are checked
+with gloo ranks on the CPU and the fp64 oracle as the compute object
+(tests/test_csbp_ranks.py).  The kernels index full-length tensors, so a
+rank would hold its rows in full-length buffers; the multi-GPU path is
 unmeasured on hardware.
 """
 from __future__ import annotations
@@ -62,11 +68,16 @@ from dataclasses import dataclass, field
 
 @dataclass(frozen=True)
 class Rows:
-    """The query rows a rank owns: clean rows of blocks [c0, c1) and the
-    corrupted rows of the listed blocks."""
+    """The query rows a rank owns: clean rows of blocks [c0, c1) and
+    corrupted rows of blocks [n0, n1)."""
     c0: int
     c1: int
-    noisy_blocks: tuple
+    n0: int
+    n1: int
+
+    @property
+    def noisy_blocks(self):
+        return tuple(range(self.n0, self.n1))
 
 
 @dataclass
@@ -89,19 +100,19 @@ class CSBPPlan:
         per = N // R
         plan = CSBPPlan(L, B, R)
         plan.clean_shards = [(r * per, (r + 1) * per) for r in range(R)]
+        # corrupted blocks: the mirror slice of the rank's clean shard
+        plan.noisy_owner = [R - 1 - j // per for j in range(N)]
         # work of block j of either stream: B rows reading (j + 1) B keys
         cost = [B * (j + 1) * B for j in range(N)]
         plan.load = [sum(cost[j] for j in range(a, b)) for (a, b) in plan.clean_shards]
-        plan.noisy_owner = [0] * N
-        for j in sorted(range(N), key=lambda j: (-cost[j], j)):  # longest first
-            r = min(range(R), key=lambda r: (plan.load[r], r))    # onto the least-loaded rank
-            plan.noisy_owner[j] = r
+        for j, r in enumerate(plan.noisy_owner):
             plan.load[r] += cost[j]
         return plan
 
     def rows(self, r: int) -> Rows:
         c0, c1 = self.clean_shards[r]
-        return Rows(c0, c1, tuple(j for j, o in enumerate(self.noisy_owner) if o == r))
+        n0, n1 = self.clean_shards[self.R - 1 - r]
+        return Rows(c0, c1, n0, n1)
 
     def shard_keys(self, s: int):
         """Clean key range (token indices) of shard s."""

@@ -240,11 +240,30 @@ bdlm_status finish(cudaError_t e, int launches, const char* what) {
   return BDLM_OK;
 }
 
+// Query-row ranges of a call: rows[0..1] the clean rows, rows[2..3] the
+// corrupted rows, [begin, end) each (validated by the caller).
+RowRange row_range(const int64_t* rows) {
+  RowRange r;
+  r.lo[0] = (int32_t)rows[0];
+  r.hi[0] = (int32_t)rows[1];
+  r.lo[1] = (int32_t)rows[2];
+  r.hi[1] = (int32_t)rows[3];
+  return r;
+}
+
+bdlm_status check_rows(const int64_t* rows, int64_t L) {
+  for (int s = 0; s < 2; ++s)
+    if (rows[2 * s] < 0 || rows[2 * s + 1] < rows[2 * s] || rows[2 * s + 1] > L)
+      return fail(BDLM_ERR_SHAPE, "%s row range [%lld, %lld) is not inside [0, %lld)", s ? "corrupted" : "clean",
+                  (long long)rows[2 * s], (long long)rows[2 * s + 1], (long long)L);
+  return BDLM_OK;
+}
+
 bdlm_status fwd_common(const void* Qc, const void* Kc, const void* Vc, const void* Qn, const void* Kn,
                        const void* Vn, int64_t L, int64_t B, int Hq, int Hkv, int d, float scale, int64_t kv_begin,
                        int64_t kv_end, int include_local, void* Oc, void* On, int o_f32, float* LSEc, float* LSEn,
                        void* ws, size_t ws_bytes, cudaStream_t st, const VarlenTabs* vt = nullptr,
-                       const FwdRef* ref = nullptr) {
+                       const FwdRef* ref = nullptr, const int64_t* rows = nullptr) {
   DeviceInfo info;
   BDLM_CHECK(device_info(info));
   EncodeTiledFn enc;
@@ -272,7 +291,8 @@ bdlm_status fwd_common(const void* Qc, const void* Kc, const void* Vc, const voi
   BDLM_CHECK(clear_status(ws, st));
   int launches = 0;
   ScopedKernelTimer tm(K_FWD, st);
-  cudaError_t e = launch_fwd(maps, p, vt, ref, d, info.sms, st, &launches);
+  const RowRange rr = rows ? row_range(rows) : RowRange();
+  cudaError_t e = launch_fwd(maps, p, vt, ref, rows ? &rr : nullptr, d, info.sms, st, &launches);
   tm.stop();
   return finish(e, launches, "forward launch");
 }
@@ -294,6 +314,7 @@ BwdParams bwd_params(const void* Qc, const void* Kc, const void* Vc, const void*
   p.dQc = p.dQn = p.dKc = p.dVc = p.dKn = p.dVn = nullptr;
   p.g_f32 = 0;
   p.dq_accumulate = 0;
+  p.dkv_accumulate = 0;
   return p;
 }
 
@@ -600,6 +621,29 @@ bdlm_status bdlm_attn_fwd_shard_refmax(const void* Qc, const void* Kc, const voi
   });
 }
 
+bdlm_status bdlm_attn_fwd_shard_rows(const void* Qc, const void* Kc, const void* Vc, const void* Qn,
+                                     const void* Kn, const void* Vn, int64_t L, int64_t B, int Hq, int Hkv, int d,
+                                     float scale, int64_t kv_begin, int64_t kv_end, int include_local,
+                                     int64_t rows_c_begin, int64_t rows_c_end, int64_t rows_n_begin,
+                                     int64_t rows_n_end, float* Op_c, float* Op_n, float* LSEp_c, float* LSEp_n,
+                                     void* workspace, size_t ws_bytes, bdlm_stream stream) {
+  return guarded([&]() -> bdlm_status {
+    BDLM_CHECK(check_shape(L, B, Hq, Hkv, d));
+    BDLM_CHECK(check_scale(scale));
+    if (kv_begin < 0 || kv_end < kv_begin || kv_end > L)
+      return fail(BDLM_ERR_SHAPE, "clean key range [%lld, %lld) is not inside [0, %lld)", (long long)kv_begin,
+                  (long long)kv_end, (long long)L);
+    const int64_t rows[4] = {rows_c_begin, rows_c_end, rows_n_begin, rows_n_end};
+    BDLM_CHECK(check_rows(rows, L));
+    BDLM_CHECK(check_ptrs("bdlm_attn_fwd_shard_rows(Qc,Kc,Vc,Qn,Kn,Vn,Op_c,Op_n,LSEp_c,LSEp_n)",
+                          {Qc, Kc, Vc, Qn, Kn, Vn, Op_c, Op_n, LSEp_c, LSEp_n}));
+    BDLM_CHECK(check_ws(workspace, ws_bytes, bdlm_workspace_size(BDLM_OP_FWD_SHARD, L, B, Hq, Hkv, d, 1)));
+    return fwd_common(Qc, Kc, Vc, Qn, Kn, Vn, L, B, Hq, Hkv, d, scale, kv_begin, kv_end, include_local, Op_c, Op_n,
+                      1, LSEp_c, LSEp_n, workspace, ws_bytes, static_cast<cudaStream_t>(stream), nullptr, nullptr,
+                      rows);
+  });
+}
+
 bdlm_status bdlm_lse_merge(int n_parts, const float* const* O_parts, const float* const* LSE_parts, int64_t rows,
                            int H, int d, void* O, bdlm_dtype o_dtype, float* LSE, bdlm_stream stream) {
   return guarded([&]() -> bdlm_status {
@@ -724,6 +768,46 @@ bdlm_status bdlm_attn_bwd_shard(const void* Qc, const void* Kc, const void* Vc, 
     cudaError_t e = launch_backward_passes(p, info, workspace, st, &launches, &vs);
     if (vs != BDLM_OK) return vs;
     return finish(e, launches, "sharded backward launch");
+  });
+}
+
+bdlm_status bdlm_attn_bwd_shard_rows(const void* Qc, const void* Kc, const void* Vc, const void* Qn,
+                                     const void* Kn, const void* Vn, const void* dOc, const void* dOn,
+                                     const float* LSEc, const float* LSEn, const float* Dc, const float* Dn, int64_t L,
+                                     int64_t B, int Hq, int Hkv, int d, float scale, int64_t kv_begin,
+                                     int64_t kv_end, int include_local, int64_t rows_c_begin, int64_t rows_c_end,
+                                     int64_t rows_n_begin, int64_t rows_n_end, float* dQc_acc, float* dQn_acc,
+                                     float* dKc_acc, float* dVc_acc, float* dKn_acc, float* dVn_acc, void* workspace,
+                                     size_t ws_bytes, bdlm_stream stream) {
+  return guarded([&]() -> bdlm_status {
+    BDLM_CHECK(check_shape(L, B, Hq, Hkv, d));
+    BDLM_CHECK(check_scale(scale));
+    if (kv_begin < 0 || kv_end < kv_begin || kv_end > L)
+      return fail(BDLM_ERR_SHAPE, "clean key range [%lld, %lld) is not inside [0, %lld)", (long long)kv_begin,
+                  (long long)kv_end, (long long)L);
+    const int64_t rows[4] = {rows_c_begin, rows_c_end, rows_n_begin, rows_n_end};
+    BDLM_CHECK(check_rows(rows, L));
+    BDLM_CHECK(check_ptrs("bdlm_attn_bwd_shard_rows(Qc,Kc,Vc,Qn,Kn,Vn,dOc,dOn,LSEc,LSEn,Dc,Dn)",
+                          {Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn}));
+    BDLM_CHECK(check_ptrs("bdlm_attn_bwd_shard_rows(dQc_acc,dQn_acc,dKc_acc,dVc_acc,dKn_acc,dVn_acc)",
+                          {dQc_acc, dQn_acc, dKc_acc, dVc_acc, dKn_acc, dVn_acc}));
+    BDLM_CHECK(check_ws(workspace, ws_bytes, bdlm_workspace_size(BDLM_OP_BWD_SHARD, L, B, Hq, Hkv, d, 1)));
+    DeviceInfo info;
+    BDLM_CHECK(device_info(info));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    BDLM_CHECK(clear_status(workspace, st));
+    BwdParams p = bwd_params(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn, L, B, Hq, Hkv, d, scale, kv_begin,
+                             kv_end, include_local, info.sms);
+    p.rows = row_range(rows);
+    p.dQc = dQc_acc; p.dQn = dQn_acc; p.dKc = dKc_acc; p.dVc = dVc_acc; p.dKn = dKn_acc; p.dVn = dVn_acc;
+    p.g_f32 = 1;
+    p.dq_accumulate = 1;
+    p.dkv_accumulate = 1;
+    int launches = 0;
+    bdlm_status vs = BDLM_OK;
+    cudaError_t e = launch_backward_passes(p, info, workspace, st, &launches, &vs);
+    if (vs != BDLM_OK) return vs;
+    return finish(e, launches, "row-restricted backward launch");
   });
 }
 

@@ -57,8 +57,9 @@ struct DkvGeo {
   int64_t off, L;                  // first row of the item's sequence in the packed tensors, its length
 };
 
-// VL: packed variable-length batch (a separate instantiation).
-template <bool VL>
+// VL: packed variable-length batch; ROWS: the call computes a row range
+// (separate instantiations).
+template <bool VL, bool ROWS>
 __device__ __forceinline__ DkvGeo dkv_geo(const BwdParams& p, const VarlenTabs& vt, int64_t idx) {
   DkvGeo t;
   Geom g = p.g;
@@ -79,6 +80,7 @@ __device__ __forceinline__ DkvGeo dkv_geo(const BwdParams& p, const VarlenTabs& 
   t.L = g.L;
   const int64_t j1 = imin64(t.j0 + KBM, g.L);
   kv_tile_rows(g, t.ks, t.j0, j1, t.rlo0, t.rhi0, t.rlo1, t.rhi1);
+  if (ROWS) clamp_rows(p.rows, t.rlo0, t.rhi0, t.rlo1, t.rhi1);  // only the call's rows
   if (t.rhi0 > t.rlo0) {
     t.t00 = t.rlo0 / KBN;
     t.nt0 = (int)(cdiv64(t.rhi0, KBN) - t.t00);
@@ -114,8 +116,11 @@ struct DkvCursor {
 };
 
 // Query-row interval [lo, hi) of stream s that sees key j of key stream ks
-// (empty if the key is not in this call's key set or j >= L).
-__device__ __forceinline__ void key_rows(const Geom& g, int ks, int64_t j, int s, int64_t& lo, int64_t& hi) {
+// (empty if the key is not in this call's key set or j >= L), within the
+// call's row range when ROWS.
+template <bool ROWS>
+__device__ __forceinline__ void key_rows(const Geom& g, const RowRange& rows, int ks, int64_t j, int s, int64_t& lo,
+                                         int64_t& hi) {
   lo = 0;
   hi = 0;
   if (j >= g.L) return;
@@ -128,6 +133,11 @@ __device__ __forceinline__ void key_rows(const Geom& g, int ks, int64_t j, int s
     if (!g.include_local || s == 0) return;
     lo = b * g.B;
     hi = (b + 1) * g.B;
+  }
+  if (ROWS) {  // only this call's rows
+    lo = imax64(lo, range_lo(rows, s));
+    hi = imin64(hi, range_hi(rows, s));
+    if (hi <= lo) lo = hi = 0;
   }
 }
 
@@ -162,7 +172,7 @@ __device__ __forceinline__ void p_cols32(const uint32_t (&us)[32], const float* 
   }
 }
 
-template <int HD, bool VL>
+template <int HD, bool VL, bool ROWS>
 __global__ void __launch_bounds__(kThreads, 1)
     bdlm_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tQc, const __grid_constant__ CUtensorMap tQn,
                            const __grid_constant__ CUtensorMap tdOc, const __grid_constant__ CUtensorMap tdOn,
@@ -219,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t rnd = 0; ok; ++rnd) {
       const int64_t idx = sched_item(p.g, rnd, cta, grid);
       if (idx >= n_items) break;
-      const DkvGeo t = dkv_geo<VL>(p, vt, idx);
+      const DkvGeo t = dkv_geo<VL, ROWS>(p, vt, idx);
       if (t.n == 0) continue;
       if (itn > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(BAR(KV_KE), (itn - 1) & 1, wd, 41));
@@ -285,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t rnd = 0; ok; ++rnd) {
         const int64_t idx = sched_item(p.g, rnd, cta, grid);
         if (idx >= n_items) break;
-        const DkvGeo t = dkv_geo<VL>(p, vt, idx);
+        const DkvGeo t = dkv_geo<VL, ROWS>(p, vt, idx);
         if (t.n == 0) continue;
         if (!mbar_wait(BAR(KV_KF), itn & 1, wd, 43)) { ok = false; break; }
         const uint32_t q_base = qc;
@@ -352,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t rnd = 0; ok; ++rnd) {
       const int64_t idx = sched_item(p.g, rnd, cta, grid);
       if (idx >= n_items) break;
-      const DkvGeo t = dkv_geo<VL>(p, vt, idx);
+      const DkvGeo t = dkv_geo<VL, ROWS>(p, vt, idx);
       if (t.n == 0) continue;
       const int64_t j = t.j0 + row;
       // query-row bounds as 32-bit values (rows are TMA coordinates, < 2^31):
@@ -366,9 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           int64_t lo, hi, a0, b0, a1, b1;
-          key_rows(gm, t.ks, j, s, lo, hi);
-          key_rows(gm, t.ks, t.j0, s, a0, b0);
-          key_rows(gm, t.ks, jl, s, a1, b1);
+          key_rows<ROWS>(gm, p.rows, t.ks, j, s, lo, hi);
+          key_rows<ROWS>(gm, p.rows, t.ks, t.j0, s, a0, b0);
+          key_rows<ROWS>(gm, p.rows, t.ks, jl, s, a1, b1);
           kl[s] = (int)lo;
           kh[s] = (int)hi;
           al[s] = (int)imax64(a0, a1);
@@ -454,8 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32x2(tmem + R.tl + kColDK + half * (HD / 2) + c4 * 32,
                     tmem + R.tl + kColDV + half * (HD / 2) + c4 * 32, uk, uv);
         if (wr) {
-          store_row32(dKo, oofs + c4 * 32, uk, p.scale, p.g_f32, 0);
-          store_row32(dVo, oofs + c4 * 32, uv, 1.f, p.g_f32, 0);
+          store_row32(dKo, oofs + c4 * 32, uk, p.scale, p.g_f32, ROWS ? p.dkv_accumulate : 0);
+          store_row32(dVo, oofs + c4 * 32, uv, 1.f, p.g_f32, ROWS ? p.dkv_accumulate : 0);
         }
       }
       tc_fence_before();
@@ -473,10 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <int HD, bool VL>
+template <int HD, bool VL, bool ROWS = false>
 cudaError_t launch_dkv_t(const BwdMaps& m, const BwdParams& p, const VarlenTabs& vt, int64_t n, int grid,
                          uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {
-  auto k = bdlm_bwd_dkv_tc_kernel<HD, VL>;
+  auto k = bdlm_bwd_dkv_tc_kernel<HD, VL, ROWS>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvLayout<HD>::kAlloc);
   if (e != cudaSuccess) return e;
   k<<<grid, kThreads, DkvLayout<HD>::kAlloc, stream>>>(m.Qc, m.Qn, m.dOc, m.dOn, m.Kc, m.Kn, m.Vc, m.Vn, p, vt, n,
@@ -491,10 +501,20 @@ cudaError_t launch_bwd_dkv_tc(const BwdMaps& m, const BwdParams& p, const Varlen
   const int grid = (int)(n < num_sms ? n : num_sms);
   const VarlenTabs none{nullptr, nullptr, nullptr, 0, 0};
   const VarlenTabs& t = vt ? *vt : none;
-  cudaError_t e = p.d == 128 ? (vt ? launch_dkv_t<128, true>(m, p, t, n, grid, status, limit_ns, stream)
-                                   : launch_dkv_t<128, false>(m, p, t, n, grid, status, limit_ns, stream))
-                             : (vt ? launch_dkv_t<64, true>(m, p, t, n, grid, status, limit_ns, stream)
-                                   : launch_dkv_t<64, false>(m, p, t, n, grid, status, limit_ns, stream));
+  // a row range, or accumulation across calls: the rows instantiation (one sequence)
+  const RowRange all;
+  const bool rows = p.dkv_accumulate || p.rows.lo[0] != all.lo[0] || p.rows.lo[1] != all.lo[1] ||
+                    p.rows.hi[0] != all.hi[0] || p.rows.hi[1] != all.hi[1];
+  if (rows && vt) return cudaErrorInvalidValue;
+  cudaError_t e;
+  if (rows)
+    e = p.d == 128 ? launch_dkv_t<128, false, true>(m, p, t, n, grid, status, limit_ns, stream)
+                   : launch_dkv_t<64, false, true>(m, p, t, n, grid, status, limit_ns, stream);
+  else
+    e = p.d == 128 ? (vt ? launch_dkv_t<128, true>(m, p, t, n, grid, status, limit_ns, stream)
+                         : launch_dkv_t<128, false>(m, p, t, n, grid, status, limit_ns, stream))
+                   : (vt ? launch_dkv_t<64, true>(m, p, t, n, grid, status, limit_ns, stream)
+                         : launch_dkv_t<64, false>(m, p, t, n, grid, status, limit_ns, stream));
   if (e != cudaSuccess) return e;
   if (launches) ++*launches;
   return cudaGetLastError();

@@ -82,6 +82,7 @@ __device__ __forceinline__ DqGeo dq_geo(const BwdParams& p, const VarlenTabs& vt
   t.q = qtile_ranges(g, t.stream, t.r0, r1, QBN);
   t.nc = (int)(t.q.c1 - t.q.c0);
   t.n = t.nc + (int)(t.q.n1 - t.q.n0);
+  if (!tile_in(p.rows, t.stream, t.r0, r1)) t.nc = t.n = 0;  // none of the call's rows
   t.rot = sweep_rotation(idx, t.nc);
   return t;
 }
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (one sequence: its length and offset come from the parameters)
       const int64_t seqL = VL ? t.L : p.g.L, seq0 = VL ? t.off : 0;
       const int64_t r = t.r0 + row;  // row within the item's sequence
-      const bool valid = r < seqL;
+      const bool valid = r < seqL && row_in(p.rows, t.stream, r);
       void* dqbase = t.stream ? p.dQn : p.dQc;
       const int64_t oofs = ((seq0 + r) * p.g.Hq + t.head) * HD + half * (HD / 2);
       if (t.n == 0) {
@@ -285,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      const int64_t rr = valid ? r : seqL - 1;
+      const int64_t rr = r < seqL ? r : seqL - 1;
       const Geom gm = VL ? seq_geom(p.g, t.L) : p.g;
       int64_t clo, chi, nlo, nhi;
       clean_interval(gm, t.stream, rr, clo, chi);

@@ -82,10 +82,11 @@ struct ItemGeo {
 
 // VL: packed variable-length batch (a separate instantiation, so that the
 // one-sequence kernel keeps its register budget).
-template <bool VL>
-__device__ __forceinline__ ItemGeo item_geo(const FwdParams& p, const VarlenTabs& vt, int64_t idx) {
+template <bool VL, bool ROWS = false>
+__device__ __forceinline__ ItemGeo item_geo(const FwdParams& p, const VarlenTabs& vt, const RowRange& rows,
+                                            int64_t idx) {
   ItemGeo t;
-  Geom g = p.g;
+  Geom gs;  // the item's sequence (packed batch only)
   int64_t qtile;
   t.off = 0;
   if (VL) {  // packed batch: the item and its sequence from the tables
@@ -94,13 +95,14 @@ __device__ __forceinline__ ItemGeo item_geo(const FwdParams& p, const VarlenTabs
     t.head = e.y >> 1;
     qtile = e.z;
     t.off = vt.seq_off[e.x];
-    g = seq_geom(p.g, vt.seq_off[e.x + 1] - t.off);
+    gs = seq_geom(p.g, vt.seq_off[e.x + 1] - t.off);
   } else {
     const QItem it = q_item(p.g, BI, idx);
     t.stream = it.stream;
     t.head = it.head;
     qtile = it.qtile;
   }
+  const Geom& g = VL ? gs : p.g;
   t.L = g.L;
   t.kvh = t.head / (p.g.Hq / p.g.Hkv);
   t.r0 = qtile * BI;
@@ -108,6 +110,7 @@ __device__ __forceinline__ ItemGeo item_geo(const FwdParams& p, const VarlenTabs
   t.q = qtile_ranges(g, t.stream, t.r0, r1, BN);
   t.nc = (int)(t.q.c1 - t.q.c0);
   t.n = t.nc + (int)(t.q.n1 - t.q.n0);
+  if (ROWS && !tile_in(rows, t.stream, t.r0, r1)) t.nc = t.n = 0;  // none of the call's rows
   t.rot = sweep_rotation(idx, t.nc);
   return t;
 }
@@ -183,12 +186,12 @@ __device__ __forceinline__ uint64_t exp_store64(const uint32_t (&a)[32], const u
   return f2_add(r, exp_store32(b, sl2x2, nm2, taddr + 16));
 }
 
-template <int HD, bool VL, bool FIXREF>
+template <int HD, bool VL, bool FIXREF, bool ROWS>
 __global__ void __launch_bounds__(kThreads, 1)
     bdlm_fwd_tc_kernel(const __grid_constant__ CUtensorMap tQc, const __grid_constant__ CUtensorMap tQn,
                        const __grid_constant__ CUtensorMap tKc, const __grid_constant__ CUtensorMap tKn,
                        const __grid_constant__ CUtensorMap tVc, const __grid_constant__ CUtensorMap tVn,
-                       const FwdParams p, const VarlenTabs vt, const FwdRef ref) {
+                       const FwdParams p, const VarlenTabs vt, const FwdRef ref, const RowRange rows) {
   using LY = Layout<HD>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -240,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t rnd = 0; ok; ++rnd) {
         const int64_t idx = sched_item(p.g, rnd, cta, grid);
         if (idx >= n_items) break;
-        const ItemGeo g = item_geo<VL>(p, vt, idx);
+        const ItemGeo g = item_geo<VL, ROWS>(p, vt, rows, idx);
         if (g.n == 0) continue;
         if (itn > 0 && !mbar_wait(BAR(B_QE), (itn - 1) & 1, wd, 1)) { ok = false; break; }
         mbar_arrive_expect_tx(BAR(B_QF), 2 * LY::kTile);
@@ -298,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t rnd = 0; ok; ++rnd) {
         const int64_t idx = sched_item(p.g, rnd, cta, grid);
         if (idx >= n_items) break;
-        const ItemGeo g = item_geo<VL>(p, vt, idx);
+        const ItemGeo g = item_geo<VL, ROWS>(p, vt, rows, idx);
         if (g.n == 0) continue;
         if (!mbar_wait(BAR(B_QF), itn & 1, wd, 4)) { ok = false; break; }
         if (!mbar_wait(BAR(B_KF + (kc & 1)), (kc >> 1) & 1, wd, 5)) { ok = false; break; }
@@ -351,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t rnd = 0; ok; ++rnd) {
       const int64_t idx = sched_item(p.g, rnd, cta, grid);
       if (idx >= n_items) break;
-      const ItemGeo g = item_geo<VL>(p, vt, idx);
+      const ItemGeo g = item_geo<VL, ROWS>(p, vt, rows, idx);
       // (one sequence: its length and offset come from the parameters, so
       // that they occupy no registers across the loop)
       const int64_t seqL = VL ? g.L : p.g.L, seq0 = VL ? g.off : 0;
@@ -361,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       void* obase = g.stream ? p.On : p.Oc;
       const int64_t oofs = ((seq0 + r) * p.g.Hq + g.head) * HD;
       if (g.n == 0) {
-        if (valid) {
+        if (valid && (!ROWS || row_in(rows, g.stream, r))) {
           if (p.o_f32) {
             float4* o = reinterpret_cast<float4*>(static_cast<float*>(obase) + oofs);
 #pragma unroll
@@ -462,10 +465,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       ok = mbar_wait(BAR(B_OD + t), itn & 1, wd, 13);
-      const ItemGeo ge = item_geo<VL>(p, vt, idx);
+      const ItemGeo ge = item_geo<VL, ROWS>(p, vt, rows, idx);
       const int64_t seqL_e = VL ? ge.L : p.g.L, seq0_e = VL ? ge.off : 0;
       const int64_t re = ge.r0 + t * BM + row;
-      const bool ve = re < seqL_e;
+      const bool ve = re < seqL_e && (!ROWS || row_in(rows, ge.stream, re));
       float* lse_e = (ge.stream ? p.LSEn : p.LSEc) + (int64_t)ge.head * p.g.L + seq0_e;
       void* obase_e = ge.stream ? p.On : p.Oc;
       const int64_t oofs_e = ((seq0_e + re) * p.g.Hq + ge.head) * HD;
@@ -521,34 +524,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <int HD, bool VL, bool FIXREF>
-cudaError_t launch_fwd_t(const FwdMaps& maps, const FwdParams& p, const VarlenTabs& vt, const FwdRef& ref, int grid,
-                         cudaStream_t stream) {
-  auto k = bdlm_fwd_tc_kernel<HD, VL, FIXREF>;
+template <int HD, bool VL, bool FIXREF, bool ROWS = false>
+cudaError_t launch_fwd_t(const FwdMaps& maps, const FwdParams& p, const VarlenTabs& vt, const FwdRef& ref,
+                         const RowRange& rows, int grid, cudaStream_t stream) {
+  auto k = bdlm_fwd_tc_kernel<HD, VL, FIXREF, ROWS>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<HD>::kAlloc);
   if (e != cudaSuccess) return e;
   k<<<grid, kThreads, Layout<HD>::kAlloc, stream>>>(maps.Qc, maps.Qn, maps.Kc, maps.Kn, maps.Vc, maps.Vn, p, vt,
-                                                    ref);
+                                                    ref, rows);
   return cudaSuccess;
 }
 
-cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, const VarlenTabs* vt, const FwdRef* ref, int d,
-                       int num_sms, cudaStream_t stream, int* launches) {
+cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, const VarlenTabs* vt, const FwdRef* ref,
+                       const RowRange* rows, int d, int num_sms, cudaStream_t stream, int* launches) {
   const int64_t grid64 = p.n_items < num_sms ? p.n_items : num_sms;
   const int grid = (int)(grid64 > 0 ? grid64 : 1);
   const VarlenTabs none{nullptr, nullptr, nullptr, 0, 0};
   const VarlenTabs& t = vt ? *vt : none;
   const FwdRef noref{nullptr, nullptr};
+  const RowRange all;
   cudaError_t e;
-  if (ref) {  // verification mode: one sequence only
+  if (ref) {  // verification mode: one sequence only, all rows
+    if (vt || rows) return cudaErrorInvalidValue;
+    e = d == 128 ? launch_fwd_t<128, false, true>(maps, p, t, *ref, all, grid, stream)
+                 : launch_fwd_t<64, false, true>(maps, p, t, *ref, all, grid, stream);
+  } else if (rows) {  // one rank's rows: one sequence only
     if (vt) return cudaErrorInvalidValue;
-    e = d == 128 ? launch_fwd_t<128, false, true>(maps, p, t, *ref, grid, stream)
-                 : launch_fwd_t<64, false, true>(maps, p, t, *ref, grid, stream);
+    e = d == 128 ? launch_fwd_t<128, false, false, true>(maps, p, t, noref, *rows, grid, stream)
+                 : launch_fwd_t<64, false, false, true>(maps, p, t, noref, *rows, grid, stream);
   } else {
-    e = d == 128 ? (vt ? launch_fwd_t<128, true, false>(maps, p, t, noref, grid, stream)
-                       : launch_fwd_t<128, false, false>(maps, p, t, noref, grid, stream))
-                 : (vt ? launch_fwd_t<64, true, false>(maps, p, t, noref, grid, stream)
-                       : launch_fwd_t<64, false, false>(maps, p, t, noref, grid, stream));
+    e = d == 128 ? (vt ? launch_fwd_t<128, true, false>(maps, p, t, noref, all, grid, stream)
+                       : launch_fwd_t<128, false, false>(maps, p, t, noref, all, grid, stream))
+                 : (vt ? launch_fwd_t<64, true, false>(maps, p, t, noref, all, grid, stream)
+                       : launch_fwd_t<64, false, false>(maps, p, t, noref, all, grid, stream));
   }
   if (e != cudaSuccess) return e;
   if (launches) ++*launches;

@@ -35,6 +35,16 @@ struct Geom {
   int round_items = 152;     // CTAs of the persistent grid (the device's SM count): items per block and KV head
 };
 
+// Query rows a call computes, per stream (0 clean, 1 corrupted): [lo, hi).
+// The defaults cover every row.  A rank of a multi-rank CSBP deployment
+// computes only the rows it owns; rows outside are neither computed into
+// other rows' results nor written.  (Kept apart from Geom: the kernels that
+// do not restrict rows keep their parameter blocks, and registers, as is.)
+struct RowRange {
+  int32_t lo[2] = {0, 0};
+  int32_t hi[2] = {0x7fffffff, 0x7fffffff};
+};
+
 BDLM_HD int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 BDLM_HD int64_t imax64(int64_t a, int64_t b) { return a > b ? a : b; }
 BDLM_HD int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -59,6 +69,32 @@ BDLM_HD void noisy_interval(const Geom& g, int stream, int64_t i, int64_t& lo, i
     lo = 0;
     hi = 0;
   }
+}
+
+// A row range's bounds for `stream` (selected, not indexed, so that a local
+// copy stays in registers).
+BDLM_HD int64_t range_lo(const RowRange& r, int stream) { return stream ? r.lo[1] : r.lo[0]; }
+BDLM_HD int64_t range_hi(const RowRange& r, int stream) { return stream ? r.hi[1] : r.hi[0]; }
+
+// True when query row i of `stream` is in the range.
+BDLM_HD bool row_in(const RowRange& r, int stream, int64_t i) {
+  return i >= range_lo(r, stream) && i < range_hi(r, stream);
+}
+
+// True when some row of the query tile [r0, r1) of `stream` is in the range.
+// (The forward and dQ visit the key tiles of a tile's rows and write only
+// the range's rows; a tile without any is skipped.)
+BDLM_HD bool tile_in(const RowRange& r, int stream, int64_t r0, int64_t r1) {
+  return r1 > range_lo(r, stream) && r0 < range_hi(r, stream);
+}
+
+// The query rows of each stream that read a key tile (kv_tile_rows),
+// restricted to the range.
+BDLM_HD void clamp_rows(const RowRange& r, int64_t& c_lo, int64_t& c_hi, int64_t& n_lo, int64_t& n_hi) {
+  c_lo = imax64(c_lo, r.lo[0]); c_hi = imin64(c_hi, r.hi[0]);
+  n_lo = imax64(n_lo, r.lo[1]); n_hi = imin64(n_hi, r.hi[1]);
+  if (c_hi <= c_lo) c_lo = c_hi = 0;
+  if (n_hi <= n_lo) n_lo = n_hi = 0;
 }
 
 BDLM_HD bool visible(const Geom& g, int stream, int64_t i, int key_stream, int64_t j) {

@@ -60,8 +60,9 @@ constexpr int kFwdItemRows = 256;
 constexpr int kFwdTileK = 128;
 
 // vt: null for one sequence.  ref: null for the production kernel (see FwdRef).
-cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, const VarlenTabs* vt, const FwdRef* ref, int d,
-                       int num_sms, cudaStream_t stream, int* launches);
+// rows: null for every row (else one sequence, no ref).
+cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, const VarlenTabs* vt, const FwdRef* ref,
+                       const RowRange* rows, int d, int num_sms, cudaStream_t stream, int* launches);
 
 // ------------------------------------------------------------- backward
 struct BwdParams {
@@ -74,6 +75,8 @@ struct BwdParams {
   void *dQc, *dQn, *dKc, *dVc, *dKn, *dVn;
   int g_f32;         // gradient outputs fp32 (else bf16)
   int dq_accumulate; // dQ += contribution (fp32 only)
+  int dkv_accumulate;  // dK, dV += contribution (fp32 only)
+  RowRange rows;       // query rows of the call (default: all)
 };
 
 // Tensor maps of the tensor-core backward passes: [L, H, d] bf16 viewed 3-D,

@@ -85,9 +85,12 @@ static void check_sched(const Geom& g, int grid, int64_t rounds) {
     }
 }
 
-// Brute-force visibility (the mask, with the call's key restriction).
+// Brute-force visibility (the mask, with the call's key restriction and,
+// for the key-tile row ranges, the call's row range).
+static RowRange g_rows;  // the row range under test (default: every row)
 static bool sees(const Geom& g, int s, int64_t i, int ks, int64_t j) {
   const int64_t bi = i / g.B, bj = j / g.B;
+  if (i < g_rows.lo[s] || i >= g_rows.hi[s]) return false;
   if (ks == 0) {
     if (j < g.kv_begin || j >= g.kv_end) return false;
     return s == 0 ? bj <= bi : bj < bi;
@@ -104,6 +107,7 @@ static void check_ranges(const Geom& g, int t) {
       const int64_t j0 = kt * t, j1 = imin64(j0 + t, g.L);
       int64_t r[4];
       kv_tile_rows(g, ks, j0, j1, r[0], r[1], r[2], r[3]);
+      clamp_rows(g_rows, r[0], r[1], r[2], r[3]);
       for (int s = 0; s < 2; ++s) {
         const int64_t lo = r[2 * s], hi = r[2 * s + 1];
         for (int64_t i = 0; i < g.L; ++i) {
@@ -114,6 +118,9 @@ static void check_ranges(const Geom& g, int t) {
         }
       }
     }
+  // (qtile_ranges covers every row of a tile: the forward and dQ skip
+  // tiles without any of the call's rows and write only the call's rows)
+  if (g_rows.lo[0] != 0 || g_rows.lo[1] != 0 || g_rows.hi[0] < g.L || g_rows.hi[1] < g.L) return;
   for (int s = 0; s < 2; ++s)
     for (int64_t qt = 0; qt < nt; ++qt) {
       const int64_t r0 = qt * t, r1 = imin64(r0 + t, g.L);
@@ -246,12 +253,23 @@ int main() {
     for (int64_t B : {1, 8, 16, 32, 48})
       for (int t : {16, 32, 64}) {
         if (L % B) continue;
-        for (int v = 0; v < 4; ++v) {
+        for (int v = 0; v < 6; ++v) {
           Geom g{L, B, 2, 1, 0, L, 1};
           if (v == 1) { g.kv_begin = L / 4; g.kv_end = L / 2; }
           if (v == 2) { g.kv_begin = L / 3; g.kv_end = L; g.include_local = 0; }
           if (v == 3) { g.kv_begin = g.kv_end = 0; }
+          g_rows = RowRange();
+          if (v == 4) {  // one rank's rows: a clean slice and another corrupted slice
+            g_rows.lo[0] = (int32_t)(L / 4); g_rows.hi[0] = (int32_t)(L / 2);
+            g_rows.lo[1] = (int32_t)(L / 2); g_rows.hi[1] = (int32_t)(3 * L / 4);
+          }
+          if (v == 5) {  // rows not aligned to tiles, with a key shard
+            g_rows.lo[0] = 5; g_rows.hi[0] = (int32_t)(L - 7);
+            g_rows.lo[1] = (int32_t)(L / 3); g_rows.hi[1] = (int32_t)(L / 3 + 9);
+            g.kv_begin = L / 8; g.kv_end = L / 2;
+          }
           check_ranges(g, t);
+          g_rows = RowRange();
         }
       }
   if (failures) {

@@ -221,3 +221,18 @@ def test_noalloc_size_limit_edge_on_host(lib):
     st = f(*([None] * 12), 4194304, 32, 1, 1, 128, 0.088, *([None] * 6), 0, None)
     assert st == 4, (st, m.bdlm_last_error())
     assert "4194272" in m.bdlm_last_error()
+
+
+def test_binding_signatures_match_header():
+    """Every function the Python binding declares to ctypes exists in the C
+    header with the same number of parameters, and every header function
+    has a binding signature."""
+    import re
+    hdr = open(m.HEADER_PATH).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    for name, (_res, args) in m._SIGS.items():
+        mm = re.search(r"\b" + name + r"\s*\((.*?)\);", hdr, flags=re.S)
+        assert mm, name
+        params = [p.strip() for p in mm.group(1).split(",") if p.strip() and p.strip() != "void"]
+        assert len(params) == len(args), (name, len(params), len(args))
+    assert set(m.header_functions()) == set(m._SIGS)

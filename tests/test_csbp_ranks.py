@@ -160,6 +160,9 @@ def test_csbp_plan_covers_and_balances():
         assert [a for (a, _) in plan.clean_shards] == [r * N // R for r in range(R)]
         assert plan.clean_shards[-1][1] == N
         assert sorted(j for r in range(R) for j in plan.rows(r).noisy_blocks) == list(range(N))
-        assert plan.imbalance() < 1.02, (L, B, R, plan.imbalance())
+        assert plan.imbalance() == 1.0, (L, B, R, plan.imbalance())
+        for r in range(R):
+            rw = plan.rows(r)
+            assert (rw.n0, rw.n1) == plan.clean_shards[R - 1 - r]   # the mirror slice, contiguous
     with pytest.raises(ValueError):
         csbp.CSBPPlan.build(256, 16, 3)   # 16 blocks do not split into 3 whole-block shards

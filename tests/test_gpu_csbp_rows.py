@@ -1,0 +1,98 @@
+"""Multi-rank CSBP's per-rank compute on one GPU: every rank of the plan
+(structured_mask_attention_gb300/csbp.py: clean shard r, the mirror slice of
+corrupted blocks) makes its calls in turn with the row-restricted kernels
+(bdlm_attn_fwd_shard_rows, bdlm_attn_bwd_shard_rows).  Each rank merges the
+partials of its own rows; the backward adds every rank's contributions into
+shared fp32 accumulators (the sum a reduce-scatter makes across ranks).
+The reassembled outputs and gradients must match the fp64 oracle, and a
+call must leave the rows outside its ranges untouched."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle.bdlm_oracle as orc
+from structured_mask_attention_gb300 import csbp
+from structured_mask_attention_gb300.inputs import make_numpy
+from tests.parity_util import check_lse, check_rel, to_dev, to_np
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+NAMES = ("Qc", "Kc", "Vc", "Qn", "Kn", "Vn", "dOc", "dOn")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import structured_mask_attention_gb300 as m
+    m.load_library()
+    return m
+
+
+@pytest.mark.parametrize("L,B,R,Hq,Hkv,d", [
+    (4096, 256, 4, 8, 4, 128),   # rank slices of 1024 rows
+    (4096, 128, 8, 4, 2, 128),   # 8 ranks, slices of 512 rows
+    (512, 32, 4, 2, 1, 64),      # slices of 128 rows: forward items (256 rows) straddle two ranks
+    (768, 32, 4, 3, 1, 128),     # slices of 192 rows: no tile boundary matches a rank boundary
+])
+def test_rank_rows_reassemble_unsharded(lib, L, B, R, Hq, Hkv, d):
+    m = lib
+    X = make_numpy(L, Hq, Hkv, d, seed=L + R)
+    X64 = {k: v.astype(np.float64) for k, v in X.items()}
+    dev = {k: to_dev(v, torch) for k, v in X.items()}
+    ins = [dev[k] for k in NAMES[:6]]
+    sc = 1.0 / math.sqrt(d)
+    plan = csbp.CSBPPlan.build(L, B, R)
+    f32 = dict(dtype=torch.float32, device="cuda")
+    Oc, On = torch.zeros((L, Hq, d), **f32), torch.zeros((L, Hq, d), **f32)
+    LSEc, LSEn = torch.full((Hq, L), float("nan"), **f32), torch.full((Hq, L), float("nan"), **f32)
+    specs = [(*plan.shard_keys(s), False) for s in range(R)] + [(0, 0, True)]
+    for r in range(R):
+        rw = plan.rows(r)
+        rc, rn = (rw.c0 * B, rw.c1 * B), (rw.n0 * B, rw.n1 * B)
+        parts = [m.bdlm_attn_fwd_shard_rows(*ins, B, lo, hi, loc, rc, rn, sc) for (lo, hi, loc) in specs]
+        # rows outside the rank's ranges keep the outputs' initial values
+        for p in parts:
+            for (a, b), O, LSE in ((rc, p[0], p[2]), (rn, p[1], p[3])):
+                assert not O[:a].any() and not O[b:].any()
+                assert torch.isneginf(LSE[:, :a]).all() and torch.isneginf(LSE[:, b:]).all()
+        oc, lc = m.bdlm_lse_merge([p[0] for p in parts], [p[2] for p in parts], o_dtype=torch.float32)
+        on, ln = m.bdlm_lse_merge([p[1] for p in parts], [p[3] for p in parts], o_dtype=torch.float32)
+        Oc[rc[0]:rc[1]], LSEc[:, rc[0]:rc[1]] = oc[rc[0]:rc[1]], lc[:, rc[0]:rc[1]]
+        On[rn[0]:rn[1]], LSEn[:, rn[0]:rn[1]] = on[rn[0]:rn[1]], ln[:, rn[0]:rn[1]]
+    assert not torch.isnan(LSEc).any() and not torch.isnan(LSEn).any()   # every row owned by some rank
+    ref = orc.fwd_blockwise(*[X64[k] for k in NAMES[:6]], B, sc)
+    check_rel("Oc (ranks)", to_np(Oc), ref[0])
+    check_rel("On (ranks)", to_np(On), ref[1])
+    check_lse("LSEc (ranks)", to_np(LSEc), ref[2])
+    check_lse("LSEn (ranks)", to_np(LSEn), ref[3])
+    # backward: merged statistics, every rank's contributions added up
+    Dc = m.bdlm_bwd_preprocess(Oc.to(torch.bfloat16), dev["dOc"])
+    Dn = m.bdlm_bwd_preprocess(On.to(torch.bfloat16), dev["dOn"])
+    z = lambda H: torch.zeros((L, H, d), **f32)
+    dQc, dQn, dKc, dVc, dKn, dVn = z(Hq), z(Hq), z(Hkv), z(Hkv), z(Hkv), z(Hkv)
+    for r in range(R):
+        rw = plan.rows(r)
+        rc, rn = (rw.c0 * B, rw.c1 * B), (rw.n0 * B, rw.n1 * B)
+        for (lo, hi, loc) in specs:
+            m.bdlm_attn_bwd_shard_rows(*ins, dev["dOc"], dev["dOn"], LSEc, LSEn, Dc, Dn, B, lo, hi, loc, rc, rn,
+                                       dQc, dQn, dKc, dVc, dKn, dVn, sc)
+    gref = orc.bwd_blockwise(*[X64[k] for k in NAMES], B, sc)
+    for name, g, r_ in zip(("dQc", "dKc", "dVc", "dQn", "dKn", "dVn"), (dQc, dKc, dVc, dQn, dKn, dVn), gref):
+        check_rel(f"{name} (ranks)", to_np(g), r_)
+
+
+def test_rank_rows_validation(lib):
+    m = lib
+    X = make_numpy(256, 2, 1, 64, seed=3)
+    ins = [to_dev(X[k], torch) for k in NAMES[:6]]
+    with pytest.raises(m.BdlmError) as e:
+        m.bdlm_attn_fwd_shard_rows(*ins, 32, 0, 256, True, (0, 300), (0, 256))
+    assert e.value.status == 2
+    with pytest.raises(m.BdlmError) as e:
+        m.bdlm_attn_fwd_shard_rows(*ins, 32, 0, 256, True, (128, 64), (0, 256))
+    assert e.value.status == 2
