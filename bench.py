@@ -649,6 +649,67 @@ def run_sweep(args):
         del X, ins, f, g, fo, go, wf, wb
         torch.cuda.empty_cache()
 
+    # ---- multi-rank CSBP: each rank's compute (its row-restricted partial
+    # forward and backward calls) timed alone on this GPU, as if it were that
+    # rank's device; the exchange is not included.  Mirror assignment of the
+    # corrupted slices (balanced) against the split by token position.
+    if "ranks" in want:
+        from structured_mask_attention_gb300 import csbp
+        w = WORKLOADS["long-128k"]
+        L, B, Hq, Hkv, d = w["L"], w["B"], w["Hq"], w["Hkv"], w["d"]
+        sc = 1.0 / math.sqrt(d)
+        X = make_torch(L, Hq, Hkv, d, seed=0, device=dev)
+        ins = [X[k] for k in names]
+        fu = m.bdlm_attn_fwd(*ins, B, sc)
+        gu = m.bdlm_attn_bwd(*ins, fu[0], fu[1], X["dOc"], X["dOn"], fu[2], fu[3], B, sc)
+        un = timed(lambda: (m.bdlm_attn_fwd(*ins, B, sc, out=fu),
+                            m.bdlm_attn_bwd(*ins, fu[0], fu[1], X["dOc"], X["dOn"], fu[2], fu[3], B, sc, out=gu)))
+        del gu
+        # merged statistics of the whole problem (the ranks' merged rows equal them up to rounding)
+        Dc = m.bdlm_bwd_preprocess(fu[0], X["dOc"])
+        Dn = m.bdlm_bwd_preprocess(fu[1], X["dOn"])
+        z = lambda H: torch.zeros((L, H, d), dtype=torch.float32, device=dev)
+        acc = (z(Hq), z(Hq), z(Hkv), z(Hkv), z(Hkv), z(Hkv))
+        for R in (2, 4, 8):
+            f32 = dict(dtype=torch.float32, device=dev)
+            parts = [(torch.zeros((L, Hq, d), **f32), torch.zeros((L, Hq, d), **f32),
+                      torch.full((Hq, L), float("-inf"), **f32), torch.full((Hq, L), float("-inf"), **f32))
+                     for _ in range(R + 1)]
+            for policy, schedule in [(p_, "per_shard") for p_ in csbp.POLICIES] + [("mirror", "gathered")]:
+                plan = csbp.CSBPPlan.build(L, B, R, policy)
+                if schedule == "per_shard":  # partials per clean shard + the local one, merged
+                    specs = [(*plan.shard_keys(s_), False) for s_ in range(R)] + [(0, 0, True)]
+                else:  # one call over the all-gathered clean sequence and the local blocks
+                    specs = [(0, L, True)]
+
+                def rank_fwd(r):
+                    rw = plan.rows(r)
+                    rc, rn = (rw.c0 * B, rw.c1 * B), (rw.n0 * B, rw.n1 * B)
+                    for (lo, hi, loc), pt in zip(specs, parts):
+                        m.bdlm_attn_fwd_shard_rows(*ins, B, lo, hi, loc, rc, rn, sc, out=pt)
+
+                def rank_bwd(r):
+                    rw = plan.rows(r)
+                    rc, rn = (rw.c0 * B, rw.c1 * B), (rw.n0 * B, rw.n1 * B)
+                    for (lo, hi, loc) in specs:
+                        m.bdlm_attn_bwd_shard_rows(*ins, X["dOc"], X["dOn"], fu[2], fu[3], Dc, Dn, B, lo, hi, loc,
+                                                   rc, rn, *acc, sc)
+
+                per = [(timed(lambda: rank_fwd(r)), timed(lambda: rank_bwd(r))) for r in range(R)]
+                tot = [a + b_ for (a, b_) in per]
+                mean = sum(tot) / R
+                emit({"sweep": "ranks", "workload": "long-128k", "L": L, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d,
+                      "R": R, "policy": policy, "schedule": schedule, "calls_per_rank": 2 * len(specs),
+                      "rank_fwd_ms": [round(a, 3) for (a, _) in per], "rank_bwd_ms": [round(b_, 3) for (_, b_) in per],
+                      "max_ms": round(max(tot), 3), "mean_ms": round(mean, 3),
+                      "imbalance": round(max(tot) / mean, 4), "model_imbalance": round(plan.imbalance(), 4),
+                      "sum_over_ranks_ms": round(sum(tot), 3), "unsharded_ms": round(un, 3),
+                      "useful_tflops_per_rank_bound": round(useful_flops(L, B, Hq, d) / R / (max(tot) * 1e-3) / 1e12, 1),
+                      "reps": reps})
+            del parts
+        del X, ins, fu, Dc, Dn, acc
+        torch.cuda.empty_cache()
+
     # ---- the fp64 oracle on the host cores: a timed sample per config,
     # extrapolated by useful FLOP to the whole config (all heads, both streams)
     for name in (("tiny", "gqa-8k", "gqa-32k", "long-128k", "sharded-256k") if "oracle" in want else ()):
@@ -706,10 +767,11 @@ def main():
                          "schedule ablation (BDLM_SCHED=naive vs longest first) and the sharded-256k "
                          "block-size sweep with merge and preprocess bandwidth, and packed batches "
                          "(one packed call vs one call per sequence)")
-    ap.add_argument("--sweep-parts", default="config,sharded,shardcheck,packed,oracle",
+    ap.add_argument("--sweep-parts", default="config,sharded,shardcheck,packed,ranks,oracle",
                     help="comma-separated parts of --sweep to run (config includes the schedule ablation; "
                          "shardcheck: sharded vs unsharded fp32 output differences, production path and "
-                         "fixed-reference mode)")
+                         "fixed-reference mode; ranks: each rank's compute of multi-rank CSBP at long-128k, "
+                         "balanced and by-position assignment)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -17,12 +17,16 @@ App. I / Table 5 per the review's Strengths):
   (R - 1 - r)-th: every rank then carries the same work,
   B^2 ((R - 1) n^2 + n (n + 1)) for n = L / (B R) blocks per slice (the
   load balancing of App. I), and both of its row sets are contiguous.
+  (``policy="contiguous"``, rank r taking the r-th slice as a split by token
+  position would, is kept as the unbalanced ablation.)
 * Forward on rank r: for every clean shard s in order 0..R-1 a partial
   (O_s, LSE_s) of the rank's rows against shard s's keys, then the local
   partial (corrupted rows against their own block), merged exactly by
   log-sum-exp in that fixed order.  Only clean K/V cross ranks: here they are
   all-gathered once; a ring that holds two shards at a time is the same
-  plan with less memory.
+  plan with less memory.  Once all shards are gathered the rank may instead
+  make one call over the whole clean sequence (``gathered=True``): the same
+  result without partials or a merge.
 * Backward on rank r, with the merged LSE and D = rowsum(dO * O) of its own
   rows: per clean shard s, dQ of its rows (summed over s in order) and the
   contribution of its rows to shard s's clean dK / dV; the clean
@@ -49,17 +53,18 @@ object passed in by the caller:
 * ``comm``: ``rank``, ``world``, ``all_gather(x) -> list`` and
   ``sum_to_owner(x, owner) -> x or None`` (the sum over ranks, on the owner).
 
-On GB300s the compute object is the library's tensor-core kernels
-restricted to a rank's rows (`bdlm_attn_fwd_shard_rows`,
+On GB300s the compute object is ``KernelCompute``: the library's
+tensor-core kernels restricted to a rank's rows (`bdlm_attn_fwd_shard_rows`,
 `bdlm_attn_bwd_shard_rows`: row ranges per stream, gradients accumulated
-over calls) and the transport is NCCL over NVLink (no TMA multicast, and no
-kernel reads a peer's memory: shards are copied into local HBM first).  The
-row-restricted kernels are checked on one GPU with every rank's calls made
-in turn (tests/test_gpu_csbp_rows.py); the plan and this driver are checked
+over calls), and the transport is ``TorchComm``, NCCL over NVLink through
+torch.distributed (no TMA multicast, and no kernel reads a peer's memory:
+shards are copied into local HBM first).  Checked: the plan and this driver
 with gloo ranks on the CPU and the fp64 oracle as the compute object
-(tests/test_csbp_ranks.py).  The kernels index full-length tensors, so a
-rank would hold its rows in full-length buffers; the multi-GPU path is
-unmeasured on hardware.
+(tests/test_csbp_ranks.py); the driver with ``KernelCompute`` for every rank
+on one GPU, the ranks as host threads exchanging through host-side
+collectives (tests/test_gpu_csbp_rows.py).  The kernels index full-length
+tensors, so a rank holds its rows in full-length buffers.  No run on
+several GPUs exists.
 """
 from __future__ import annotations
 
@@ -80,28 +85,37 @@ class Rows:
         return tuple(range(self.n0, self.n1))
 
 
+POLICIES = ("mirror", "contiguous")
+
+
 @dataclass
 class CSBPPlan:
     """Ownership of a length-L, block-size-B problem on R ranks."""
     L: int
     B: int
     R: int
+    policy: str = "mirror"
     clean_shards: list = field(default_factory=list)  # per rank: (first block, end block)
     noisy_owner: list = field(default_factory=list)   # per corrupted block: its rank
     load: list = field(default_factory=list)          # per rank: rows x keys of its work, both streams
 
     @staticmethod
-    def build(L: int, B: int, R: int) -> "CSBPPlan":
+    def build(L: int, B: int, R: int, policy: str = "mirror") -> "CSBPPlan":
+        """``policy``: "mirror" (rank r takes the (R - 1 - r)-th slice of
+        corrupted blocks: every rank carries the same work) or "contiguous"
+        (rank r takes the r-th slice, the split by token position of plain
+        context parallelism; an ablation without load balancing)."""
         if L <= 0 or B <= 0 or R <= 0 or L % B:
             raise ValueError("need L, B, R > 0 and L a multiple of B")
+        if policy not in POLICIES:
+            raise ValueError(f"policy must be one of {POLICIES}")
         N = L // B
         if N % R:
             raise ValueError("the clean shards hold whole blocks: (L / B) must be a multiple of R")
         per = N // R
-        plan = CSBPPlan(L, B, R)
+        plan = CSBPPlan(L, B, R, policy)
         plan.clean_shards = [(r * per, (r + 1) * per) for r in range(R)]
-        # corrupted blocks: the mirror slice of the rank's clean shard
-        plan.noisy_owner = [R - 1 - j // per for j in range(N)]
+        plan.noisy_owner = [(R - 1 - j // per) if policy == "mirror" else j // per for j in range(N)]
         # work of block j of either stream: B rows reading (j + 1) B keys
         cost = [B * (j + 1) * B for j in range(N)]
         plan.load = [sum(cost[j] for j in range(a, b)) for (a, b) in plan.clean_shards]
@@ -111,7 +125,7 @@ class CSBPPlan:
 
     def rows(self, r: int) -> Rows:
         c0, c1 = self.clean_shards[r]
-        n0, n1 = self.clean_shards[self.R - 1 - r]
+        n0, n1 = self.clean_shards[self.R - 1 - r if self.policy == "mirror" else r]
         return Rows(c0, c1, n0, n1)
 
     def shard_keys(self, s: int):
@@ -130,27 +144,49 @@ def gather_clean_kv(comm, Kc_local, Vc_local):
     return list(zip(comm.all_gather(Kc_local), comm.all_gather(Vc_local)))
 
 
-def forward(plan: CSBPPlan, comm, compute, shards):
-    """Forward of the rank's rows: partials against every clean shard in
-    order (``shards`` from ``gather_clean_kv``), then the local partial,
-    merged.  Returns the rank's (Oc, On, LSEc, LSEn) rows."""
+def _gathered(shards):
+    """The whole clean K and V from the all-gathered shards."""
+    import torch
+    return torch.cat([k for (k, _) in shards]), torch.cat([v for (_, v) in shards])
+
+
+def forward(plan: CSBPPlan, comm, compute, shards, gathered: bool = False):
+    """Forward of the rank's rows given ``shards`` from ``gather_clean_kv``.
+    Per-shard schedule (default): partials against every clean shard in
+    order, then the local partial, merged (the order a ring that overlaps
+    the exchange with compute would follow).  ``gathered``: one call over the
+    whole clean sequence and the local blocks (the rank holds every clean
+    shard after the all-gather; no partials, no merge).  Returns the rank's
+    (Oc, On, LSEc, LSEn) rows."""
     rows = plan.rows(comm.rank)
+    if gathered:
+        return compute.merge([compute.fwd(rows, (0, plan.L), _gathered(shards), True)])
     parts = [compute.fwd(rows, plan.shard_keys(s), shards[s], False) for s in range(plan.R)]
     parts.append(compute.fwd(rows, (0, 0), None, True))
     return compute.merge(parts)
 
 
-def backward(plan: CSBPPlan, comm, compute, shards, out, dO):
+def backward(plan: CSBPPlan, comm, compute, shards, out, dO, gathered: bool = False):
     """Backward of the rank's rows given its merged forward outputs
     ``out`` = (Oc, On, LSEc, LSEn) and upstream ``dO`` = (dOc, dOn) of its
     rows.  Returns (dQc, dQn) of its rows, the clean (dK, dV) of its own
     shard (summed over every rank's rows) and the corrupted (dK, dV) of its
-    own blocks."""
+    own blocks.  ``gathered``: one call over the whole clean sequence, its
+    clean dK / dV then summed shard by shard onto the owners."""
     rows = plan.rows(comm.rank)
     Oc, On, LSEc, LSEn = out
     stats = (LSEc, LSEn, compute.preprocess(Oc, dO[0]), compute.preprocess(On, dO[1]))
-    dQc = dQn = None
     mine = None
+    if gathered:
+        dQc, dQn, gk, gv, gkn, gvn = compute.bwd(rows, (0, plan.L), _gathered(shards), True, stats)
+        for s in range(plan.R):
+            a, b = plan.shard_keys(s)
+            k = comm.sum_to_owner(gk[a:b], s)
+            v = comm.sum_to_owner(gv[a:b], s)
+            if s == comm.rank:
+                mine = (k, v)
+        return (dQc, dQn), mine, (gkn, gvn)
+    dQc = dQn = None
     for s in range(plan.R):
         gq_c, gq_n, gk, gv, _, _ = compute.bwd(rows, plan.shard_keys(s), shards[s], False, stats)
         dQc = gq_c if dQc is None else dQc + gq_c
@@ -161,3 +197,107 @@ def backward(plan: CSBPPlan, comm, compute, shards, out, dO):
             mine = (k, v)
     gq_c, gq_n, _, _, gkn, gvn = compute.bwd(rows, (0, 0), None, True, stats)
     return (dQc + gq_c, dQn + gq_n), mine, (gkn, gvn)
+
+
+class TorchComm:
+    """The transport over torch.distributed: gloo for CPU tensors, NCCL for
+    CUDA tensors (no kernel of this library reads a peer's memory: every
+    exchanged shard lands in the rank's own memory first).  Uses the default
+    process group."""
+
+    def __init__(self):
+        import torch.distributed as dist
+        self._dist = dist
+        self.rank = dist.get_rank()
+        self.world = dist.get_world_size()
+
+    def all_gather(self, x):
+        """Every rank's ``x`` (same shape on every rank), in rank order."""
+        import torch
+        x = x.contiguous()
+        out = [torch.empty_like(x) for _ in range(self.world)]
+        self._dist.all_gather(out, x)
+        return out
+
+    def sum_to_owner(self, x, owner):
+        """The sum over ranks of ``x`` on rank ``owner`` (None elsewhere)."""
+        t = x.clone().contiguous()
+        self._dist.reduce(t, dst=owner, op=self._dist.ReduceOp.SUM)
+        return t if self.rank == owner else None
+
+
+class KernelCompute:
+    """One rank's compute on its GPU through the library's row-restricted
+    calls (``bdlm_attn_fwd_shard_rows``, ``bdlm_lse_merge``,
+    ``bdlm_bwd_preprocess``, ``bdlm_attn_bwd_shard_rows``).
+
+    ``local`` holds the rank's own tensors on the device: "Qc", "Kc", "Vc",
+    "dOc" are the rows of its clean shard, "Qn", "Kn", "Vn", "dOn" the rows of
+    its corrupted blocks ([rows, H, d], bf16).  The kernels index
+    full-length tensors, so they are placed into length-L buffers (zero
+    elsewhere; rows outside the rank's ranges are never read as queries, and
+    keys outside a call's key set are never read), and each clean shard
+    received from the exchange is copied into its key range before the
+    calls that use it.  Results are returned for the rank's rows only."""
+
+    def __init__(self, lib, plan: CSBPPlan, rank: int, local: dict, scale: float):
+        import torch
+        self.lib, self.plan, self.scale = lib, plan, scale
+        L, B = plan.L, plan.B
+        rw = plan.rows(rank)
+        self.rc, self.rn = (rw.c0 * B, rw.c1 * B), (rw.n0 * B, rw.n1 * B)
+
+        def full(name, rng):
+            t = local[name]
+            buf = torch.zeros((L,) + tuple(t.shape[1:]), dtype=t.dtype, device=t.device)
+            buf[rng[0]:rng[1]] = t
+            return buf
+
+        self.Qc, self.Qn = full("Qc", self.rc), full("Qn", self.rn)
+        self.Kn, self.Vn = full("Kn", self.rn), full("Vn", self.rn)
+        self.dOc, self.dOn = full("dOc", self.rc), full("dOn", self.rn)
+        self.Kc = torch.zeros((L,) + tuple(local["Kc"].shape[1:]), dtype=local["Kc"].dtype,
+                              device=local["Kc"].device)
+        self.Vc = torch.zeros_like(self.Kc)
+
+    def _place(self, kv, kv_data):
+        if kv_data is not None:
+            self.Kc[kv[0]:kv[1]] = kv_data[0]
+            self.Vc[kv[0]:kv[1]] = kv_data[1]
+
+    def _ins(self):
+        return self.Qc, self.Kc, self.Vc, self.Qn, self.Kn, self.Vn
+
+    def fwd(self, rows, kv, kv_data, local):
+        self._place(kv, kv_data)
+        return self.lib.bdlm_attn_fwd_shard_rows(*self._ins(), self.plan.B, kv[0], kv[1], local, self.rc, self.rn,
+                                                 self.scale)
+
+    def merge(self, parts):
+        import torch
+        oc, lc = self.lib.bdlm_lse_merge([p[0] for p in parts], [p[2] for p in parts], o_dtype=torch.float32)
+        on, ln = self.lib.bdlm_lse_merge([p[1] for p in parts], [p[3] for p in parts], o_dtype=torch.float32)
+        (a, b), (c, d) = self.rc, self.rn
+        return oc[a:b], on[c:d], lc[:, a:b].contiguous(), ln[:, c:d].contiguous()
+
+    def preprocess(self, O, dO):
+        return self.lib.bdlm_bwd_preprocess(O.contiguous(), dO.contiguous())
+
+    def bwd(self, rows, kv, kv_data, local, stats):
+        import torch
+        self._place(kv, kv_data)
+        L = self.plan.L
+        (a, b), (c, d) = self.rc, self.rn
+
+        def stat(v, lo, hi):
+            full_ = torch.zeros((v.shape[0], L), dtype=torch.float32, device=v.device)
+            full_[:, lo:hi] = v
+            return full_
+
+        LSEc, LSEn, Dc, Dn = stat(stats[0], a, b), stat(stats[1], c, d), stat(stats[2], a, b), stat(stats[3], c, d)
+        z = lambda t: torch.zeros(t.shape, dtype=torch.float32, device=t.device)
+        acc = (z(self.Qc), z(self.Qn), z(self.Kc), z(self.Vc), z(self.Kn), z(self.Vn))
+        self.lib.bdlm_attn_bwd_shard_rows(*self._ins(), self.dOc, self.dOn, LSEc, LSEn, Dc, Dn, self.plan.B,
+                                          kv[0], kv[1], local, self.rc, self.rn, *acc, self.scale)
+        dQc, dQn, dKc, dVc, dKn, dVn = acc
+        return dQc[a:b], dQn[c:d], dKc[kv[0]:kv[1]], dVc[kv[0]:kv[1]], dKn[c:d], dVn[c:d]

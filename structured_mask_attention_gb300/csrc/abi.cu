@@ -285,13 +285,14 @@ bdlm_status fwd_common(const void* Qc, const void* Kc, const void* Vc, const voi
   p.o_f32 = o_f32;
   p.LSEc = LSEc;
   p.LSEn = LSEn;
-  p.n_items = vt ? vt->n_q : q_items(p.g, kFwdItemRows);
+  const RowRange rr = rows ? row_range(rows) : RowRange();
+  // a row-restricted call lists only the query tiles that hold its rows
+  p.n_items = vt ? vt->n_q : rows ? q_items_rows(p.g, rr, kFwdItemRows) : q_items(p.g, kFwdItemRows);
   p.status = static_cast<uint32_t*>(ws);
   p.limit_ns = wait_limit_ns();
   BDLM_CHECK(clear_status(ws, st));
   int launches = 0;
   ScopedKernelTimer tm(K_FWD, st);
-  const RowRange rr = rows ? row_range(rows) : RowRange();
   cudaError_t e = launch_fwd(maps, p, vt, ref, rows ? &rr : nullptr, d, info.sms, st, &launches);
   tm.stop();
   return finish(e, launches, "forward launch");

@@ -502,9 +502,7 @@ cudaError_t launch_bwd_dkv_tc(const BwdMaps& m, const BwdParams& p, const Varlen
   const VarlenTabs none{nullptr, nullptr, nullptr, 0, 0};
   const VarlenTabs& t = vt ? *vt : none;
   // a row range, or accumulation across calls: the rows instantiation (one sequence)
-  const RowRange all;
-  const bool rows = p.dkv_accumulate || p.rows.lo[0] != all.lo[0] || p.rows.lo[1] != all.lo[1] ||
-                    p.rows.hi[0] != all.hi[0] || p.rows.hi[1] != all.hi[1];
+  const bool rows = p.dkv_accumulate || range_restricts(p.rows);
   if (rows && vt) return cudaErrorInvalidValue;
   cudaError_t e;
   if (rows)

@@ -56,7 +56,7 @@ struct DqGeo {
 };
 
 // VL: packed variable-length batch (a separate instantiation).
-template <bool VL>
+template <bool VL, bool ROWS>
 __device__ __forceinline__ DqGeo dq_geo(const BwdParams& p, const VarlenTabs& vt, int64_t idx) {
   DqGeo t;
   Geom g = p.g;
@@ -70,7 +70,7 @@ __device__ __forceinline__ DqGeo dq_geo(const BwdParams& p, const VarlenTabs& vt
     t.off = vt.seq_off[e.x];
     g = seq_geom(p.g, vt.seq_off[e.x + 1] - t.off);
   } else {
-    const QItem it = q_item(p.g, QBM, idx);
+    const QItem it = ROWS ? q_item_rows(p.g, p.rows, QBM, idx) : q_item(p.g, QBM, idx);
     t.stream = it.stream;
     t.head = it.head;
     qtile = it.qtile;
@@ -82,7 +82,7 @@ __device__ __forceinline__ DqGeo dq_geo(const BwdParams& p, const VarlenTabs& vt
   t.q = qtile_ranges(g, t.stream, t.r0, r1, QBN);
   t.nc = (int)(t.q.c1 - t.q.c0);
   t.n = t.nc + (int)(t.q.n1 - t.q.n0);
-  if (!tile_in(p.rows, t.stream, t.r0, r1)) t.nc = t.n = 0;  // none of the call's rows
+  if (ROWS && !tile_in(p.rows, t.stream, t.r0, r1)) t.nc = t.n = 0;  // none of the call's rows (not listed)
   t.rot = sweep_rotation(idx, t.nc);
   return t;
 }
@@ -95,7 +95,7 @@ __device__ __forceinline__ int dq_key0(const DqGeo& t, int j) {
   return (int)((j < t.nc ? t.q.c0 + c : t.q.n0 + (j - t.nc)) * QBN);
 }
 
-template <int HD, bool VL>
+template <int HD, bool VL, bool ROWS>
 __global__ void __launch_bounds__(kThreads, 1)
     bdlm_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tQc, const __grid_constant__ CUtensorMap tQn,
                           const __grid_constant__ CUtensorMap tdOc, const __grid_constant__ CUtensorMap tdOn,
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t rnd = 0; ok; ++rnd) {
         const int64_t idx = sched_item(p.g, rnd, cta, grid);
         if (idx >= n_items) break;
-        const DqGeo t = dq_geo<VL>(p, vt, idx);
+        const DqGeo t = dq_geo<VL, ROWS>(p, vt, idx);
         if (t.n == 0) continue;
         if (itn > 0 && !mbar_wait(BAR(DQ_QE), (itn - 1) & 1, wd, 21)) { ok = false; break; }
         mbar_arrive_expect_tx(BAR(DQ_QF), 2 * LY::kTile);
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t rnd = 0; ok; ++rnd) {
         const int64_t idx = sched_item(p.g, rnd, cta, grid);
         if (idx >= n_items) break;
-        const DqGeo t = dq_geo<VL>(p, vt, idx);
+        const DqGeo t = dq_geo<VL, ROWS>(p, vt, idx);
         if (t.n == 0) continue;
         if (!mbar_wait(BAR(DQ_QF), itn & 1, wd, 24)) { ok = false; break; }
         // stage of the previous step (read by its dQ MMA)
@@ -264,11 +264,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t rnd = 0; ok; ++rnd) {
       const int64_t idx = sched_item(p.g, rnd, cta, grid);
       if (idx >= n_items) break;
-      const DqGeo t = dq_geo<VL>(p, vt, idx);
+      const DqGeo t = dq_geo<VL, ROWS>(p, vt, idx);
       // (one sequence: its length and offset come from the parameters)
       const int64_t seqL = VL ? t.L : p.g.L, seq0 = VL ? t.off : 0;
       const int64_t r = t.r0 + row;  // row within the item's sequence
-      const bool valid = r < seqL && row_in(p.rows, t.stream, r);
+      const bool valid = r < seqL && (!ROWS || row_in(p.rows, t.stream, r));
       void* dqbase = t.stream ? p.dQn : p.dQc;
       const int64_t oofs = ((seq0 + r) * p.g.Hq + t.head) * HD + half * (HD / 2);
       if (t.n == 0) {
@@ -358,10 +358,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <int HD, bool VL>
+template <int HD, bool VL, bool ROWS = false>
 cudaError_t launch_dq_t(const BwdMaps& m, const BwdParams& p, const VarlenTabs& vt, int64_t n, int grid,
                         uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {
-  auto k = bdlm_bwd_dq_tc_kernel<HD, VL>;
+  auto k = bdlm_bwd_dq_tc_kernel<HD, VL, ROWS>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<HD>::kAlloc);
   if (e != cudaSuccess) return e;
   k<<<grid, kThreads, DqLayout<HD>::kAlloc, stream>>>(m.Qc, m.Qn, m.dOc, m.dOn, m.Kc, m.Kn, m.Vc, m.Vn, p, vt, n,
@@ -371,15 +371,23 @@ cudaError_t launch_dq_t(const BwdMaps& m, const BwdParams& p, const VarlenTabs& 
 
 cudaError_t launch_bwd_dq_tc(const BwdMaps& m, const BwdParams& p, const VarlenTabs* vt, int num_sms,
                              uint32_t* status, uint64_t limit_ns, cudaStream_t stream, int* launches) {
-  const int64_t n = vt ? vt->n_q : q_items(p.g, QBM);
+  // a row-restricted call lists only the query tiles that hold its rows (one sequence)
+  const bool rows = range_restricts(p.rows);
+  if (rows && vt) return cudaErrorInvalidValue;
+  const int64_t n = vt ? vt->n_q : rows ? q_items_rows(p.g, p.rows, QBM) : q_items(p.g, QBM);
   if (n == 0) return cudaSuccess;
   const int grid = (int)(n < num_sms ? n : num_sms);
   const VarlenTabs none{nullptr, nullptr, nullptr, 0, 0};
   const VarlenTabs& t = vt ? *vt : none;
-  cudaError_t e = p.d == 128 ? (vt ? launch_dq_t<128, true>(m, p, t, n, grid, status, limit_ns, stream)
-                                   : launch_dq_t<128, false>(m, p, t, n, grid, status, limit_ns, stream))
-                             : (vt ? launch_dq_t<64, true>(m, p, t, n, grid, status, limit_ns, stream)
-                                   : launch_dq_t<64, false>(m, p, t, n, grid, status, limit_ns, stream));
+  cudaError_t e;
+  if (rows)
+    e = p.d == 128 ? launch_dq_t<128, false, true>(m, p, t, n, grid, status, limit_ns, stream)
+                   : launch_dq_t<64, false, true>(m, p, t, n, grid, status, limit_ns, stream);
+  else
+    e = p.d == 128 ? (vt ? launch_dq_t<128, true>(m, p, t, n, grid, status, limit_ns, stream)
+                         : launch_dq_t<128, false>(m, p, t, n, grid, status, limit_ns, stream))
+                   : (vt ? launch_dq_t<64, true>(m, p, t, n, grid, status, limit_ns, stream)
+                         : launch_dq_t<64, false>(m, p, t, n, grid, status, limit_ns, stream));
   if (e != cudaSuccess) return e;
   if (launches) ++*launches;
   return cudaGetLastError();

@@ -97,7 +97,7 @@ __device__ __forceinline__ ItemGeo item_geo(const FwdParams& p, const VarlenTabs
     t.off = vt.seq_off[e.x];
     gs = seq_geom(p.g, vt.seq_off[e.x + 1] - t.off);
   } else {
-    const QItem it = q_item(p.g, BI, idx);
+    const QItem it = ROWS ? q_item_rows(p.g, rows, BI, idx) : q_item(p.g, BI, idx);
     t.stream = it.stream;
     t.head = it.head;
     qtile = it.qtile;
@@ -110,7 +110,7 @@ __device__ __forceinline__ ItemGeo item_geo(const FwdParams& p, const VarlenTabs
   t.q = qtile_ranges(g, t.stream, t.r0, r1, BN);
   t.nc = (int)(t.q.c1 - t.q.c0);
   t.n = t.nc + (int)(t.q.n1 - t.q.n0);
-  if (ROWS && !tile_in(rows, t.stream, t.r0, r1)) t.nc = t.n = 0;  // none of the call's rows
+  if (ROWS && !tile_in(rows, t.stream, t.r0, r1)) t.nc = t.n = 0;  // none of the call's rows (not listed)
   t.rot = sweep_rotation(idx, t.nc);
   return t;
 }

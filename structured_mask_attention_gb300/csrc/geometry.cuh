@@ -71,6 +71,12 @@ BDLM_HD void noisy_interval(const Geom& g, int stream, int64_t i, int64_t& lo, i
   }
 }
 
+// True unless the range is the default (every row of both streams).
+BDLM_HD bool range_restricts(const RowRange& r) {
+  const RowRange all;
+  return r.lo[0] != all.lo[0] || r.lo[1] != all.lo[1] || r.hi[0] != all.hi[0] || r.hi[1] != all.hi[1];
+}
+
 // A row range's bounds for `stream` (selected, not indexed, so that a local
 // copy stays in registers).
 BDLM_HD int64_t range_lo(const RowRange& r, int stream) { return stream ? r.lo[1] : r.lo[0]; }
@@ -210,6 +216,104 @@ BDLM_HD QItem q_item(const Geom& g, int tq, int64_t idx) {
   it.qtile = hi - r2 / per_kv;
   it.stream = (int)(combo % 2);
   it.head = (int)(kv * grp + combo / 2);
+  return it;
+}
+
+// Work items of a row-restricted call (one rank's rows of a multi-rank
+// deployment): only the query tiles that hold rows of the call's range, so
+// that the persistent grid's rounds stay full.  Per stream those tiles are
+// one range [t0, t1); the two ranges are merged by tile index, largest
+// first (the clean tile before the corrupted one of the same index: a
+// query tile's visible key count grows with its index in either stream),
+// and the merged list takes the place of the query tiles in the blocked,
+// longest-first order above, one stream per entry.
+BDLM_HD void range_tiles(const Geom& g, const RowRange& r, int stream, int tq, int64_t& t0, int64_t& t1) {
+  const int64_t lo = range_lo(r, stream), hi = imin64(range_hi(r, stream), g.L);
+  if (hi <= lo) {
+    t0 = t1 = 0;
+    return;
+  }
+  t0 = lo / tq;
+  t1 = cdiv64(hi, tq);
+}
+
+// Tiles of [t0, t1) at index t or above.
+BDLM_HD int64_t tiles_at_least(int64_t t0, int64_t t1, int64_t t) {
+  const int64_t lo = imax64(t0, t);
+  return t1 > lo ? t1 - lo : 0;
+}
+
+struct RowTiles {
+  int64_t a0, a1, b0, b1;  // clean and corrupted tile ranges
+  BDLM_HD int64_t at_least(int64_t t) const { return tiles_at_least(a0, a1, t) + tiles_at_least(b0, b1, t); }
+  BDLM_HD int64_t count() const { return at_least(0); }
+};
+
+BDLM_HD RowTiles row_tiles(const Geom& g, const RowRange& r, int tq) {
+  RowTiles rt;
+  range_tiles(g, r, 0, tq, rt.a0, rt.a1);
+  range_tiles(g, r, 1, tq, rt.b0, rt.b1);
+  return rt;
+}
+
+// Entry v (0 <= v < count) of the merged list: its tile and stream.  The
+// tile is the largest t with more than v entries at index t or above
+// (binary search: that count falls as t grows).
+BDLM_HD void row_tile_at(const RowTiles& rt, int64_t v, int64_t& tile, int& stream) {
+  int64_t lo = 0, hi = imax64(rt.a1, rt.b1);  // at_least(lo) > v >= at_least(hi) = 0
+  while (hi - lo > 1) {
+    const int64_t mid = lo + (hi - lo) / 2;
+    if (rt.at_least(mid) > v) lo = mid;
+    else hi = mid;
+  }
+  tile = lo;
+  const bool in_a = lo >= rt.a0 && lo < rt.a1;
+  const int64_t first = rt.at_least(lo + 1);  // entries of larger tiles come first
+  stream = (in_a && v == first) ? 0 : 1;
+}
+
+BDLM_HD int64_t q_items_rows(const Geom& g, const RowRange& r, int tq) { return row_tiles(g, r, tq).count() * g.Hq; }
+
+// Entry and head of item idx of a segment of ne merged entries: blocks of qb
+// entries, one KV head after the other inside a block (or the heads of one
+// entry together when the segment is short).
+BDLM_HD void segment_item(int64_t ne, int64_t qb, int grp, int Hq, int64_t idx, int64_t& e, int& head) {
+  if (ne < kBlockedMinQBlocks * qb) {
+    e = idx / Hq;
+    head = (int)(idx % Hq);
+    return;
+  }
+  const int64_t per_block = qb * Hq;
+  const int64_t bi = idx / per_block;
+  const int64_t e0 = bi * qb;
+  const int64_t nb = imin64(qb, ne - e0);
+  const int64_t rr = idx - bi * per_block;
+  const int64_t kv = rr / (nb * grp);
+  const int64_t r2 = rr - kv * (nb * grp);
+  e = e0 + r2 / grp;
+  head = (int)(kv * grp + r2 % grp);
+}
+
+// When the two tile ranges do not overlap the merged list is the upper range
+// followed by the lower one, and each is blocked on its own, so that no
+// block (about one grid round) mixes the long items of one with the short
+// items of the other.
+BDLM_HD QItem q_item_rows(const Geom& g, const RowRange& r, int tq, int64_t idx) {
+  const RowTiles rt = row_tiles(g, r, tq);
+  const int64_t n = rt.count();
+  const int grp = g.Hq / g.Hkv;
+  const int64_t qb = imax64(g.round_items / grp, 1);  // entries per block: about one grid round
+  const bool disjoint = rt.a1 <= rt.b0 || rt.b1 <= rt.a0;
+  const int64_t n0 = disjoint ? (rt.a0 >= rt.b1 ? rt.a1 - rt.a0 : rt.b1 - rt.b0) : n;  // first segment
+  int64_t e;
+  QItem it;
+  if (idx < n0 * g.Hq) {
+    segment_item(n0, qb, grp, g.Hq, idx, e, it.head);
+  } else {
+    segment_item(n - n0, qb, grp, g.Hq, idx - n0 * g.Hq, e, it.head);
+    e += n0;
+  }
+  row_tile_at(rt, e, it.qtile, it.stream);
   return it;
 }
 

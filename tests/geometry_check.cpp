@@ -49,7 +49,58 @@ static void check_q(const Geom& g, int tq) {
     }
 }
 
-// (key stream, KV head, key tile) items of the dK/dV list.
+// Items of a row-restricted call: exactly the (stream, head, query tile)
+// whose tile holds rows of the range, each once; the merged tile list runs
+// from the largest tile down, and inside each stream tiles never increase
+// along the list in the unblocked order.
+static void check_q_rows(const Geom& g, const RowRange& r, int tq) {
+  const int64_t nqt = cdiv64(g.L, tq);
+  std::vector<unsigned char> want((size_t)(nqt * g.Hq * 2), 0);
+  int64_t n_want = 0;
+  for (int s = 0; s < 2; ++s)
+    for (int64_t t = 0; t < nqt; ++t) {
+      const int64_t r0 = t * tq, r1 = imin64(r0 + tq, g.L);
+      if (!tile_in(r, s, r0, r1)) continue;
+      for (int h = 0; h < g.Hq; ++h) {
+        want[(size_t)((t * g.Hq + h) * 2 + s)] = 1;
+        ++n_want;
+      }
+    }
+  const int64_t n = q_items_rows(g, r, tq);
+  CHECK(n == n_want, "rows item count %lld vs %lld (L=%lld tq=%d)", (long long)n, (long long)n_want,
+        (long long)g.L, tq);
+  const RowTiles rt = row_tiles(g, r, tq);
+  int64_t prev = 1LL << 62;
+  for (int64_t v = 0; v < rt.count(); ++v) {  // merged list: largest tile first, each (tile, stream) once
+    int64_t t;
+    int s;
+    row_tile_at(rt, v, t, s);
+    const bool in = s == 0 ? (t >= rt.a0 && t < rt.a1) : (t >= rt.b0 && t < rt.b1);
+    CHECK(in && t <= prev, "merged entry %lld -> tile %lld stream %d", (long long)v, (long long)t, s);
+    if (v > 0 && t == prev) {
+      int64_t tp;
+      int sp;
+      row_tile_at(rt, v - 1, tp, sp);
+      CHECK(sp == 0 && s == 1, "equal tiles: clean first (entry %lld)", (long long)v);
+    }
+    prev = t;
+  }
+  std::vector<unsigned char> seen(want.size(), 0);
+  for (int64_t i = 0; i < n; ++i) {
+    const QItem it = q_item_rows(g, r, tq, i);
+    const bool ok = it.stream >= 0 && it.stream < 2 && it.head >= 0 && it.head < g.Hq && it.qtile >= 0 &&
+                    it.qtile < nqt;
+    CHECK(ok, "rows item %lld out of range (L=%lld tq=%d)", (long long)i, (long long)g.L, tq);
+    if (!ok) continue;
+    const size_t key = (size_t)((it.qtile * g.Hq + it.head) * 2 + it.stream);
+    CHECK(want[key], "rows item %lld outside the range (tile %lld stream %d)", (long long)i, (long long)it.qtile,
+          it.stream);
+    CHECK(!seen[key], "rows item %lld repeated", (long long)i);
+    seen[key] = 1;
+  }
+}
+
+// (key stream, KV head, key tile) items of the dK/dV list.// (key stream, KV head, key tile) items of the dK/dV list.
 static void check_kv(const Geom& g, int tk) {
   int64_t cf, cc, nn;
   kv_tile_span(g, tk, cf, cc, nn);
@@ -188,6 +239,31 @@ static void check_balance(const Geom& g, int grid, bool kv, double max_over_mean
         (long long)g.L, mx, mn, cmax);
 }
 
+// The same per-CTA balance over a row-restricted list (one rank's rows):
+// no CTA more than two items' cost above the mean.
+static void check_balance_rows(const Geom& g, const RowRange& rows, int grid, int tq) {
+  const int tk = 128;
+  const int64_t n = q_items_rows(g, rows, tq);
+  std::vector<double> tot((size_t)grid, 0.0);
+  double sum = 0.0, cmax = 0.0;
+  for (int64_t r = 0; r * grid < n; ++r)
+    for (int c = 0; c < grid; ++c) {
+      const int64_t idx = sched_item(g, r, c, grid);
+      if (idx >= n) continue;
+      const QItem it = q_item_rows(g, rows, tq, idx);
+      const int64_t r0 = it.qtile * tq;
+      const QTileRanges q = qtile_ranges(g, it.stream, r0, imin64(r0 + tq, g.L), tk);
+      const double cost = (double)((q.c1 - q.c0) + (q.n1 - q.n0));
+      tot[(size_t)c] += cost;
+      sum += cost;
+      cmax = cost > cmax ? cost : cmax;
+    }
+  double mx = 0.0;
+  for (double t : tot) mx = t > mx ? t : mx;
+  CHECK(mx <= sum / grid + 2 * cmax, "rows balance grid=%d L=%lld tq=%d rows c[%d,%d) n[%d,%d): max %.0f mean %.0f item %.0f",
+        grid, (long long)g.L, tq, rows.lo[0], rows.hi[0], rows.lo[1], rows.hi[1], mx, sum / grid, cmax);
+}
+
 int main() {
   const int64_t Ls[] = {96, 256, 1024, 8192, 16384, 32768, 131072, 262144};
   const int64_t Bs[] = {32, 128, 512};
@@ -247,6 +323,26 @@ int main() {
           check_balance(g, grid, true, 1.05);
         }
       }
+  // one rank's rows at full size: the mirror and the by-position
+  // assignments of an R-rank plan, and rows not aligned to tiles
+  for (int64_t L : {16384, 131072, 262144})
+    for (const auto& h : heads)
+      for (int R : {2, 4, 8}) {
+        Geom g{L, 512, h[0], h[1], 0, L, 1};
+        const int64_t sl = L / R;
+        for (int r = 0; r < R; ++r)
+          for (int mirror = 0; mirror < 2; ++mirror) {
+            RowRange rows;
+            rows.lo[0] = (int32_t)(r * sl);
+            rows.hi[0] = (int32_t)((r + 1) * sl);
+            const int64_t m = mirror ? R - 1 - r : r;
+            rows.lo[1] = (int32_t)(m * sl + (mirror ? 0 : 77));
+            rows.hi[1] = (int32_t)((m + 1) * sl - (mirror ? 0 : 13));
+            for (int tq : {128, 256}) check_q_rows(g, rows, tq);
+            if (L >= 131072)
+              for (int tq : {128, 256}) check_balance_rows(g, rows, 152, tq);
+          }
+      }
   // tile ranges against the mask on small shapes: tiles smaller than,
   // equal to and larger than the blocks, ragged tails, shards, no local block
   for (int64_t L : {48, 96, 160, 256})
@@ -269,6 +365,7 @@ int main() {
             g.kv_begin = L / 8; g.kv_end = L / 2;
           }
           check_ranges(g, t);
+          if (v >= 4) check_q_rows(g, g_rows, t);
           g_rows = RowRange();
         }
       }

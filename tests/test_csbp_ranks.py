@@ -27,28 +27,20 @@ def _free_port():
         return s.getsockname()[1]
 
 
-class _GlooComm:
-    def __init__(self):
-        self.rank = dist.get_rank()
-        self.world = dist.get_world_size()
+def _np(x):
+    return x.numpy() if isinstance(x, torch.Tensor) else np.asarray(x)
 
-    def all_gather(self, x):
-        t = torch.from_numpy(np.ascontiguousarray(x))
-        out = [torch.empty_like(t) for _ in range(self.world)]
-        dist.all_gather(out, t)
-        return [o.numpy() for o in out]
 
-    def sum_to_owner(self, x, owner):
-        t = torch.from_numpy(np.ascontiguousarray(x)).clone()
-        dist.reduce(t, dst=owner, op=dist.ReduceOp.SUM)
-        return t.numpy() if self.rank == owner else None
+def _t(*xs):
+    return tuple(torch.from_numpy(np.ascontiguousarray(x)) for x in xs)
 
 
 class _OracleCompute:
     """The oracle on one rank's rows: its local arrays are placed into
     full-length zero arrays (rows it does not own get zero queries, upstream
     gradients and statistics, so they contribute nothing) and the oracle's
-    partial functions compute the requested key range."""
+    partial functions compute the requested key range.  Takes and returns
+    CPU tensors, the currency of the transport."""
 
     def __init__(self, orc, local, rows, L, B, sc):
         self.orc, self.loc, self.rows, self.L, self.B, self.sc = orc, local, rows, L, B, sc
@@ -70,25 +62,25 @@ class _OracleCompute:
         Kc = np.zeros((self.L,) + self.loc["Kc"].shape[1:])
         Vc = np.zeros_like(Kc)
         if kv_data is not None:
-            Kc[kv[0]:kv[1]], Vc[kv[0]:kv[1]] = kv_data
+            Kc[kv[0]:kv[1]], Vc[kv[0]:kv[1]] = _np(kv_data[0]), _np(kv_data[1])
         Kn, Vn = (self._put("Kn", "Kn"), self._put("Vn", "Vn")) if local else (np.zeros_like(Kc), np.zeros_like(Kc))
         return Qc, Kc, Vc, Qn, Kn, Vn
 
     def fwd(self, rows, kv, kv_data, local):
         Oc, On, LSEc, LSEn = self.orc.fwd_partial(*self._inputs(kv, kv_data, local), self.B, self.sc, kv[0], kv[1],
                                                   local, blocks=self.blocks)
-        return Oc[self.crow], On[self.nrows], LSEc[:, self.crow], LSEn[:, self.nrows]
+        return _t(Oc[self.crow], On[self.nrows], LSEc[:, self.crow], LSEn[:, self.nrows])
 
     def merge(self, parts):
-        Oc, LSEc = self.orc.lse_merge([p[0] for p in parts], [p[2] for p in parts])
-        On, LSEn = self.orc.lse_merge([p[1] for p in parts], [p[3] for p in parts])
-        return Oc, On, LSEc, LSEn
+        Oc, LSEc = self.orc.lse_merge([_np(p[0]) for p in parts], [_np(p[2]) for p in parts])
+        On, LSEn = self.orc.lse_merge([_np(p[1]) for p in parts], [_np(p[3]) for p in parts])
+        return _t(Oc, On, LSEc, LSEn)
 
     def preprocess(self, O, dO):
-        return self.orc.bwd_preprocess(O, dO)
+        return _t(self.orc.bwd_preprocess(_np(O), _np(dO)))[0]
 
     def bwd(self, rows, kv, kv_data, local, stats):
-        LSEc_r, LSEn_r, Dc_r, Dn_r = stats
+        LSEc_r, LSEn_r, Dc_r, Dn_r = (_np(x) for x in stats)
         H = LSEc_r.shape[0]
         stat = lambda v, sel: (lambda a: (a.__setitem__((slice(None), sel), v), a)[1])(np.zeros((H, self.L)))
         g = self.orc.bwd_partial(*self._inputs(kv, kv_data, local), self._put("dOc", "dOc"),
@@ -96,11 +88,11 @@ class _OracleCompute:
                                  stat(Dc_r, self.crow), stat(Dn_r, self.nrows), self.B, self.sc, kv[0], kv[1], local,
                                  blocks=self.blocks)
         dQc, dKc, dVc, dQn, dKn, dVn = g
-        return (dQc[self.crow], dQn[self.nrows], dKc[kv[0]:kv[1]], dVc[kv[0]:kv[1]], dKn[self.nrows],
-                dVn[self.nrows])
+        return _t(dQc[self.crow], dQn[self.nrows], dKc[kv[0]:kv[1]], dVc[kv[0]:kv[1]], dKn[self.nrows],
+                  dVn[self.nrows])
 
 
-def _rank_main(rank, world, port, L, B, Hq, Hkv, d, out):
+def _rank_main(rank, world, port, L, B, Hq, Hkv, d, out, policy="mirror", gathered=False):
     import sys
     sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
     import oracle.bdlm_oracle as orc
@@ -109,19 +101,20 @@ def _rank_main(rank, world, port, L, B, Hq, Hkv, d, out):
     try:
         X = {k: v.astype(np.float64) for k, v in make_numpy(L, Hq, Hkv, d, seed=11).items()}
         sc = 1.0 / math.sqrt(d)
-        plan = csbp.CSBPPlan.build(L, B, world)
+        plan = csbp.CSBPPlan.build(L, B, world, policy)
         rows = plan.rows(rank)
         crow = slice(rows.c0 * B, rows.c1 * B)
         nrows = np.concatenate([np.arange(j * B, (j + 1) * B) for j in rows.noisy_blocks])
         # this rank's own data only
         local = {"Qc": X["Qc"][crow], "Kc": X["Kc"][crow], "Vc": X["Vc"][crow], "dOc": X["dOc"][crow],
                  "Qn": X["Qn"][nrows], "Kn": X["Kn"][nrows], "Vn": X["Vn"][nrows], "dOn": X["dOn"][nrows]}
-        comm = _GlooComm()
+        comm = csbp.TorchComm()
         comp = _OracleCompute(orc, local, rows, L, B, sc)
-        shards = csbp.gather_clean_kv(comm, local["Kc"], local["Vc"])
-        o = csbp.forward(plan, comm, comp, shards)
-        (dqc, dqn), (dkc, dvc), (dkn, dvn) = csbp.backward(plan, comm, comp, shards, o,
-                                                          (local["dOc"], local["dOn"]))
+        shards = csbp.gather_clean_kv(comm, *_t(local["Kc"], local["Vc"]))
+        o = [_np(x) for x in csbp.forward(plan, comm, comp, shards, gathered)]
+        (dqc, dqn), (dkc, dvc), (dkn, dvn) = csbp.backward(plan, comm, comp, shards, _t(*o),
+                                                          _t(local["dOc"], local["dOn"]), gathered)
+        dqc, dqn, dkc, dvc, dkn, dvn = (_np(x) for x in (dqc, dqn, dkc, dvc, dkn, dvn))
         names = ("Qc", "Kc", "Vc", "Qn", "Kn", "Vn")
         rf = orc.fwd_blockwise(*[X[k] for k in names], B, sc)
         rg = orc.bwd_blockwise(*[X[k] for k in names], X["dOc"], X["dOn"], B, sc)
@@ -135,13 +128,16 @@ def _rank_main(rank, world, port, L, B, Hq, Hkv, d, out):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world,L,B", [(2, 256, 16), (4, 256, 16)])
-def test_csbp_ranks_match_unsharded_oracle(world, L, B):
+@pytest.mark.parametrize("world,L,B,policy,gathered", [(2, 256, 16, "mirror", False), (4, 256, 16, "mirror", False),
+                                                        (4, 256, 16, "contiguous", False),
+                                                        (4, 256, 16, "mirror", True)])
+def test_csbp_ranks_match_unsharded_oracle(world, L, B, policy, gathered):
     Hq, Hkv, d = 2, 1, 16
     port = _free_port()
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
-    procs = [ctx.Process(target=_rank_main, args=(r, world, port, L, B, Hq, Hkv, d, q)) for r in range(world)]
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, L, B, Hq, Hkv, d, q, policy, gathered))
+             for r in range(world)]
     for p in procs:
         p.start()
     got = sorted(q.get(timeout=300) for _ in range(world))
@@ -166,3 +162,18 @@ def test_csbp_plan_covers_and_balances():
             assert (rw.n0, rw.n1) == plan.clean_shards[R - 1 - r]   # the mirror slice, contiguous
     with pytest.raises(ValueError):
         csbp.CSBPPlan.build(256, 16, 3)   # 16 blocks do not split into 3 whole-block shards
+    with pytest.raises(ValueError):
+        csbp.CSBPPlan.build(256, 16, 2, "lpt")
+
+
+def test_csbp_contiguous_ablation_is_unbalanced():
+    """The split by token position (rank r owns clean and corrupted slice r)
+    puts the most work on the last rank: slice r of n blocks holds
+    n^2 (r + 1/2) + n/2 block-units of work per stream, so the largest load
+    over the mean is (2 R n - n + 1) / (R n + 1) -> 2 - 1/R."""
+    for (L, B, R) in ((262144, 1024, 8), (131072, 512, 4), (4096, 128, 2)):
+        plan = csbp.CSBPPlan.build(L, B, R, "contiguous")
+        n = L // B // R
+        assert [plan.rows(r).n0 for r in range(R)] == [r * n for r in range(R)]
+        assert abs(plan.imbalance() - (2 * R * n - n + 1) / (R * n + 1)) < 1e-12
+        assert plan.load == sorted(plan.load)

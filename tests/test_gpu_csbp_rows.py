@@ -96,3 +96,136 @@ def test_rank_rows_validation(lib):
     with pytest.raises(m.BdlmError) as e:
         m.bdlm_attn_fwd_shard_rows(*ins, 32, 0, 256, True, (128, 64), (0, 256))
     assert e.value.status == 2
+
+
+class _ThreadComm:
+    """R ranks as host threads of one process, exchanging through shared
+    slots and a barrier.  Only the host waits: every rank's kernels go to the
+    device's default stream in the order the threads issue them, and no
+    kernel waits on another."""
+
+    class Shared:
+        def __init__(self, world):
+            import threading
+            self.world = world
+            self.slots = [None] * world
+            self.barrier = threading.Barrier(world, timeout=600)
+
+    def __init__(self, shared, rank):
+        self.s, self.rank, self.world = shared, rank, shared.world
+
+    def all_gather(self, x):
+        self.s.slots[self.rank] = x.clone()
+        self.s.barrier.wait()
+        out = list(self.s.slots)
+        self.s.barrier.wait()
+        return out
+
+    def sum_to_owner(self, x, owner):
+        self.s.slots[self.rank] = x.clone()
+        self.s.barrier.wait()
+        res = None
+        if self.rank == owner:   # summed in rank order
+            res = self.s.slots[0].clone()
+            for t in self.s.slots[1:]:
+                res += t
+        self.s.barrier.wait()
+        return res
+
+
+@pytest.mark.parametrize("L,B,R,Hq,Hkv,d,policy,gathered", [
+    (1024, 64, 4, 4, 2, 128, "mirror", False),
+    (2048, 64, 8, 2, 1, 128, "mirror", False),
+    (1024, 32, 4, 2, 2, 64, "contiguous", False),
+    (2048, 64, 8, 2, 1, 128, "mirror", True),
+    (768, 32, 4, 3, 1, 64, "contiguous", True),
+])
+def test_csbp_driver_on_kernels(lib, L, B, R, Hq, Hkv, d, policy, gathered):
+    """The per-rank CSBP driver (csbp.forward / csbp.backward) with
+    csbp.KernelCompute on every rank: each rank starts from its own rows
+    only, clean K/V are all-gathered, clean dK/dV summed onto the shard
+    owners; per-shard partials or one call over the gathered sequence.  The
+    reassembled outputs and gradients match the fp64 oracle."""
+    import threading
+
+    m = lib
+    X = make_numpy(L, Hq, Hkv, d, seed=L + R + 7)
+    X64 = {k: v.astype(np.float64) for k, v in X.items()}
+    dev = {k: to_dev(v, torch) for k, v in X.items()}
+    sc = 1.0 / math.sqrt(d)
+    plan = csbp.CSBPPlan.build(L, B, R, policy)
+    shared = _ThreadComm.Shared(R)
+    results, errors = [None] * R, []
+
+    def rank_job(r):
+        try:
+            rw = plan.rows(r)
+            c, n = slice(rw.c0 * B, rw.c1 * B), slice(rw.n0 * B, rw.n1 * B)
+            local = {k: dev[k][c].clone() for k in ("Qc", "Kc", "Vc", "dOc")}
+            local.update({k: dev[k][n].clone() for k in ("Qn", "Kn", "Vn", "dOn")})
+            comm = _ThreadComm(shared, r)
+            comp = csbp.KernelCompute(m, plan, r, local, sc)
+            shards = csbp.gather_clean_kv(comm, local["Kc"], local["Vc"])
+            o = csbp.forward(plan, comm, comp, shards, gathered)
+            g = csbp.backward(plan, comm, comp, shards, o, (local["dOc"], local["dOn"]), gathered)
+            torch.cuda.synchronize()
+            results[r] = (o, g)
+        except BaseException as e:  # release the other ranks, then report
+            errors.append(e)
+            shared.barrier.abort()
+
+    threads = [threading.Thread(target=rank_job, args=(r,)) for r in range(R)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=900)
+    assert not errors, errors[0]
+    f32 = dict(dtype=torch.float32, device="cuda")
+    Oc, On = torch.zeros((L, Hq, d), **f32), torch.zeros((L, Hq, d), **f32)
+    LSEc, LSEn = torch.zeros((Hq, L), **f32), torch.zeros((Hq, L), **f32)
+    dQc, dQn = torch.zeros((L, Hq, d), **f32), torch.zeros((L, Hq, d), **f32)
+    dKc, dVc, dKn, dVn = (torch.zeros((L, Hkv, d), **f32) for _ in range(4))
+    for r in range(R):
+        rw = plan.rows(r)
+        c, n = slice(rw.c0 * B, rw.c1 * B), slice(rw.n0 * B, rw.n1 * B)
+        (oc, on, lc, ln), ((gqc, gqn), (gkc, gvc), (gkn, gvn)) = results[r]
+        Oc[c], On[n], LSEc[:, c], LSEn[:, n] = oc, on, lc, ln
+        dQc[c], dQn[n], dKc[c], dVc[c], dKn[n], dVn[n] = gqc, gqn, gkc, gvc, gkn, gvn
+    ref = orc.fwd_blockwise(*[X64[k] for k in NAMES[:6]], B, sc)
+    check_rel("Oc (driver)", to_np(Oc), ref[0])
+    check_rel("On (driver)", to_np(On), ref[1])
+    check_lse("LSEc (driver)", to_np(LSEc), ref[2])
+    check_lse("LSEn (driver)", to_np(LSEn), ref[3])
+    gref = orc.bwd_blockwise(*[X64[k] for k in NAMES], B, sc)
+    for name, g, r_ in zip(("dQc", "dKc", "dVc", "dQn", "dKn", "dVn"), (dQc, dKc, dVc, dQn, dKn, dVn), gref):
+        check_rel(f"{name} (driver)", to_np(g), r_)
+
+
+def test_rank_rows_empty_and_one_sided(lib):
+    """A call with no rows writes nothing and adds nothing; a call with
+    rows of one stream only matches the oracle on those rows."""
+    m = lib
+    L, B, Hq, Hkv, d = 512, 32, 2, 1, 64
+    X = make_numpy(L, Hq, Hkv, d, seed=5)
+    X64 = {k: v.astype(np.float64) for k, v in X.items()}
+    dev = {k: to_dev(v, torch) for k, v in X.items()}
+    ins = [dev[k] for k in NAMES[:6]]
+    sc = 1.0 / math.sqrt(d)
+    o = m.bdlm_attn_fwd_shard_rows(*ins, B, 0, L, True, (0, 0), (0, 0), sc)
+    assert not o[0].any() and not o[1].any()
+    assert torch.isneginf(o[2]).all() and torch.isneginf(o[3]).all()
+    f = m.bdlm_attn_fwd(*ins, B, sc, o_dtype=torch.float32)
+    Dc, Dn = m.bdlm_bwd_preprocess(f[0], dev["dOc"]), m.bdlm_bwd_preprocess(f[1], dev["dOn"])
+    z = lambda H: torch.zeros((L, H, d), dtype=torch.float32, device="cuda")
+    acc = (z(Hq), z(Hq), z(Hkv), z(Hkv), z(Hkv), z(Hkv))
+    m.bdlm_attn_bwd_shard_rows(*ins, dev["dOc"], dev["dOn"], f[2], f[3], Dc, Dn, B, 0, L, True, (0, 0), (0, 0),
+                               *acc, sc)
+    assert not any(a.any() for a in acc)
+    ref = orc.fwd_blockwise(*[X64[k] for k in NAMES[:6]], B, sc)
+    o = m.bdlm_attn_fwd_shard_rows(*ins, B, 0, L, True, (0, 0), (100, 400), sc)   # corrupted rows only
+    check_rel("On rows 100..400", to_np(o[1])[100:400], ref[1][100:400])
+    check_lse("LSEn rows 100..400", to_np(o[3])[:, 100:400], ref[3][:, 100:400])
+    assert not o[0].any() and not o[1][:100].any() and not o[1][400:].any()
+    o = m.bdlm_attn_fwd_shard_rows(*ins, B, 0, L, True, (37, 300), (0, 0), sc)    # clean rows only
+    check_rel("Oc rows 37..300", to_np(o[0])[37:300], ref[0][37:300])
+    assert not o[1].any() and not o[0][:37].any() and not o[0][300:].any()
