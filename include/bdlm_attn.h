@@ -276,6 +276,44 @@ bdlm_status bdlm_attn_bwd_shard_rows(const void* Qc, const void* Kc, const void*
                                      float* dKc_acc, float* dVc_acc, float* dKn_acc, float* dVn_acc,
                                      void* workspace, size_t ws_bytes, bdlm_stream stream);
 
+/* ---- One rank's rows with rank-local tensors (multi-rank CSBP) -----------
+ * The same computation as bdlm_attn_fwd_shard_rows / bdlm_attn_bwd_shard_rows,
+ * with every tensor holding only what the rank holds (so that no rank stores
+ * the whole sequence: evolve.pub FAQ on CSBP, memory):
+ *  - clean-stream row tensors hold rows [rows_c_begin, rows_c_end) only:
+ *    Qc, dOc, Op_c, dQc_acc as [rows_c_end - rows_c_begin, H, d], LSEp_c,
+ *    LSEc, Dc as [Hq, rows_c_end - rows_c_begin];
+ *  - corrupted-stream tensors hold rows [rows_n_begin, rows_n_end) only: Qn,
+ *    Kn, Vn, dOn, Op_n, LSEp_n, LSEn, Dn, dQn_acc, dKn_acc, dVn_acc (with the
+ *    local partial, include_local, this range must be whole blocks of B, or
+ *    end at L: a corrupted row reads its whole block's keys);
+ *  - Kc, Vc, dKc_acc, dVc_acc hold the clean keys [kv_begin, kv_end) only
+ *    (one shard as received, or the whole gathered clean sequence).
+ * L is the full sequence length; row and key indices are global.  A tensor
+ * of a stream with no rows may be any valid 16-byte-aligned device buffer
+ * (it is not read).  Errors as for the full-length calls, plus
+ * BDLM_ERR_SHAPE for a corrupted range that is not whole blocks. */
+bdlm_status bdlm_attn_fwd_rank(const void* Qc, const void* Kc, const void* Vc,
+                               const void* Qn, const void* Kn, const void* Vn,
+                               int64_t L, int64_t B, int Hq, int Hkv, int d, float scale,
+                               int64_t kv_begin, int64_t kv_end, int include_local,
+                               int64_t rows_c_begin, int64_t rows_c_end,
+                               int64_t rows_n_begin, int64_t rows_n_end,
+                               float* Op_c, float* Op_n, float* LSEp_c, float* LSEp_n,
+                               void* workspace, size_t ws_bytes, bdlm_stream stream);
+
+bdlm_status bdlm_attn_bwd_rank(const void* Qc, const void* Kc, const void* Vc,
+                               const void* Qn, const void* Kn, const void* Vn,
+                               const void* dOc, const void* dOn,
+                               const float* LSEc, const float* LSEn, const float* Dc, const float* Dn,
+                               int64_t L, int64_t B, int Hq, int Hkv, int d, float scale,
+                               int64_t kv_begin, int64_t kv_end, int include_local,
+                               int64_t rows_c_begin, int64_t rows_c_end,
+                               int64_t rows_n_begin, int64_t rows_n_end,
+                               float* dQc_acc, float* dQn_acc,
+                               float* dKc_acc, float* dVc_acc, float* dKn_acc, float* dVn_acc,
+                               void* workspace, size_t ws_bytes, bdlm_stream stream);
+
 /* ---- Packed variable-length batch (batch > 1) ---------------------------
  * Several independent two-stream problems in one call, for batches of
  * sequences (the pages tune the batch size alongside the parallelism:

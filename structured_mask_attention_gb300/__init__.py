@@ -19,6 +19,7 @@ import re
 __all__ = [
     "BdlmError", "load_library", "bdlm_workspace_size", "bdlm_attn_fwd", "bdlm_attn_fwd_shard",
     "bdlm_attn_fwd_shard_refmax", "bdlm_attn_fwd_shard_rows", "bdlm_attn_bwd_shard_rows",
+    "bdlm_attn_fwd_rank", "bdlm_attn_bwd_rank",
     "bdlm_lse_merge", "bdlm_bwd_preprocess", "bdlm_attn_bwd", "bdlm_attn_bwd_noalloc", "bdlm_attn_bwd_shard",
     "bdlm_worklist", "bdlm_workspace_size_varlen", "bdlm_attn_fwd_varlen", "bdlm_attn_bwd_varlen",
     "bdlm_sync_status", "bdlm_watchdog_selftest", "bdlm_sync_status_noalloc", "bdlm_watchdog_selftest_noalloc",
@@ -68,6 +69,10 @@ _SIGS = {
                                  + [_P] * 5 + [_SZ, _P]),
     "bdlm_attn_bwd_shard_rows": (_I, [_P] * 12 + [_I64, _I64, _I, _I, _I, _F, _I64, _I64, _I] + [_I64] * 4
                                  + [_P] * 7 + [_SZ, _P]),
+    "bdlm_attn_fwd_rank": (_I, [_P] * 6 + [_I64, _I64, _I, _I, _I, _F, _I64, _I64, _I] + [_I64] * 4
+                           + [_P] * 5 + [_SZ, _P]),
+    "bdlm_attn_bwd_rank": (_I, [_P] * 12 + [_I64, _I64, _I, _I, _I, _F, _I64, _I64, _I] + [_I64] * 4
+                           + [_P] * 7 + [_SZ, _P]),
     "bdlm_worklist": (_I64, [_I64, _I64, _I, _I, _I, _I, _I64, _I64, _I, _P, _I64]),
     "bdlm_workspace_size_varlen": (_SZ, [_I, _P, _I, _I, _I, _I]),
     "bdlm_attn_fwd_varlen": (_I, [_P] * 6 + [_P, _I, _I64, _I, _I, _I, _F, _P, _P, _I, _P, _P, _P, _SZ, _P]),
@@ -390,6 +395,75 @@ def bdlm_attn_bwd_shard_rows(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, D
         _ptr(Dc), _ptr(Dn), L, B, Hq, Hkv, d, scale, kv_begin, kv_end, int(bool(include_local)),
         int(rows_c[0]), int(rows_c[1]), int(rows_n[0]), int(rows_n[1]),
         _ptr(dQc_acc), _ptr(dQn_acc), _ptr(dKc_acc), _ptr(dVc_acc), _ptr(dKn_acc), _ptr(dVn_acc),
+        _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def _held(t, n, name):
+    """A rank-local tensor must hold exactly n rows."""
+    if t.shape[0] != n:
+        raise ValueError(f"{name} holds {t.shape[0]} rows, the call's range has {n}")
+
+
+def _ptr_held(t, spare):
+    """A tensor with no rows is not read: a spare buffer stands in for its (null) address."""
+    return _ptr(t) if t.numel() > 0 else _ptr(spare)
+
+
+def bdlm_attn_fwd_rank(Qc, Kc, Vc, Qn, Kn, Vn, L: int, B: int, kv_begin: int, kv_end: int, include_local: bool,
+                       rows_c, rows_n, scale: float | None = None, out=None, workspace=None, stream=None):
+    """One rank's rows with rank-local tensors: Qc holds clean rows
+    ``rows_c`` = (begin, end) only, Qn / Kn / Vn the corrupted rows
+    ``rows_n`` only, Kc / Vc the clean keys [kv_begin, kv_end) only; L is the
+    full length.  Returns the partial (Op_c, Op_n, LSEp_c, LSEp_n) of those
+    rows (fp32, [rows, Hq, d] and [Hq, rows])."""
+    torch = _torch()
+    _check_inputs(Qc, Kc, Vc, Qn, Kn, Vn)
+    nc, nn = rows_c[1] - rows_c[0], rows_n[1] - rows_n[0]
+    for t, n, name in ((Qc, nc, "Qc"), (Qn, nn, "Qn"), (Kn, nn, "Kn"), (Vn, nn, "Vn"),
+                       (Kc, kv_end - kv_begin, "Kc"), (Vc, kv_end - kv_begin, "Vc")):
+        _held(t, n, name)
+    Hq, d, Hkv = Qc.shape[1], Qc.shape[2], Kn.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dev = Qc.device
+    if out is None:
+        out = (torch.zeros((nc, Hq, d), dtype=torch.float32, device=dev),
+               torch.zeros((nn, Hq, d), dtype=torch.float32, device=dev),
+               torch.full((Hq, nc), float("-inf"), dtype=torch.float32, device=dev),
+               torch.full((Hq, nn), float("-inf"), dtype=torch.float32, device=dev))
+    ws = _workspace(OP_FWD_SHARD, L, B, Hq, Hkv, d, dev, workspace)
+    spare = torch.empty(256, dtype=torch.uint8, device=dev)
+    _check(load_library().bdlm_attn_fwd_rank(
+        *[_ptr_held(t, spare) for t in (Qc, Kc, Vc, Qn, Kn, Vn)], L, B, Hq, Hkv, d, scale, kv_begin, kv_end,
+        int(bool(include_local)), int(rows_c[0]), int(rows_c[1]), int(rows_n[0]), int(rows_n[1]),
+        *[_ptr_held(t, spare) for t in out], _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def bdlm_attn_bwd_rank(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn, L: int, B: int, kv_begin: int,
+                       kv_end: int, include_local: bool, rows_c, rows_n, dQc_acc, dQn_acc, dKc_acc, dVc_acc,
+                       dKn_acc, dVn_acc, scale: float | None = None, workspace=None, stream=None):
+    """One rank's rows of the backward with rank-local tensors (as
+    bdlm_attn_fwd_rank; LSE, D of its rows as [Hq, rows]): adds the rows' dQ
+    and their contributions to the call's keys' dK, dV into the fp32
+    accumulators ([rows, Hq, d] for dQ, [keys, Hkv, d] for dK / dV)."""
+    torch = _torch()
+    _check_inputs(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn)
+    nc, nn, nk = rows_c[1] - rows_c[0], rows_n[1] - rows_n[0], kv_end - kv_begin
+    for t, n, name in ((Qc, nc, "Qc"), (dOc, nc, "dOc"), (dQc_acc, nc, "dQc_acc"), (Qn, nn, "Qn"), (Kn, nn, "Kn"),
+                       (Vn, nn, "Vn"), (dOn, nn, "dOn"), (dQn_acc, nn, "dQn_acc"), (dKn_acc, nn, "dKn_acc"),
+                       (dVn_acc, nn, "dVn_acc"), (Kc, nk, "Kc"), (Vc, nk, "Vc"), (dKc_acc, nk, "dKc_acc"),
+                       (dVc_acc, nk, "dVc_acc")):
+        _held(t, n, name)
+    Hq, d, Hkv = Qc.shape[1], Qc.shape[2], Kn.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dev = Qc.device
+    ws = _workspace(OP_BWD_SHARD, L, B, Hq, Hkv, d, dev, workspace)
+    spare = torch.empty(256, dtype=torch.uint8, device=dev)
+    ts = (Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn)
+    acc = (dQc_acc, dQn_acc, dKc_acc, dVc_acc, dKn_acc, dVn_acc)
+    _check(load_library().bdlm_attn_bwd_rank(
+        *[_ptr_held(t, spare) for t in ts], L, B, Hq, Hkv, d, scale, kv_begin, kv_end, int(bool(include_local)),
+        int(rows_c[0]), int(rows_c[1]), int(rows_n[0]), int(rows_n[1]), *[_ptr_held(t, spare) for t in acc],
         _ptr(ws), ws.numel(), _stream(stream)))
 
 

@@ -54,17 +54,16 @@ object passed in by the caller:
   ``sum_to_owner(x, owner) -> x or None`` (the sum over ranks, on the owner).
 
 On GB300s the compute object is ``KernelCompute``: the library's
-tensor-core kernels restricted to a rank's rows (`bdlm_attn_fwd_shard_rows`,
-`bdlm_attn_bwd_shard_rows`: row ranges per stream, gradients accumulated
-over calls), and the transport is ``TorchComm``, NCCL over NVLink through
+tensor-core kernels restricted to a rank's rows, on rank-local tensors
+(`bdlm_attn_fwd_rank`, `bdlm_attn_bwd_rank`: row ranges per stream,
+gradients accumulated over calls), and the transport is ``TorchComm``, NCCL over NVLink through
 torch.distributed (no TMA multicast, and no kernel reads a peer's memory:
 shards are copied into local HBM first).  Checked: the plan and this driver
 with gloo ranks on the CPU and the fp64 oracle as the compute object
 (tests/test_csbp_ranks.py); the driver with ``KernelCompute`` for every rank
 on one GPU, the ranks as host threads exchanging through host-side
-collectives (tests/test_gpu_csbp_rows.py).  The kernels index full-length
-tensors, so a rank holds its rows in full-length buffers.  No run on
-several GPUs exists.
+collectives (tests/test_gpu_csbp_rows.py).  A rank holds only its own rows
+and the clean K / V it receives.  No run on several GPUs exists.
 """
 from __future__ import annotations
 
@@ -227,77 +226,56 @@ class TorchComm:
 
 
 class KernelCompute:
-    """One rank's compute on its GPU through the library's row-restricted
-    calls (``bdlm_attn_fwd_shard_rows``, ``bdlm_lse_merge``,
-    ``bdlm_bwd_preprocess``, ``bdlm_attn_bwd_shard_rows``).
+    """One rank's compute on its GPU through the library's rank-local calls
+    (``bdlm_attn_fwd_rank``, ``bdlm_lse_merge``, ``bdlm_bwd_preprocess``,
+    ``bdlm_attn_bwd_rank``).
 
     ``local`` holds the rank's own tensors on the device: "Qc", "Kc", "Vc",
     "dOc" are the rows of its clean shard, "Qn", "Kn", "Vn", "dOn" the rows of
-    its corrupted blocks ([rows, H, d], bf16).  The kernels index
-    full-length tensors, so they are placed into length-L buffers (zero
-    elsewhere; rows outside the rank's ranges are never read as queries, and
-    keys outside a call's key set are never read), and each clean shard
-    received from the exchange is copied into its key range before the
-    calls that use it.  Results are returned for the rank's rows only."""
+    its corrupted blocks ([rows, H, d], bf16).  Nothing of length L is held:
+    the calls take the rank's rows as they are, each clean shard (or the whole
+    gathered clean sequence) as received, and return results for the rank's
+    rows and the call's keys only."""
 
     def __init__(self, lib, plan: CSBPPlan, rank: int, local: dict, scale: float):
         import torch
         self.lib, self.plan, self.scale = lib, plan, scale
-        L, B = plan.L, plan.B
+        B = plan.B
         rw = plan.rows(rank)
         self.rc, self.rn = (rw.c0 * B, rw.c1 * B), (rw.n0 * B, rw.n1 * B)
+        self.loc = {k: v.contiguous() for k, v in local.items()}
+        kn = self.loc["Kn"]
+        self.no_keys = torch.empty((0,) + tuple(kn.shape[1:]), dtype=kn.dtype, device=kn.device)
 
-        def full(name, rng):
-            t = local[name]
-            buf = torch.zeros((L,) + tuple(t.shape[1:]), dtype=t.dtype, device=t.device)
-            buf[rng[0]:rng[1]] = t
-            return buf
-
-        self.Qc, self.Qn = full("Qc", self.rc), full("Qn", self.rn)
-        self.Kn, self.Vn = full("Kn", self.rn), full("Vn", self.rn)
-        self.dOc, self.dOn = full("dOc", self.rc), full("dOn", self.rn)
-        self.Kc = torch.zeros((L,) + tuple(local["Kc"].shape[1:]), dtype=local["Kc"].dtype,
-                              device=local["Kc"].device)
-        self.Vc = torch.zeros_like(self.Kc)
-
-    def _place(self, kv, kv_data):
-        if kv_data is not None:
-            self.Kc[kv[0]:kv[1]] = kv_data[0]
-            self.Vc[kv[0]:kv[1]] = kv_data[1]
-
-    def _ins(self):
-        return self.Qc, self.Kc, self.Vc, self.Qn, self.Kn, self.Vn
+    def _kv(self, kv_data):
+        if kv_data is None:
+            return self.no_keys, self.no_keys
+        return kv_data[0].contiguous(), kv_data[1].contiguous()
 
     def fwd(self, rows, kv, kv_data, local):
-        self._place(kv, kv_data)
-        return self.lib.bdlm_attn_fwd_shard_rows(*self._ins(), self.plan.B, kv[0], kv[1], local, self.rc, self.rn,
-                                                 self.scale)
+        Kc, Vc = self._kv(kv_data)
+        x = self.loc
+        return self.lib.bdlm_attn_fwd_rank(x["Qc"], Kc, Vc, x["Qn"], x["Kn"], x["Vn"], self.plan.L, self.plan.B,
+                                           kv[0], kv[1], local, self.rc, self.rn, self.scale)
 
     def merge(self, parts):
         import torch
         oc, lc = self.lib.bdlm_lse_merge([p[0] for p in parts], [p[2] for p in parts], o_dtype=torch.float32)
         on, ln = self.lib.bdlm_lse_merge([p[1] for p in parts], [p[3] for p in parts], o_dtype=torch.float32)
-        (a, b), (c, d) = self.rc, self.rn
-        return oc[a:b], on[c:d], lc[:, a:b].contiguous(), ln[:, c:d].contiguous()
+        return oc, on, lc, ln
 
     def preprocess(self, O, dO):
         return self.lib.bdlm_bwd_preprocess(O.contiguous(), dO.contiguous())
 
     def bwd(self, rows, kv, kv_data, local, stats):
         import torch
-        self._place(kv, kv_data)
-        L = self.plan.L
-        (a, b), (c, d) = self.rc, self.rn
-
-        def stat(v, lo, hi):
-            full_ = torch.zeros((v.shape[0], L), dtype=torch.float32, device=v.device)
-            full_[:, lo:hi] = v
-            return full_
-
-        LSEc, LSEn, Dc, Dn = stat(stats[0], a, b), stat(stats[1], c, d), stat(stats[2], a, b), stat(stats[3], c, d)
-        z = lambda t: torch.zeros(t.shape, dtype=torch.float32, device=t.device)
-        acc = (z(self.Qc), z(self.Qn), z(self.Kc), z(self.Vc), z(self.Kn), z(self.Vn))
-        self.lib.bdlm_attn_bwd_shard_rows(*self._ins(), self.dOc, self.dOn, LSEc, LSEn, Dc, Dn, self.plan.B,
-                                          kv[0], kv[1], local, self.rc, self.rn, *acc, self.scale)
-        dQc, dQn, dKc, dVc, dKn, dVn = acc
-        return dQc[a:b], dQn[c:d], dKc[kv[0]:kv[1]], dVc[kv[0]:kv[1]], dKn[c:d], dVn[c:d]
+        Kc, Vc = self._kv(kv_data)
+        x = self.loc
+        f32 = dict(dtype=torch.float32, device=x["Qc"].device)
+        z = lambda t: torch.zeros(t.shape, **f32)
+        acc = (z(x["Qc"]), z(x["Qn"]), z(Kc), z(Vc), z(x["Kn"]), z(x["Vn"]))
+        LSEc, LSEn, Dc, Dn = (t.contiguous() for t in stats)
+        self.lib.bdlm_attn_bwd_rank(x["Qc"], Kc, Vc, x["Qn"], x["Kn"], x["Vn"], x["dOc"], x["dOn"], LSEc, LSEn, Dc,
+                                    Dn, self.plan.L, self.plan.B, kv[0], kv[1], local, self.rc, self.rn, *acc,
+                                    self.scale)
+        return acc

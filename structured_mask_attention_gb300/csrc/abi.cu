@@ -241,15 +241,25 @@ bdlm_status finish(cudaError_t e, int launches, const char* what) {
 }
 
 // Query-row ranges of a call: rows[0..1] the clean rows, rows[2..3] the
-// corrupted rows, [begin, end) each (validated by the caller).
-RowRange row_range(const int64_t* rows) {
+// corrupted rows, [begin, end) each (validated by the caller).  local: the
+// call's tensors hold only its rows (and the clean K / V only the keys
+// [kv_begin, kv_end)); else they are full length.
+RowRange row_range(const int64_t* rows, int64_t L, bool local, int64_t kv_begin, int64_t kv_end) {
   RowRange r;
-  r.lo[0] = (int32_t)rows[0];
-  r.hi[0] = (int32_t)rows[1];
-  r.lo[1] = (int32_t)rows[2];
-  r.hi[1] = (int32_t)rows[3];
+  for (int s = 0; s < 2; ++s) {
+    r.lo[s] = (int32_t)rows[2 * s];
+    r.hi[s] = (int32_t)rows[2 * s + 1];
+    r.base[s] = local ? (int32_t)rows[2 * s] : 0;
+    r.len[s] = (int32_t)(local ? rows[2 * s + 1] - rows[2 * s] : L);
+  }
+  r.kbase = local ? (int32_t)kv_begin : 0;
+  r.klen = (int32_t)(local ? kv_end - kv_begin : L);
   return r;
 }
+
+// Rows a tensor map covers: the held rows (at least one, so that a map over
+// a stream with no rows, which no kernel reads, still encodes).
+int64_t map_rows(int64_t held) { return held > 0 ? held : 1; }
 
 bdlm_status check_rows(const int64_t* rows, int64_t L) {
   for (int s = 0; s < 2; ++s)
@@ -263,18 +273,21 @@ bdlm_status fwd_common(const void* Qc, const void* Kc, const void* Vc, const voi
                        const void* Vn, int64_t L, int64_t B, int Hq, int Hkv, int d, float scale, int64_t kv_begin,
                        int64_t kv_end, int include_local, void* Oc, void* On, int o_f32, float* LSEc, float* LSEn,
                        void* ws, size_t ws_bytes, cudaStream_t st, const VarlenTabs* vt = nullptr,
-                       const FwdRef* ref = nullptr, const int64_t* rows = nullptr) {
+                       const FwdRef* ref = nullptr, const RowRange* rows = nullptr) {
   DeviceInfo info;
   BDLM_CHECK(device_info(info));
   EncodeTiledFn enc;
   BDLM_CHECK(get_encoder(enc));
   FwdMaps maps;
-  BDLM_CHECK(encode_lhd(enc, &maps.Qc, Qc, L, Hq, d, kFwdTileQ));
-  BDLM_CHECK(encode_lhd(enc, &maps.Qn, Qn, L, Hq, d, kFwdTileQ));
-  BDLM_CHECK(encode_lhd(enc, &maps.Kc, Kc, L, Hkv, d, kFwdTileK));
-  BDLM_CHECK(encode_lhd(enc, &maps.Kn, Kn, L, Hkv, d, kFwdTileK));
-  BDLM_CHECK(encode_lhd(enc, &maps.Vc, Vc, L, Hkv, d, kFwdTileK));
-  BDLM_CHECK(encode_lhd(enc, &maps.Vn, Vn, L, Hkv, d, kFwdTileK));
+  // rows held by each tensor (a row-restricted call may hold only its own)
+  const int64_t hc = rows ? map_rows(rows->len[0]) : L, hn = rows ? map_rows(rows->len[1]) : L;
+  const int64_t hk = rows ? map_rows(rows->klen) : L;
+  BDLM_CHECK(encode_lhd(enc, &maps.Qc, Qc, hc, Hq, d, kFwdTileQ));
+  BDLM_CHECK(encode_lhd(enc, &maps.Qn, Qn, hn, Hq, d, kFwdTileQ));
+  BDLM_CHECK(encode_lhd(enc, &maps.Kc, Kc, hk, Hkv, d, kFwdTileK));
+  BDLM_CHECK(encode_lhd(enc, &maps.Kn, Kn, hn, Hkv, d, kFwdTileK));
+  BDLM_CHECK(encode_lhd(enc, &maps.Vc, Vc, hk, Hkv, d, kFwdTileK));
+  BDLM_CHECK(encode_lhd(enc, &maps.Vn, Vn, hn, Hkv, d, kFwdTileK));
   FwdParams p;
   p.g = Geom{L, B, Hq, Hkv, kv_begin, kv_end, include_local ? 1 : 0};
   p.g.naive_order = naive_schedule();
@@ -285,15 +298,14 @@ bdlm_status fwd_common(const void* Qc, const void* Kc, const void* Vc, const voi
   p.o_f32 = o_f32;
   p.LSEc = LSEc;
   p.LSEn = LSEn;
-  const RowRange rr = rows ? row_range(rows) : RowRange();
   // a row-restricted call lists only the query tiles that hold its rows
-  p.n_items = vt ? vt->n_q : rows ? q_items_rows(p.g, rr, kFwdItemRows) : q_items(p.g, kFwdItemRows);
+  p.n_items = vt ? vt->n_q : rows ? q_items_rows(p.g, *rows, kFwdItemRows) : q_items(p.g, kFwdItemRows);
   p.status = static_cast<uint32_t*>(ws);
   p.limit_ns = wait_limit_ns();
   BDLM_CHECK(clear_status(ws, st));
   int launches = 0;
   ScopedKernelTimer tm(K_FWD, st);
-  cudaError_t e = launch_fwd(maps, p, vt, ref, rows ? &rr : nullptr, d, info.sms, st, &launches);
+  cudaError_t e = launch_fwd(maps, p, vt, ref, rows, d, info.sms, st, &launches);
   tm.stop();
   return finish(e, launches, "forward launch");
 }
@@ -316,6 +328,7 @@ BwdParams bwd_params(const void* Qc, const void* Kc, const void* Vc, const void*
   p.g_f32 = 0;
   p.dq_accumulate = 0;
   p.dkv_accumulate = 0;
+  p.rows_call = 0;
   return p;
 }
 
@@ -328,11 +341,16 @@ cudaError_t launch_backward_passes(const BwdParams& p, const DeviceInfo& info, v
   BwdMaps m;
   const int64_t L = p.g.L;
   const int Hq = p.g.Hq, Hkv = p.g.Hkv, d = p.d;
-  struct E { CUtensorMap* map; const void* ptr; int H; };
-  const E list[8] = {{&m.Qc, p.Qc, Hq},   {&m.Qn, p.Qn, Hq},   {&m.dOc, p.dOc, Hq}, {&m.dOn, p.dOn, Hq},
-                     {&m.Kc, p.Kc, Hkv}, {&m.Kn, p.Kn, Hkv}, {&m.Vc, p.Vc, Hkv},  {&m.Vn, p.Vn, Hkv}};
+  // rows held by each tensor (a row-restricted call may hold only its own)
+  const bool rc = p.rows_call != 0;
+  const int64_t hc = rc ? map_rows(p.rows.len[0]) : L, hn = rc ? map_rows(p.rows.len[1]) : L;
+  const int64_t hk = rc ? map_rows(p.rows.klen) : L;
+  struct E { CUtensorMap* map; const void* ptr; int H; int64_t rows; };
+  const E list[8] = {{&m.Qc, p.Qc, Hq, hc},   {&m.Qn, p.Qn, Hq, hn},   {&m.dOc, p.dOc, Hq, hc},
+                     {&m.dOn, p.dOn, Hq, hn}, {&m.Kc, p.Kc, Hkv, hk},  {&m.Kn, p.Kn, Hkv, hn},
+                     {&m.Vc, p.Vc, Hkv, hk},  {&m.Vn, p.Vn, Hkv, hn}};
   for (const E& x : list)
-    if ((*vstatus = encode_lhd(enc, x.map, x.ptr, L, x.H, d, kBwdTile)) != BDLM_OK) return cudaSuccess;
+    if ((*vstatus = encode_lhd(enc, x.map, x.ptr, x.rows, x.H, d, kBwdTile)) != BDLM_OK) return cudaSuccess;
   uint32_t* status = static_cast<uint32_t*>(ws);
   cudaError_t e;
   {
@@ -622,6 +640,77 @@ bdlm_status bdlm_attn_fwd_shard_refmax(const void* Qc, const void* Kc, const voi
   });
 }
 
+}  // extern "C"
+
+namespace {
+
+// The clean key range and, for rank-local tensors with the local partial,
+// whole corrupted blocks (a corrupted row reads its whole block's keys, which
+// the rank's corrupted K / V must hold).
+bdlm_status check_rows_call(int64_t L, int64_t B, int64_t kv_begin, int64_t kv_end, int include_local,
+                            const int64_t* rows, bool local) {
+  if (kv_begin < 0 || kv_end < kv_begin || kv_end > L)
+    return fail(BDLM_ERR_SHAPE, "clean key range [%lld, %lld) is not inside [0, %lld)", (long long)kv_begin,
+                (long long)kv_end, (long long)L);
+  BDLM_CHECK(check_rows(rows, L));
+  if (local && include_local && rows[3] > rows[2] && (rows[2] % B || (rows[3] % B && rows[3] != L)))
+    return fail(BDLM_ERR_SHAPE,
+                "rank-local corrupted rows [%lld, %lld) must be whole blocks of %lld (their keys are read)",
+                (long long)rows[2], (long long)rows[3], (long long)B);
+  return BDLM_OK;
+}
+
+bdlm_status fwd_rows_impl(const char* name, const void* Qc, const void* Kc, const void* Vc, const void* Qn,
+                          const void* Kn, const void* Vn, int64_t L, int64_t B, int Hq, int Hkv, int d, float scale,
+                          int64_t kv_begin, int64_t kv_end, int include_local, const int64_t* rows, bool local,
+                          float* Op_c, float* Op_n, float* LSEp_c, float* LSEp_n, void* workspace, size_t ws_bytes,
+                          bdlm_stream stream) {
+  BDLM_CHECK(check_shape(L, B, Hq, Hkv, d));
+  BDLM_CHECK(check_scale(scale));
+  BDLM_CHECK(check_rows_call(L, B, kv_begin, kv_end, include_local, rows, local));
+  BDLM_CHECK(check_ptrs(name, {Qc, Kc, Vc, Qn, Kn, Vn, Op_c, Op_n, LSEp_c, LSEp_n}));
+  BDLM_CHECK(check_ws(workspace, ws_bytes, bdlm_workspace_size(BDLM_OP_FWD_SHARD, L, B, Hq, Hkv, d, 1)));
+  const RowRange rr = row_range(rows, L, local, kv_begin, kv_end);
+  return fwd_common(Qc, Kc, Vc, Qn, Kn, Vn, L, B, Hq, Hkv, d, scale, kv_begin, kv_end, include_local, Op_c, Op_n, 1,
+                    LSEp_c, LSEp_n, workspace, ws_bytes, static_cast<cudaStream_t>(stream), nullptr, nullptr, &rr);
+}
+
+bdlm_status bwd_rows_impl(const char* name, const void* Qc, const void* Kc, const void* Vc, const void* Qn,
+                          const void* Kn, const void* Vn, const void* dOc, const void* dOn, const float* LSEc,
+                          const float* LSEn, const float* Dc, const float* Dn, int64_t L, int64_t B, int Hq, int Hkv,
+                          int d, float scale, int64_t kv_begin, int64_t kv_end, int include_local,
+                          const int64_t* rows, bool local, float* dQc_acc, float* dQn_acc, float* dKc_acc,
+                          float* dVc_acc, float* dKn_acc, float* dVn_acc, void* workspace, size_t ws_bytes,
+                          bdlm_stream stream) {
+  BDLM_CHECK(check_shape(L, B, Hq, Hkv, d));
+  BDLM_CHECK(check_scale(scale));
+  BDLM_CHECK(check_rows_call(L, B, kv_begin, kv_end, include_local, rows, local));
+  BDLM_CHECK(check_ptrs(name, {Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn}));
+  BDLM_CHECK(check_ptrs(name, {dQc_acc, dQn_acc, dKc_acc, dVc_acc, dKn_acc, dVn_acc}));
+  BDLM_CHECK(check_ws(workspace, ws_bytes, bdlm_workspace_size(BDLM_OP_BWD_SHARD, L, B, Hq, Hkv, d, 1)));
+  DeviceInfo info;
+  BDLM_CHECK(device_info(info));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  BDLM_CHECK(clear_status(workspace, st));
+  BwdParams p = bwd_params(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn, L, B, Hq, Hkv, d, scale, kv_begin,
+                           kv_end, include_local, info.sms);
+  p.rows = row_range(rows, L, local, kv_begin, kv_end);
+  p.rows_call = 1;
+  p.dQc = dQc_acc; p.dQn = dQn_acc; p.dKc = dKc_acc; p.dVc = dVc_acc; p.dKn = dKn_acc; p.dVn = dVn_acc;
+  p.g_f32 = 1;
+  p.dq_accumulate = 1;
+  p.dkv_accumulate = 1;
+  int launches = 0;
+  bdlm_status vs = BDLM_OK;
+  cudaError_t e = launch_backward_passes(p, info, workspace, st, &launches, &vs);
+  if (vs != BDLM_OK) return vs;
+  return finish(e, launches, "row-restricted backward launch");
+}
+
+}  // namespace
+
+extern "C" {
+
 bdlm_status bdlm_attn_fwd_shard_rows(const void* Qc, const void* Kc, const void* Vc, const void* Qn,
                                      const void* Kn, const void* Vn, int64_t L, int64_t B, int Hq, int Hkv, int d,
                                      float scale, int64_t kv_begin, int64_t kv_end, int include_local,
@@ -629,19 +718,24 @@ bdlm_status bdlm_attn_fwd_shard_rows(const void* Qc, const void* Kc, const void*
                                      int64_t rows_n_end, float* Op_c, float* Op_n, float* LSEp_c, float* LSEp_n,
                                      void* workspace, size_t ws_bytes, bdlm_stream stream) {
   return guarded([&]() -> bdlm_status {
-    BDLM_CHECK(check_shape(L, B, Hq, Hkv, d));
-    BDLM_CHECK(check_scale(scale));
-    if (kv_begin < 0 || kv_end < kv_begin || kv_end > L)
-      return fail(BDLM_ERR_SHAPE, "clean key range [%lld, %lld) is not inside [0, %lld)", (long long)kv_begin,
-                  (long long)kv_end, (long long)L);
     const int64_t rows[4] = {rows_c_begin, rows_c_end, rows_n_begin, rows_n_end};
-    BDLM_CHECK(check_rows(rows, L));
-    BDLM_CHECK(check_ptrs("bdlm_attn_fwd_shard_rows(Qc,Kc,Vc,Qn,Kn,Vn,Op_c,Op_n,LSEp_c,LSEp_n)",
-                          {Qc, Kc, Vc, Qn, Kn, Vn, Op_c, Op_n, LSEp_c, LSEp_n}));
-    BDLM_CHECK(check_ws(workspace, ws_bytes, bdlm_workspace_size(BDLM_OP_FWD_SHARD, L, B, Hq, Hkv, d, 1)));
-    return fwd_common(Qc, Kc, Vc, Qn, Kn, Vn, L, B, Hq, Hkv, d, scale, kv_begin, kv_end, include_local, Op_c, Op_n,
-                      1, LSEp_c, LSEp_n, workspace, ws_bytes, static_cast<cudaStream_t>(stream), nullptr, nullptr,
-                      rows);
+    return fwd_rows_impl("bdlm_attn_fwd_shard_rows(Qc,Kc,Vc,Qn,Kn,Vn,Op_c,Op_n,LSEp_c,LSEp_n)", Qc, Kc, Vc, Qn, Kn,
+                         Vn, L, B, Hq, Hkv, d, scale, kv_begin, kv_end, include_local, rows, false, Op_c, Op_n,
+                         LSEp_c, LSEp_n, workspace, ws_bytes, stream);
+  });
+}
+
+bdlm_status bdlm_attn_fwd_rank(const void* Qc, const void* Kc, const void* Vc, const void* Qn, const void* Kn,
+                               const void* Vn, int64_t L, int64_t B, int Hq, int Hkv, int d, float scale,
+                               int64_t kv_begin, int64_t kv_end, int include_local, int64_t rows_c_begin,
+                               int64_t rows_c_end, int64_t rows_n_begin, int64_t rows_n_end, float* Op_c,
+                               float* Op_n, float* LSEp_c, float* LSEp_n, void* workspace, size_t ws_bytes,
+                               bdlm_stream stream) {
+  return guarded([&]() -> bdlm_status {
+    const int64_t rows[4] = {rows_c_begin, rows_c_end, rows_n_begin, rows_n_end};
+    return fwd_rows_impl("bdlm_attn_fwd_rank(Qc,Kc,Vc,Qn,Kn,Vn,Op_c,Op_n,LSEp_c,LSEp_n)", Qc, Kc, Vc, Qn, Kn, Vn, L,
+                         B, Hq, Hkv, d, scale, kv_begin, kv_end, include_local, rows, true, Op_c, Op_n, LSEp_c,
+                         LSEp_n, workspace, ws_bytes, stream);
   });
 }
 
@@ -781,34 +875,25 @@ bdlm_status bdlm_attn_bwd_shard_rows(const void* Qc, const void* Kc, const void*
                                      float* dKc_acc, float* dVc_acc, float* dKn_acc, float* dVn_acc, void* workspace,
                                      size_t ws_bytes, bdlm_stream stream) {
   return guarded([&]() -> bdlm_status {
-    BDLM_CHECK(check_shape(L, B, Hq, Hkv, d));
-    BDLM_CHECK(check_scale(scale));
-    if (kv_begin < 0 || kv_end < kv_begin || kv_end > L)
-      return fail(BDLM_ERR_SHAPE, "clean key range [%lld, %lld) is not inside [0, %lld)", (long long)kv_begin,
-                  (long long)kv_end, (long long)L);
     const int64_t rows[4] = {rows_c_begin, rows_c_end, rows_n_begin, rows_n_end};
-    BDLM_CHECK(check_rows(rows, L));
-    BDLM_CHECK(check_ptrs("bdlm_attn_bwd_shard_rows(Qc,Kc,Vc,Qn,Kn,Vn,dOc,dOn,LSEc,LSEn,Dc,Dn)",
-                          {Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn}));
-    BDLM_CHECK(check_ptrs("bdlm_attn_bwd_shard_rows(dQc_acc,dQn_acc,dKc_acc,dVc_acc,dKn_acc,dVn_acc)",
-                          {dQc_acc, dQn_acc, dKc_acc, dVc_acc, dKn_acc, dVn_acc}));
-    BDLM_CHECK(check_ws(workspace, ws_bytes, bdlm_workspace_size(BDLM_OP_BWD_SHARD, L, B, Hq, Hkv, d, 1)));
-    DeviceInfo info;
-    BDLM_CHECK(device_info(info));
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    BDLM_CHECK(clear_status(workspace, st));
-    BwdParams p = bwd_params(Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn, Dc, Dn, L, B, Hq, Hkv, d, scale, kv_begin,
-                             kv_end, include_local, info.sms);
-    p.rows = row_range(rows);
-    p.dQc = dQc_acc; p.dQn = dQn_acc; p.dKc = dKc_acc; p.dVc = dVc_acc; p.dKn = dKn_acc; p.dVn = dVn_acc;
-    p.g_f32 = 1;
-    p.dq_accumulate = 1;
-    p.dkv_accumulate = 1;
-    int launches = 0;
-    bdlm_status vs = BDLM_OK;
-    cudaError_t e = launch_backward_passes(p, info, workspace, st, &launches, &vs);
-    if (vs != BDLM_OK) return vs;
-    return finish(e, launches, "row-restricted backward launch");
+    return bwd_rows_impl("bdlm_attn_bwd_shard_rows(tensors, accumulators)", Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc,
+                         LSEn, Dc, Dn, L, B, Hq, Hkv, d, scale, kv_begin, kv_end, include_local, rows, false, dQc_acc,
+                         dQn_acc, dKc_acc, dVc_acc, dKn_acc, dVn_acc, workspace, ws_bytes, stream);
+  });
+}
+
+bdlm_status bdlm_attn_bwd_rank(const void* Qc, const void* Kc, const void* Vc, const void* Qn, const void* Kn,
+                               const void* Vn, const void* dOc, const void* dOn, const float* LSEc,
+                               const float* LSEn, const float* Dc, const float* Dn, int64_t L, int64_t B, int Hq,
+                               int Hkv, int d, float scale, int64_t kv_begin, int64_t kv_end, int include_local,
+                               int64_t rows_c_begin, int64_t rows_c_end, int64_t rows_n_begin, int64_t rows_n_end,
+                               float* dQc_acc, float* dQn_acc, float* dKc_acc, float* dVc_acc, float* dKn_acc,
+                               float* dVn_acc, void* workspace, size_t ws_bytes, bdlm_stream stream) {
+  return guarded([&]() -> bdlm_status {
+    const int64_t rows[4] = {rows_c_begin, rows_c_end, rows_n_begin, rows_n_end};
+    return bwd_rows_impl("bdlm_attn_bwd_rank(tensors, accumulators)", Qc, Kc, Vc, Qn, Kn, Vn, dOc, dOn, LSEc, LSEn,
+                         Dc, Dn, L, B, Hq, Hkv, d, scale, kv_begin, kv_end, include_local, rows, true, dQc_acc,
+                         dQn_acc, dKc_acc, dVc_acc, dKn_acc, dVn_acc, workspace, ws_bytes, stream);
   });
 }
 

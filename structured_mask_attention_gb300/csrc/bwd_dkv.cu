@@ -241,8 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* mv = t.ks ? &tVn : &tVc;
 #pragma unroll
         for (int pn = 0; pn < HD / 64; ++pn) {
-          tma_load_3d(sK + pn * LY::kPanel, mk, BAR(KV_KF), pn * 64, t.kvh, (int)((VL ? t.off : 0) + t.j0));
-          tma_load_3d(sV + pn * LY::kPanel, mv, BAR(KV_KF), pn * 64, t.kvh, (int)((VL ? t.off : 0) + t.j0));
+          // (a row-restricted call's K / V hold only its keys: local index)
+          const int kj = (int)((VL ? t.off : 0) + (ROWS ? local_key(p.rows, t.ks, t.j0) : t.j0));
+          tma_load_3d(sK + pn * LY::kPanel, mk, BAR(KV_KF), pn * 64, t.kvh, kj);
+          tma_load_3d(sV + pn * LY::kPanel, mv, BAR(KV_KF), pn * 64, t.kvh, kj);
         }
       }
       DkvCursor cur;
@@ -263,21 +265,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int pn = 0; pn < HD / 64; ++pn) {
             tma_load_3d(sQ + st * LY::kTile + pn * LY::kPanel, mq, BAR(KV_QF + st), pn * 64, head,
-                        (int)((VL ? t.off : 0) + q0));
+                        (int)((VL ? t.off : 0) + (ROWS ? local_row(p.rows, s, q0) : q0)));
             tma_load_3d(sdO + st * LY::kTile + pn * LY::kPanel, mo, BAR(KV_QF + st), pn * 64, head,
-                        (int)((VL ? t.off : 0) + q0));
+                        (int)((VL ? t.off : 0) + (ROWS ? local_row(p.rows, s, q0) : q0)));
           }
         }
-        // LSE and D of the tile's 128 rows, asynchronously (rows >= L read as 0)
-        const float* LSE = (s ? p.LSEn : p.LSEc) + (int64_t)head * p.g.L + (VL ? t.off : 0);
-        const float* Dr = (s ? p.Dn : p.Dc) + (int64_t)head * p.g.L + (VL ? t.off : 0);
+        // LSE and D of the tile's 128 rows, asynchronously (rows >= L, and rows
+        // a row-restricted call's statistics do not hold, read as 0)
+        const int64_t lstride = ROWS ? held_rows(p.rows, s) : p.g.L;
+        const float* LSE = (s ? p.LSEn : p.LSEc) + (int64_t)head * lstride + (VL ? t.off : 0);
+        const float* Dr = (s ? p.Dn : p.Dc) + (int64_t)head * lstride + (VL ? t.off : 0);
         const uint32_t stat = sStat + st * 2 * KBN * 4;
 #pragma unroll
         for (int c = R.lane; c < KBN; c += 32) {
           const int64_t r = q0 + c;
-          const bool v = r < (VL ? t.L : p.g.L);
-          cp_async4(stat + c * 4, LSE + (v ? r : 0), v);
-          cp_async4(stat + (KBN + c) * 4, Dr + (v ? r : 0), v);
+          const int64_t lr = ROWS ? local_row(p.rows, s, r) : r;
+          const bool v = ROWS ? (r < p.g.L && lr >= 0 && lr < lstride) : r < (VL ? t.L : p.g.L);
+          cp_async4(stat + c * 4, LSE + (v ? lr : 0), v);
+          cp_async4(stat + (KBN + c) * 4, Dr + (v ? lr : 0), v);
         }
         cp_async_mbar_arrive(BAR(KV_QF + st));
       }
@@ -453,11 +458,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       // the key set of this call: clean keys in [kv_begin, kv_end), corrupted keys all
+      // (and, in a row-restricted call, the keys its dK / dV hold)
       const bool wr = VL ? j < t.L
-                         : j < p.g.L && (t.ks == 1 || (j >= p.g.kv_begin && j < p.g.kv_end));
+                         : j < p.g.L && (t.ks == 1 || (j >= p.g.kv_begin && j < p.g.kv_end)) &&
+                               (!ROWS || key_held(p.rows, t.ks, j));
       void* dKo = t.ks ? p.dKn : p.dKc;
       void* dVo = t.ks ? p.dVn : p.dVc;
-      const int64_t oofs = (((VL ? t.off : 0) + j) * p.g.Hkv + t.kvh) * HD + half * (HD / 2);
+      const int64_t oofs =
+          (((VL ? t.off : 0) + (ROWS ? local_key(p.rows, t.ks, j) : j)) * p.g.Hkv + t.kvh) * HD + half * (HD / 2);
 #pragma unroll
       for (int c4 = 0; c4 < HD / 64; ++c4) {
         uint32_t uk[32], uv[32];
@@ -502,7 +510,7 @@ cudaError_t launch_bwd_dkv_tc(const BwdMaps& m, const BwdParams& p, const Varlen
   const VarlenTabs none{nullptr, nullptr, nullptr, 0, 0};
   const VarlenTabs& t = vt ? *vt : none;
   // a row range, or accumulation across calls: the rows instantiation (one sequence)
-  const bool rows = p.dkv_accumulate || range_restricts(p.rows);
+  const bool rows = p.rows_call != 0;
   if (rows && vt) return cudaErrorInvalidValue;
   cudaError_t e;
   if (rows)

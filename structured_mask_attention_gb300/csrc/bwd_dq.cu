@@ -163,13 +163,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* mo = t.stream ? &tdOn : &tdOc;
 #pragma unroll
         for (int pn = 0; pn < HD / 64; ++pn) {
-          tma_load_3d(sQ + pn * LY::kPanel, mq, BAR(DQ_QF), pn * 64, t.head, (int)((VL ? t.off : 0) + t.r0));
-          tma_load_3d(sdO + pn * LY::kPanel, mo, BAR(DQ_QF), pn * 64, t.head, (int)((VL ? t.off : 0) + t.r0));
+          tma_load_3d(sQ + pn * LY::kPanel, mq, BAR(DQ_QF), pn * 64, t.head, (int)((VL ? t.off : 0) + (ROWS ? local_row(p.rows, t.stream, t.r0) : t.r0)));
+          tma_load_3d(sdO + pn * LY::kPanel, mo, BAR(DQ_QF), pn * 64, t.head, (int)((VL ? t.off : 0) + (ROWS ? local_row(p.rows, t.stream, t.r0) : t.r0)));
         }
         ++itn;
         for (int j = 0; j < t.n; ++j, ++g) {
           const bool cs = j < t.nc;
-          const int key0 = (int)((VL ? t.off : 0) + dq_key0(t, j));  // packed-tensor row
+          // packed-tensor row, or the key's index in a row-restricted call's K / V
+          const int key0 =
+              (int)((VL ? t.off : 0) + (ROWS ? local_key(p.rows, cs ? 0 : 1, dq_key0(t, j)) : dq_key0(t, j)));
           const int ks = g % KNS, vs = g & 1;
           if (g >= KNS && !mbar_wait(BAR(DQ_KE + ks), ((g / KNS) - 1) & 1, wd, 22)) { ok = false; break; }
           mbar_arrive_expect_tx(BAR(DQ_KF + ks), LY::kTile);
@@ -270,7 +272,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t r = t.r0 + row;  // row within the item's sequence
       const bool valid = r < seqL && (!ROWS || row_in(p.rows, t.stream, r));
       void* dqbase = t.stream ? p.dQn : p.dQc;
-      const int64_t oofs = ((seq0 + r) * p.g.Hq + t.head) * HD + half * (HD / 2);
+      // the row's index in its stream's tensors (packed row in a batch, local
+      // row in a row-restricted call) and the [H, rows] statistics' stride
+      const int64_t lrow = VL ? seq0 + r : (ROWS ? local_row(p.rows, t.stream, r) : r);
+      const int64_t lstride = ROWS ? held_rows(p.rows, t.stream) : p.g.L;
+      const int64_t oofs = (lrow * p.g.Hq + t.head) * HD + half * (HD / 2);
       if (t.n == 0) {
         // no visible key for the whole tile: dQ rows are zero
         if (valid && !p.dq_accumulate) {
@@ -291,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t clo, chi, nlo, nhi;
       clean_interval(gm, t.stream, rr, clo, chi);
       noisy_interval(gm, t.stream, rr, nlo, nhi);
-      const int64_t srow = (int64_t)t.head * p.g.L + seq0 + r;  // [H, rows] statistics
+      const int64_t srow = (int64_t)t.head * lstride + lrow;  // [H, rows] statistics
       const float nlse2 = valid ? -(t.stream ? p.LSEn : p.LSEc)[srow] * kLog2e : 0.f;
       const float Dv = valid ? (t.stream ? p.Dn : p.Dc)[srow] : 0.f;
       const uint64_t sl2x2 = f2(p.scale_log2, p.scale_log2), nl2 = f2(nlse2, nlse2), nD2 = f2(-Dv, -Dv);
@@ -372,7 +378,7 @@ cudaError_t launch_dq_t(const BwdMaps& m, const BwdParams& p, const VarlenTabs& 
 cudaError_t launch_bwd_dq_tc(const BwdMaps& m, const BwdParams& p, const VarlenTabs* vt, int num_sms,
                              uint32_t* status, uint64_t limit_ns, cudaStream_t stream, int* launches) {
   // a row-restricted call lists only the query tiles that hold its rows (one sequence)
-  const bool rows = range_restricts(p.rows);
+  const bool rows = p.rows_call != 0;
   if (rows && vt) return cudaErrorInvalidValue;
   const int64_t n = vt ? vt->n_q : rows ? q_items_rows(p.g, p.rows, QBM) : q_items(p.g, QBM);
   if (n == 0) return cudaSuccess;

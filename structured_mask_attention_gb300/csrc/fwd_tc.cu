@@ -253,12 +253,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int pn = 0; pn < HD / 64; ++pn)
             tma_load_3d(sQ + t * LY::kTile + pn * kPanel, mq, BAR(B_QF), pn * 64, g.head,
-                        (int)(g.off + g.r0 + t * BM));
+                        (int)(g.off + (ROWS ? local_row(rows, g.stream, g.r0 + t * BM) : g.r0 + t * BM)));
         ++itn;
         for (int j = 0; j < g.n; ++j, ++kc) {
           const int st = kc & 1;
           const bool cs = j < g.nc;
-          const int key0 = (int)(g.off + tile_key0(g, j));  // packed-tensor row
+          // packed-tensor row, or the key's index in a row-restricted call's K / V
+          const int key0 = (int)(g.off + (ROWS ? local_key(rows, cs ? 0 : 1, tile_key0(g, j)) : tile_key0(g, j)));
           if (kc >= 2 && !mbar_wait(BAR(B_KE + st), ((kc >> 1) - 1) & 1, wd, 2)) { ok = false; break; }
           mbar_arrive_expect_tx(BAR(B_KF + st), LY::kTile);
 #pragma unroll
@@ -360,9 +361,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t seqL = VL ? g.L : p.g.L, seq0 = VL ? g.off : 0;
       const int64_t r = g.r0 + t * BM + row;  // row within the item's sequence
       const bool valid = r < seqL;
-      float* lse_out = (g.stream ? p.LSEn : p.LSEc) + (int64_t)g.head * p.g.L + seq0;
+      // the row's index in its stream's O and LSE (the packed row in a batch,
+      // the local row in a row-restricted call) and the LSE row stride
+      const int64_t lrow = VL ? seq0 + r : (ROWS ? local_row(rows, g.stream, r) : r);
+      const int64_t lstride = ROWS ? held_rows(rows, g.stream) : p.g.L;
+      float* lse_out = (g.stream ? p.LSEn : p.LSEc) + (int64_t)g.head * lstride;
       void* obase = g.stream ? p.On : p.Oc;
-      const int64_t oofs = ((seq0 + r) * p.g.Hq + g.head) * HD;
+      const int64_t oofs = (lrow * p.g.Hq + g.head) * HD;
       if (g.n == 0) {
         if (valid && (!ROWS || row_in(rows, g.stream, r))) {
           if (p.o_f32) {
@@ -374,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < HD / 8; ++c) o[c] = make_uint4(0u, 0u, 0u, 0u);
           }
-          lse_out[r] = -INFINITY;
+          lse_out[lrow] = -INFINITY;
         }
         continue;
       }
@@ -469,9 +474,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t seqL_e = VL ? ge.L : p.g.L, seq0_e = VL ? ge.off : 0;
       const int64_t re = ge.r0 + t * BM + row;
       const bool ve = re < seqL_e && (!ROWS || row_in(rows, ge.stream, re));
-      float* lse_e = (ge.stream ? p.LSEn : p.LSEc) + (int64_t)ge.head * p.g.L + seq0_e;
+      const int64_t lrow_e = VL ? seq0_e + re : (ROWS ? local_row(rows, ge.stream, re) : re);
+      const int64_t lstride_e = ROWS ? held_rows(rows, ge.stream) : p.g.L;
+      float* lse_e = (ge.stream ? p.LSEn : p.LSEc) + (int64_t)ge.head * lstride_e;
       void* obase_e = ge.stream ? p.On : p.Oc;
-      const int64_t oofs_e = ((seq0_e + re) * p.g.Hq + ge.head) * HD;
+      const int64_t oofs_e = (lrow_e * p.g.Hq + ge.head) * HD;
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -509,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(BAR(B_OE + t));
-      if (ve) lse_e[re] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      if (ve) lse_e[lrow_e] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
       ++itn;
     }
   }

@@ -40,9 +40,21 @@ struct Geom {
 // computes only the rows it owns; rows outside are neither computed into
 // other rows' results nor written.  (Kept apart from Geom: the kernels that
 // do not restrict rows keep their parameter blocks, and registers, as is.)
+//
+// The same calls describe where the tensors' rows live.  The row-indexed
+// tensors of stream s (its Q, dO, O, LSE, D, dQ; for the corrupted stream
+// also its K, V, dK, dV, since a rank owns whole corrupted blocks) hold rows
+// [base[s], base[s] + len[s]), row i at local index i - base[s]; the clean K,
+// V, dK, dV hold keys [kbase, kbase + klen).  Full-length tensors: base 0,
+// len = klen = L.  Rank-local tensors: base = lo, len = hi - lo, and the
+// clean keys the call reads.  The kernels' tensor maps cover only the held
+// rows, so a tile that reaches past them reads zeros there.
 struct RowRange {
   int32_t lo[2] = {0, 0};
   int32_t hi[2] = {0x7fffffff, 0x7fffffff};
+  int32_t base[2] = {0, 0};
+  int32_t len[2] = {0, 0};
+  int32_t kbase = 0, klen = 0;
 };
 
 BDLM_HD int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
@@ -81,6 +93,19 @@ BDLM_HD bool range_restricts(const RowRange& r) {
 // copy stays in registers).
 BDLM_HD int64_t range_lo(const RowRange& r, int stream) { return stream ? r.lo[1] : r.lo[0]; }
 BDLM_HD int64_t range_hi(const RowRange& r, int stream) { return stream ? r.hi[1] : r.hi[0]; }
+
+// Local index of row i of `stream` in that stream's row-indexed tensors, the
+// row stride of its [H, rows] statistics, and the local index of key j of
+// key stream ks.
+BDLM_HD int64_t local_row(const RowRange& r, int stream, int64_t i) { return i - (stream ? r.base[1] : r.base[0]); }
+BDLM_HD int64_t held_rows(const RowRange& r, int stream) { return stream ? r.len[1] : r.len[0]; }
+BDLM_HD int64_t local_key(const RowRange& r, int ks, int64_t j) { return j - (ks ? r.base[1] : r.kbase); }
+
+// True when key j of key stream ks is held by the call's K / V tensors.
+BDLM_HD bool key_held(const RowRange& r, int ks, int64_t j) {
+  const int64_t k = local_key(r, ks, j);
+  return k >= 0 && k < (ks ? r.len[1] : r.klen);
+}
 
 // True when query row i of `stream` is in the range.
 BDLM_HD bool row_in(const RowRange& r, int stream, int64_t i) {

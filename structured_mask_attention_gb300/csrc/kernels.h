@@ -76,7 +76,8 @@ struct BwdParams {
   int g_f32;         // gradient outputs fp32 (else bf16)
   int dq_accumulate; // dQ += contribution (fp32 only)
   int dkv_accumulate;  // dK, dV += contribution (fp32 only)
-  RowRange rows;       // query rows of the call (default: all)
+  int rows_call;       // row-restricted call: the kernels' rows instantiations
+  RowRange rows;       // query rows of the call and where its tensors' rows live
 };
 
 // Tensor maps of the tensor-core backward passes: [L, H, d] bf16 viewed 3-D,

@@ -229,3 +229,86 @@ def test_rank_rows_empty_and_one_sided(lib):
     o = m.bdlm_attn_fwd_shard_rows(*ins, B, 0, L, True, (37, 300), (0, 0), sc)    # clean rows only
     check_rel("Oc rows 37..300", to_np(o[0])[37:300], ref[0][37:300])
     assert not o[1].any() and not o[0][:37].any() and not o[0][300:].any()
+
+
+@pytest.mark.parametrize("L,B,R,Hq,Hkv,d", [
+    (2048, 128, 4, 4, 2, 128),
+    (768, 32, 4, 3, 1, 64),      # slices of 192 rows: tiles straddle the held rows
+])
+def test_rank_local_tensors(lib, L, B, R, Hq, Hkv, d):
+    """bdlm_attn_fwd_rank / bdlm_attn_bwd_rank on tensors that hold only a
+    rank's rows and one clean shard's keys: every partial equals the
+    full-length call's rows bit for bit, and the ranks' merged outputs and
+    summed gradients match the fp64 oracle."""
+    m = lib
+    X = make_numpy(L, Hq, Hkv, d, seed=L + 3 * R)
+    X64 = {k: v.astype(np.float64) for k, v in X.items()}
+    dev = {k: to_dev(v, torch) for k, v in X.items()}
+    ins = [dev[k] for k in NAMES[:6]]
+    sc = 1.0 / math.sqrt(d)
+    plan = csbp.CSBPPlan.build(L, B, R)
+    f32 = dict(dtype=torch.float32, device="cuda")
+    Oc, On = torch.zeros((L, Hq, d), **f32), torch.zeros((L, Hq, d), **f32)
+    LSEc, LSEn = torch.zeros((Hq, L), **f32), torch.zeros((Hq, L), **f32)
+    dQc, dQn = torch.zeros((L, Hq, d), **f32), torch.zeros((L, Hq, d), **f32)
+    dKc, dVc, dKn, dVn = (torch.zeros((L, Hkv, d), **f32) for _ in range(4))
+    no_keys = torch.empty((0, Hkv, d), dtype=torch.bfloat16, device="cuda")
+    specs = [(*plan.shard_keys(s), False) for s in range(R)] + [(0, 0, True)]
+    for r in range(R):
+        rw = plan.rows(r)
+        rc, rn = (rw.c0 * B, rw.c1 * B), (rw.n0 * B, rw.n1 * B)
+        c, n = slice(*rc), slice(*rn)
+        loc = {k: dev[k][c].contiguous() for k in ("Qc", "dOc")}
+        loc.update({k: dev[k][n].contiguous() for k in ("Qn", "Kn", "Vn", "dOn")})
+        kv = lambda lo, hi: ((dev["Kc"][lo:hi].contiguous(), dev["Vc"][lo:hi].contiguous()) if hi > lo
+                             else (no_keys, no_keys))
+        parts = []
+        for (lo, hi, local) in specs:
+            Kc_, Vc_ = kv(lo, hi)
+            pl = m.bdlm_attn_fwd_rank(loc["Qc"], Kc_, Vc_, loc["Qn"], loc["Kn"], loc["Vn"], L, B, lo, hi, local,
+                                      rc, rn, sc)
+            pf = m.bdlm_attn_fwd_shard_rows(*ins, B, lo, hi, local, rc, rn, sc)
+            for got, full in ((pl[0], pf[0][c]), (pl[1], pf[1][n]), (pl[2], pf[2][:, c]), (pl[3], pf[3][:, n])):
+                assert torch.equal(got, full)
+            parts.append(pl)
+        oc, lc = m.bdlm_lse_merge([p[0] for p in parts], [p[2] for p in parts], o_dtype=torch.float32)
+        on, ln = m.bdlm_lse_merge([p[1] for p in parts], [p[3] for p in parts], o_dtype=torch.float32)
+        Oc[c], On[n], LSEc[:, c], LSEn[:, n] = oc, on, lc, ln
+        Dc, Dn = m.bdlm_bwd_preprocess(oc, loc["dOc"]), m.bdlm_bwd_preprocess(on, loc["dOn"])
+        z = lambda t: torch.zeros(t.shape, **f32)
+        aq = (z(loc["Qc"]), z(loc["Qn"]))
+        akn = (z(loc["Kn"]), z(loc["Vn"]))
+        for (lo, hi, local) in specs:
+            Kc_, Vc_ = kv(lo, hi)
+            akc = (z(Kc_), z(Vc_))
+            m.bdlm_attn_bwd_rank(loc["Qc"], Kc_, Vc_, loc["Qn"], loc["Kn"], loc["Vn"], loc["dOc"], loc["dOn"],
+                                 lc.contiguous(), ln.contiguous(), Dc, Dn, L, B, lo, hi, local, rc, rn, *aq, *akc,
+                                 *akn, sc)
+            dKc[lo:hi] += akc[0]
+            dVc[lo:hi] += akc[1]
+        dQc[c], dQn[n], dKn[n], dVn[n] = aq[0], aq[1], akn[0], akn[1]
+    ref = orc.fwd_blockwise(*[X64[k] for k in NAMES[:6]], B, sc)
+    check_rel("Oc (rank-local)", to_np(Oc), ref[0])
+    check_rel("On (rank-local)", to_np(On), ref[1])
+    check_lse("LSEc (rank-local)", to_np(LSEc), ref[2])
+    check_lse("LSEn (rank-local)", to_np(LSEn), ref[3])
+    gref = orc.bwd_blockwise(*[X64[k] for k in NAMES], B, sc)
+    for name, g, r_ in zip(("dQc", "dKc", "dVc", "dQn", "dKn", "dVn"), (dQc, dKc, dVc, dQn, dKn, dVn), gref):
+        check_rel(f"{name} (rank-local)", to_np(g), r_)
+
+
+def test_rank_local_validation(lib):
+    m = lib
+    L, B, Hq, Hkv, d = 512, 64, 2, 1, 64
+    X = make_numpy(L, Hq, Hkv, d, seed=9)
+    dev = {k: to_dev(v, torch) for k, v in X.items()}
+    no_keys = torch.empty((0, Hkv, d), dtype=torch.bfloat16, device="cuda")
+    # the local partial needs whole corrupted blocks (their keys are read)
+    with pytest.raises(m.BdlmError) as e:
+        m.bdlm_attn_fwd_rank(dev["Qc"][:128], no_keys, no_keys, dev["Qn"][32:160], dev["Kn"][32:160],
+                             dev["Vn"][32:160], L, B, 0, 0, True, (0, 128), (32, 160))
+    assert e.value.status == 2
+    # tensors must hold exactly the call's rows
+    with pytest.raises(ValueError):
+        m.bdlm_attn_fwd_rank(dev["Qc"][:100], no_keys, no_keys, dev["Qn"][:128], dev["Kn"][:128], dev["Vn"][:128],
+                             L, B, 0, 0, True, (0, 128), (0, 128))
