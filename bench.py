@@ -411,6 +411,66 @@ def per_rank_memory(L, Hq, Hkv, d, R):
     return {"pure_bp": g(bp), "csbp_allgather": g(csbp + gathered), "csbp_ring": g(csbp + ring)}
 
 
+def rank_program_memory(m, plan, rank, Hq, Hkv, d, schedule, dev):
+    """Peak device memory (bytes above what was allocated before) of one
+    rank's forward + backward through the rank-local calls: its own rows as
+    inputs (its clean shard's Q, K, V, dO; its corrupted blocks' Q, K, V, dO),
+    the clean K / V it receives (all shards at once when gathered; one shard
+    at a time beside its own, as a two-shard ring holds them, per shard), the
+    partials, merged outputs, statistics and fp32 gradients.  Input values
+    are random: only the sizes matter here."""
+    import torch
+    L, B = plan.L, plan.B
+    rw = plan.rows(rank)
+    rc, rn = (rw.c0 * B, rw.c1 * B), (rw.n0 * B, rw.n1 * B)
+    nc, nn = rc[1] - rc[0], rn[1] - rn[0]
+    sc = 1.0 / math.sqrt(d)
+    torch.cuda.synchronize(dev)
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    bf = lambda n, H: torch.randn((n, H, d), device=dev, dtype=torch.bfloat16)
+    z32 = lambda n, H: torch.zeros((n, H, d), device=dev, dtype=torch.float32)
+    Qc, dOc, Kc_own, Vc_own = bf(nc, Hq), bf(nc, Hq), bf(nc, Hkv), bf(nc, Hkv)
+    Qn, dOn, Kn, Vn = bf(nn, Hq), bf(nn, Hq), bf(nn, Hkv), bf(nn, Hkv)
+    nk = torch.empty((0, Hkv, d), dtype=torch.bfloat16, device=dev)
+    if schedule == "gathered":
+        Kg, Vg = bf(L, Hkv), bf(L, Hkv)  # after the all-gather
+        parts = [m.bdlm_attn_fwd_rank(Qc, Kg, Vg, Qn, Kn, Vn, L, B, 0, L, True, rc, rn, sc)]
+    else:  # a running merge, as csbp.forward does: two partials held at most
+        parts = []
+        for s_ in range(plan.R + 1):
+            lo, hi = plan.shard_keys(s_) if s_ < plan.R else (0, 0)
+            Ks, Vs = (bf(hi - lo, Hkv), bf(hi - lo, Hkv)) if hi > lo else (nk, nk)  # the shard in flight
+            parts.append(m.bdlm_attn_fwd_rank(Qc, Ks, Vs, Qn, Kn, Vn, L, B, lo, hi, s_ == plan.R, rc, rn, sc))
+            del Ks, Vs
+            if len(parts) == 2:
+                mc = m.bdlm_lse_merge([parts[0][0], parts[1][0]], [parts[0][2], parts[1][2]], o_dtype=torch.float32)
+                mn = m.bdlm_lse_merge([parts[0][1], parts[1][1]], [parts[0][3], parts[1][3]], o_dtype=torch.float32)
+                parts = [(mc[0], mn[0], mc[1], mn[1])]
+                del mc, mn
+    oc, lc = m.bdlm_lse_merge([p_[0] for p_ in parts], [p_[2] for p_ in parts], o_dtype=torch.float32)
+    on, ln = m.bdlm_lse_merge([p_[1] for p_ in parts], [p_[3] for p_ in parts], o_dtype=torch.float32)
+    del parts
+    Dc, Dn = m.bdlm_bwd_preprocess(oc, dOc), m.bdlm_bwd_preprocess(on, dOn)
+    dQc, dQn, dKn, dVn = z32(nc, Hq), z32(nn, Hq), z32(nn, Hkv), z32(nn, Hkv)
+    if schedule == "gathered":
+        dKg, dVg = z32(L, Hkv), z32(L, Hkv)  # summed shard by shard onto the owners afterwards
+        m.bdlm_attn_bwd_rank(Qc, Kg, Vg, Qn, Kn, Vn, dOc, dOn, lc, ln, Dc, Dn, L, B, 0, L, True, rc, rn,
+                             dQc, dQn, dKg, dVg, dKn, dVn, sc)
+    else:
+        for s_ in range(plan.R):
+            lo, hi = plan.shard_keys(s_)
+            Ks, Vs, dKs, dVs = bf(hi - lo, Hkv), bf(hi - lo, Hkv), z32(hi - lo, Hkv), z32(hi - lo, Hkv)
+            m.bdlm_attn_bwd_rank(Qc, Ks, Vs, Qn, Kn, Vn, dOc, dOn, lc, ln, Dc, Dn, L, B, lo, hi, False, rc, rn,
+                                 dQc, dQn, dKs, dVs, dKn, dVn, sc)
+            del Ks, Vs, dKs, dVs
+        e0 = torch.empty((0, Hkv, d), dtype=torch.float32, device=dev)
+        m.bdlm_attn_bwd_rank(Qc, nk, nk, Qn, Kn, Vn, dOc, dOn, lc, ln, Dc, Dn, L, B, 0, 0, True, rc, rn,
+                             dQc, dQn, e0, e0, dKn, dVn, sc)
+    torch.cuda.synchronize(dev)
+    return torch.cuda.max_memory_allocated(dev) - base
+
+
 # ------------------------------------------------------------------ sweep (measurement tables)
 def run_sweep(args):
     """Per-config timings, the schedule ablation and the sharded block-size
@@ -709,6 +769,16 @@ def run_sweep(args):
             del parts
         del X, ins, fu, Dc, Dn, acc
         torch.cuda.empty_cache()
+        # each rank's device memory through the rank-local calls (rank 0 and
+        # the last rank of the balanced plan; nothing else allocated)
+        for R in (2, 4, 8):
+            plan = csbp.CSBPPlan.build(L, B, R)
+            for schedule in ("gathered", "per_shard"):
+                peaks = [rank_program_memory(m, plan, r, Hq, Hkv, d, schedule, dev) for r in (0, R - 1)]
+                torch.cuda.empty_cache()
+                emit({"sweep": "rank_memory", "workload": "long-128k", "R": R, "schedule": schedule,
+                      "peak_gib_rank0_last": [round(x / 2 ** 30, 3) for x in peaks],
+                      "model_gib": per_rank_memory(L, Hq, Hkv, d, R)})
 
     # ---- the fp64 oracle on the host cores: a timed sample per config,
     # extrapolated by useful FLOP to the whole config (all heads, both streams)

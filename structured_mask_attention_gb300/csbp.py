@@ -22,7 +22,8 @@ App. I / Table 5 per the review's Strengths):
 * Forward on rank r: for every clean shard s in order 0..R-1 a partial
   (O_s, LSE_s) of the rank's rows against shard s's keys, then the local
   partial (corrupted rows against their own block), merged exactly by
-  log-sum-exp in that fixed order.  Only clean K/V cross ranks: here they are
+  log-sum-exp in that fixed order, each partial folded into a running merge
+  as it is computed.  Only clean K/V cross ranks: here they are
   all-gathered once; a ring that holds two shards at a time is the same
   plan with less memory.  Once all shards are gathered the rank may instead
   make one call over the whole clean sequence (``gathered=True``): the same
@@ -160,9 +161,13 @@ def forward(plan: CSBPPlan, comm, compute, shards, gathered: bool = False):
     rows = plan.rows(comm.rank)
     if gathered:
         return compute.merge([compute.fwd(rows, (0, plan.L), _gathered(shards), True)])
-    parts = [compute.fwd(rows, plan.shard_keys(s), shards[s], False) for s in range(plan.R)]
-    parts.append(compute.fwd(rows, (0, 0), None, True))
-    return compute.merge(parts)
+    # a running merge: each partial is folded in as it is computed, so that
+    # no more than two are held (the LSE merge is associative)
+    acc = None
+    for s in range(plan.R):
+        part = compute.fwd(rows, plan.shard_keys(s), shards[s], False)
+        acc = part if acc is None else compute.merge([acc, part])
+    return compute.merge([acc, compute.fwd(rows, (0, 0), None, True)])
 
 
 def backward(plan: CSBPPlan, comm, compute, shards, out, dO, gathered: bool = False):
