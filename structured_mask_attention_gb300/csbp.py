@@ -63,7 +63,8 @@ shards are copied into local HBM first).  Checked: the plan and this driver
 with gloo ranks on the CPU and the fp64 oracle as the compute object
 (tests/test_csbp_ranks.py); the driver with ``KernelCompute`` for every rank
 on one GPU, the ranks as host threads exchanging through host-side
-collectives (tests/test_gpu_csbp_rows.py).  A rank holds only its own rows
+collectives, and over NCCL through ``TorchComm`` as a one-rank group
+(tests/test_gpu_csbp_rows.py).  A rank holds only its own rows
 and the clean K / V it receives.  No run on several GPUs exists.
 """
 from __future__ import annotations

@@ -312,3 +312,74 @@ def test_rank_local_validation(lib):
     with pytest.raises(ValueError):
         m.bdlm_attn_fwd_rank(dev["Qc"][:100], no_keys, no_keys, dev["Qn"][:128], dev["Kn"][:128], dev["Vn"][:128],
                              L, B, 0, 0, True, (0, 128), (0, 128))
+
+
+def _nccl_single_rank(port, L, B, Hq, Hkv, d, gathered, out):
+    """Child process: one NCCL rank runs the CSBP driver with TorchComm and
+    KernelCompute and reports its largest relative error against the fp64
+    oracle."""
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    os.environ.setdefault("NCCL_NVLS_ENABLE", "0")
+    import numpy as np_
+    import torch as t_
+    import torch.distributed as dist
+    import oracle.bdlm_oracle as orc_
+    import structured_mask_attention_gb300 as m
+    from structured_mask_attention_gb300 import csbp as csbp_
+    from structured_mask_attention_gb300.inputs import make_numpy as mk
+    m.load_library()
+    t_.cuda.set_device(0)
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1)
+    try:
+        X = mk(L, Hq, Hkv, d, seed=21)
+        dev = {k: t_.from_numpy(v).to("cuda").to(t_.bfloat16).contiguous() for k, v in X.items()}
+        X64 = {k: dev[k].float().cpu().numpy().astype(np_.float64) for k in dev}
+        sc = 1.0 / np_.sqrt(d)
+        plan = csbp_.CSBPPlan.build(L, B, 1)
+        comm = csbp_.TorchComm()
+        comp = csbp_.KernelCompute(m, plan, 0, dict(dev), sc)
+        shards = csbp_.gather_clean_kv(comm, dev["Kc"], dev["Vc"])
+        o = csbp_.forward(plan, comm, comp, shards, gathered)
+        (dqc, dqn), (dkc, dvc), (dkn, dvn) = csbp_.backward(plan, comm, comp, shards, o, (dev["dOc"], dev["dOn"]),
+                                                           gathered)
+        t_.cuda.synchronize()
+        names = ("Qc", "Kc", "Vc", "Qn", "Kn", "Vn")
+        rf = orc_.fwd_blockwise(*[X64[k] for k in names], B, sc)
+        rg = orc_.bwd_blockwise(*[X64[k] for k in names], X64["dOc"], X64["dOn"], B, sc)
+        err = 0.0
+        for got, ref in ((o[0], rf[0]), (o[1], rf[1]), (dqc, rg[0]), (dkc, rg[1]), (dvc, rg[2]), (dqn, rg[3]),
+                         (dkn, rg[4]), (dvn, rg[5])):
+            g = got.float().cpu().numpy()
+            err = max(err, float(np_.abs(g - ref).max() / np_.abs(ref).max()))
+        lerr = max(float(np_.abs(o[2].cpu().numpy() - rf[2]).max()), float(np_.abs(o[3].cpu().numpy() - rf[3]).max()))
+        out.put(("ok", err, lerr))
+    except BaseException as e:  # reported to the parent
+        out.put(("error", repr(e), 0.0))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("gathered", [False, True])
+def test_csbp_driver_nccl_single_rank(gathered):
+    """The transport on NCCL with CUDA tensors: a one-rank NCCL group runs the
+    CSBP driver end to end (all-gather and reduce through torch.distributed)
+    on the kernels; outputs and gradients match the fp64 oracle."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    p = ctx.Process(target=_nccl_single_rank, args=(port, 512, 64, 2, 1, 64, gathered, q))
+    p.start()
+    status, err, lerr = q.get(timeout=600)
+    p.join(timeout=120)
+    assert status == "ok", err
+    assert p.exitcode == 0
+    assert err <= 2e-2, err
+    assert lerr <= 1e-3, lerr
