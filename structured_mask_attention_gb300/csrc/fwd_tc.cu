@@ -9,10 +9,10 @@
 // (clean keys restricted to [kv_begin, kv_end), corrupted own block optional:
 // CSBP, evolve.pub FAQ), writing O = 0, LSE = -inf for rows with no key.
 //
-// Design (one CTA per SM, persistent; 10 warps).  An item is 256 consecutive
-// query rows of one stream and head, split into two 128-row sub-tiles that
-// share every key tile (rows of one block see the same keys), so each
-// 128-key K/V tile is loaded once for both:
+// Design (one CTA per SM, persistent; 12 warps in three warpgroups).  An
+// item is 256 consecutive query rows of one stream and head, split into two
+// 128-row sub-tiles that share every key tile (rows of one block see the
+// same keys), so each 128-key K/V tile is loaded once for both:
 //   warp 0      TMA producer: Q of both sub-tiles, then K and V tiles through
 //               two 2-stage rings;
 //   warp 1      owns TMEM (512 columns: S of sub-tile t at 128 t, O of
@@ -20,7 +20,10 @@
 //               order S0(j), S1(j), PV0(j), S0(j+1), PV1(j), S1(j+1), ... so
 //               the tensor pipe works on one sub-tile while the other one's
 //               softmax runs;
-//   warps 2-5   softmax of sub-tile 0, warps 6-9 of sub-tile 1: one query row
+//   warps 2-3   no role: they complete the first warpgroup, which gives its
+//               registers to the softmax warpgroups (setmaxnreg), so that a
+//               softmax thread holds its row's 128 scores without spilling;
+//   warps 4-7   softmax of sub-tile 0, warps 8-11 of sub-tile 1: one query row
 //               per thread, online softmax in the log2 domain with a lazy
 //               rescale (the reference max moves only when the row max grows
 //               by more than 8), P written back over S in TMEM as packed bf16
@@ -49,7 +52,14 @@ namespace {
 constexpr int BM = kFwdTileQ;      // query rows per sub-tile (128)
 constexpr int BI = kFwdItemRows;   // query rows per item (256)
 constexpr int BN = kFwdTileK;      // keys per step (128)
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;      // three warpgroups (see the register split below)
+// Register split: the block launches with kThreads x kLaunchRegs registers
+// (the kernel's register count under __launch_bounds__(kThreads, 1)); the
+// first warpgroup (TMA producer, MMA issuer, two idle warps) keeps
+// kRegsControl per thread and gives the rest to the two softmax warpgroups.
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsControl = 104, kRegsSoftmax = 200;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kLaunchRegs, "register split exceeds the block");
 constexpr int kPanel = 128 * 128;  // 128 rows x 128 bytes (64 bf16)
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -233,8 +243,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int grid = gridDim.x, cta = blockIdx.x;
   const int64_t n_items = p.n_items;
 
+  // (each role sets its warpgroup's register budget first, inside its own
+  // branch, so that every role's code is compiled with its own budget)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    setmaxnreg_dec<kRegsControl>();
     if (lane == 0) {
       tma_prefetch_desc(&tQc); tma_prefetch_desc(&tQn); tma_prefetch_desc(&tKc);
       tma_prefetch_desc(&tKn); tma_prefetch_desc(&tVc); tma_prefetch_desc(&tVn);
@@ -275,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    setmaxnreg_dec<kRegsControl>();
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(BM, BN, false, false);
       constexpr uint32_t kIdO = idesc_bf16(BM, HD, false, true);
@@ -343,9 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++itn;
       }
     }
+  } else if (warp < 4) {
+    setmaxnreg_dec<kRegsControl>();  // warps 2 and 3: no role
   } else {
     // ------------------------------------------------------------ softmax (thread = row of sub-tile t)
-    const int t = (warp - 2) >> 2;
+    setmaxnreg_inc<kRegsSoftmax>();
+    const int t = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t tl = (uint32_t)(quarter * 32) << 16;
@@ -444,12 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // loaded again (layout of p_col)
         const uint64_t sl2x2 = f2(sl2, sl2), nm2 = f2(nm, nm);
         uint64_t rs = exp_store64(h0, h1, sl2x2, nm2, tS + 64);
-        tmem_ld32x2(tS, tS + 32, a0, a1);
-        // (lo, hi made opaque so that the compiler recomputes this mask
-        // instead of keeping the first pass's 64 predicates alive)
-        asm volatile("" : "+r"(lo), "+r"(hi));
-        if (!full) mask64(a0, a1, 0, lo, hi);
-        rs = f2_add(rs, exp_store64(a0, a1, sl2x2, nm2, tS));
+        rs = f2_add(rs, exp_store64(a0, a1, sl2x2, nm2, tS));  // keys [0, 64), masked in pass 1
         float r0, r1;
         f2_split(rs, r0, r1);
         l = l * alpha + (r0 + r1);
@@ -535,7 +547,12 @@ template <int HD, bool VL, bool FIXREF, bool ROWS = false>
 cudaError_t launch_fwd_t(const FwdMaps& maps, const FwdParams& p, const VarlenTabs& vt, const FwdRef& ref,
                          const RowRange& rows, int grid, cudaStream_t stream) {
   auto k = bdlm_fwd_tc_kernel<HD, VL, FIXREF, ROWS>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<HD>::kAlloc);
+  // the register split needs the block's full allotment: refuse to launch otherwise
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, k);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs * kThreads < 128 * kRegsControl + 256 * kRegsSoftmax) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<HD>::kAlloc);
   if (e != cudaSuccess) return e;
   k<<<grid, kThreads, Layout<HD>::kAlloc, stream>>>(maps.Qc, maps.Qn, maps.Kc, maps.Kn, maps.Vc, maps.Vn, p, vt,
                                                     ref, rows);
