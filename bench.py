@@ -393,6 +393,92 @@ def run_native(args, rank, world, local_rank):
     return line
 
 
+class _OneRank:
+    """The exchange of a single rank (no process group): its own shard."""
+    rank, world = 0, 1
+
+    def all_gather(self, x):
+        return [x]
+
+    def sum_to_owner(self, x, owner):
+        return x
+
+
+def run_csbp(args, rank, world, local_rank):
+    """Multi-rank CSBP, strong scaling: one sequence of the workload split
+    over the ranks by the balanced plan of
+    structured_mask_attention_gb300.csbp (rank r: clean slice r, corrupted
+    slice R - 1 - r), each rank computing its rows with the rank-local calls
+    (gathered schedule), the clean K / V all-gathered and the clean dK / dV
+    summed onto their owners through torch.distributed (NCCL).  The step
+    time, exchange included, is the maximum over ranks of each rank's
+    CUDA-event time; the rate counts the whole sequence's useful FLOP."""
+    import torch
+    import torch.distributed as dist
+
+    import structured_mask_attention_gb300 as m
+    from structured_mask_attention_gb300 import csbp
+    from structured_mask_attention_gb300.inputs import WORKLOADS, make_torch
+
+    m.load_library()
+    w = WORKLOADS[args.workload]
+    L, B, Hq, Hkv, d = w["L"], w["B"], w["Hq"], w["Hkv"], w["d"]
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    plan = csbp.CSBPPlan.build(L, B, world)
+    rw = plan.rows(rank)
+    # the same seeded sequence on every rank; each keeps only its own rows
+    X = make_torch(L, Hq, Hkv, d, seed=0, device=dev)
+    c, n = slice(rw.c0 * B, rw.c1 * B), slice(rw.n0 * B, rw.n1 * B)
+    local = {k: X[k][c].clone() for k in ("Qc", "Kc", "Vc", "dOc")}
+    local.update({k: X[k][n].clone() for k in ("Qn", "Kn", "Vn", "dOn")})
+    del X
+    torch.cuda.empty_cache()
+    comm = csbp.TorchComm() if world > 1 else _OneRank()
+    comp = csbp.KernelCompute(m, plan, rank, local, 1.0 / math.sqrt(d))
+
+    def step():
+        shards = csbp.gather_clean_kv(comm, local["Kc"], local["Vc"])
+        o = csbp.forward(plan, comm, comp, shards, gathered=True)
+        return csbp.backward(plan, comm, comp, shards, o, (local["dOc"], local["dOn"]), gathered=True)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats(dev)
+    clocks = ClockSampler(local_rank)
+    barrier()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = job_time_ms(ev0.elapsed_time(ev1), world, dev)
+    peak = torch.tensor([torch.cuda.max_memory_allocated(dev) / 2 ** 30], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(peak, op=dist.ReduceOp.MAX)
+    ms_step = ms / args.steps
+    value = useful_flops(L, B, Hq, d) / (ms_step * 1e-3) / 1e12
+    return {"metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True,
+            "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1), bf16)",
+            "config": {"workload": args.workload, "L": L, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d,
+                       "parallelism": "csbp%d" % world, "assignment": "mirror", "schedule": "gathered",
+                       "exchange": "torch.distributed (NCCL)" if world > 1 else "none (one rank)"},
+            "tokens_per_s": round(2 * L / (ms_step * 1e-3), 1),
+            "peak_gib_per_rank": round(float(peak.item()), 3), "clocks": clk}
+
+
 def per_rank_memory(L, Hq, Hkv, d, R):
     """Attention tensors one of R ranks holds for a fwd+bwd step (GiB), by
     the shapes alone: bf16 Q, O, dO and fp32 dQ per query head; bf16 K, V and
@@ -837,6 +923,10 @@ def main():
                          "schedule ablation (BDLM_SCHED=naive vs longest first) and the sharded-256k "
                          "block-size sweep with merge and preprocess bandwidth, and packed batches "
                          "(one packed call vs one call per sequence)")
+    ap.add_argument("--csbp", action="store_true",
+                    help="multi-rank CSBP instead of replicas: one sequence split over the --gpus ranks "
+                         "(balanced plan, rank-local calls, clean K/V all-gathered and clean dK/dV reduced "
+                         "over NCCL); strong scaling")
     ap.add_argument("--sweep-parts", default="config,sharded,shardcheck,packed,ranks,oracle",
                     help="comma-separated parts of --sweep to run (config includes the schedule ablation; "
                          "shardcheck: sharded vs unsharded fp32 output differences, production path and "
@@ -861,7 +951,7 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    line = run_native(args, rank, world, local_rank)
+    line = run_csbp(args, rank, world, local_rank) if args.csbp else run_native(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
