@@ -438,12 +438,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           hi = max(min((cs ? hi_c : hi_n) - key0, BN + 1), -1);
         }
         uint32_t a0[32], a1[32], h0[32], h1[32];
-        tmem_ld32x2(tS, tS + 32, a0, a1);
-        if (!full) mask64(a0, a1, 0, lo, hi);
-        const float mx01 = max64(a0, a1);
-        tmem_ld32x2(tS + 64, tS + 96, h0, h1);
-        if (!full) mask64(h0, h1, 64, lo, hi);
-        const float mx = fmaxf(mx01, max64(h0, h1));
+        tmem_ld32x4(tS, a0, a1, h0, h1);  // the row's 128 scores, one wait
+        if (!full) {
+          mask64(a0, a1, 0, lo, hi);
+          mask64(h0, h1, 64, lo, hi);
+        }
+        const float mx = fmaxf(max64(a0, a1), max64(h0, h1));
         const float mx2 = mx * sl2;
         bool rescale = false;
         float alpha = 1.f, m_use = m_ref;
