@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           hi = max(min((cs ? hi_c : hi_n) - key0, BN + 1), -1);
         }
         uint32_t a0[32], a1[32], h0[32], h1[32];
-        tmem_ld32x4(tS, a0, a1, h0, h1);  // the row's 128 scores, one wait
+        tmem_ld32x4(tS, tS + 32, tS + 64, tS + 96, a0, a1, h0, h1);  // the row's 128 scores, one wait
         if (!full) {
           mask64(a0, a1, 0, lo, hi);
           mask64(h0, h1, 64, lo, hi);

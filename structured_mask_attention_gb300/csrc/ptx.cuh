@@ -232,10 +232,9 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t (
       : "memory");
 }
 
-// 128 consecutive columns (32 lanes x 32 bit) in four loads and one wait:
-// a row's columns [0, 32), [32, 64), [64, 96), [96, 128) from taddr.
-__device__ __forceinline__ void tmem_ld32x4(uint32_t taddr, uint32_t (&a)[32], uint32_t (&b)[32], uint32_t (&c)[32],
-                                            uint32_t (&e)[32]) {
+// Four 32-column loads (32 lanes x 32 bit) from ta, tb, tc, td and one wait.
+__device__ __forceinline__ void tmem_ld32x4(uint32_t ta, uint32_t tb, uint32_t tc, uint32_t td, uint32_t (&a)[32],
+                                            uint32_t (&b)[32], uint32_t (&c)[32], uint32_t (&e)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
       "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%128];\n\t"
@@ -262,7 +261,7 @@ __device__ __forceinline__ void tmem_ld32x4(uint32_t taddr, uint32_t (&a)[32], u
         "=r"(e[8]), "=r"(e[9]), "=r"(e[10]), "=r"(e[11]), "=r"(e[12]), "=r"(e[13]), "=r"(e[14]), "=r"(e[15]),
         "=r"(e[16]), "=r"(e[17]), "=r"(e[18]), "=r"(e[19]), "=r"(e[20]), "=r"(e[21]), "=r"(e[22]), "=r"(e[23]),
         "=r"(e[24]), "=r"(e[25]), "=r"(e[26]), "=r"(e[27]), "=r"(e[28]), "=r"(e[29]), "=r"(e[30]), "=r"(e[31])
-      : "r"(taddr), "r"(taddr + 32), "r"(taddr + 64), "r"(taddr + 96));
+      : "r"(ta), "r"(tb), "r"(tc), "r"(td));
 }
 
 // 4-byte asynchronous global -> shared copy (zero-filled when !pred).
