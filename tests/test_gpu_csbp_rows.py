@@ -383,3 +383,14 @@ def test_csbp_driver_nccl_single_rank(gathered):
     assert p.exitcode == 0
     assert err <= 2e-2, err
     assert lerr <= 1e-3, lerr
+
+
+def test_bench_csbp_mode_one_rank(lib):
+    """bench.py --csbp at one rank (no process group): the multi-rank CSBP
+    step runs end to end through the driver and reports a sane line."""
+    import argparse
+    import bench
+    args = argparse.Namespace(workload="profile-16k", steps=1, warmup=3)
+    line = bench.run_csbp(args, 0, 1, 0)
+    assert line["config"]["parallelism"] == "csbp1" and line["scaling"] == "strong"
+    assert line["ms_per_step"] > 0 and line["value"] > 0 and line["peak_gib_per_rank"] > 0
