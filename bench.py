@@ -613,7 +613,7 @@ def run_sweep(args):
               "tokens_per_s": round(2 * L / (tot * 1e-3), 1), "pct_of_peak": round(100 * useful / peak_tf, 2),
               "peak": peak_src, "reps": reps})
         if name == "long-128k":
-            # schedule ablation: natural order + round robin vs longest first + boustrophedon
+            # schedule ablation: natural order + round robin vs longest first, claimed in list order
             step = lambda: (m.bdlm_attn_fwd(*ins, B, sc, out=f),
                             m.bdlm_attn_bwd(*ins, f[0], f[1], X["dOc"], X["dOn"], f[2], f[3], B, sc, out=g))
             res = {}

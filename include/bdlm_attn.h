@@ -34,6 +34,8 @@
  *  - Memory.  Every pointer is a device pointer owned by the caller, who also
  *    owns the workspace (size from bdlm_workspace_size).  The library
  *    allocates and frees nothing.  Device pointers must be 16-byte aligned.
+ *    A workspace serves one call at a time: calls that may overlap on the
+ *    GPU (different streams, no ordering) need workspaces of their own.
  *  - Execution.  Calls enqueue work on `stream` and return without waiting.
  *  - Validation.  Arguments are checked on the host before anything is
  *    enqueued; a failing check returns a non-OK status, enqueues nothing and
@@ -78,8 +80,11 @@ typedef void* bdlm_stream;
 
 /* Workspace bytes a call of kind `op` needs at this shape (P is ignored by
  * every op today and kept for shard-count dependent variants).  The
- * workspace holds the status word (first 4 bytes) and, for BDLM_OP_BWD, the
- * row statistic D of both streams.  Returns 0 for an invalid shape. */
+ * workspace holds a 256-byte header (the status word in its first 4 bytes,
+ * then the counters from which the kernels' persistent CTAs claim work
+ * items; every call zeroes what it uses before its first kernel) and, for
+ * BDLM_OP_BWD, the row statistic D of both streams.  Returns 0 for an
+ * invalid shape. */
 size_t bdlm_workspace_size(int op, int64_t L, int64_t B, int Hq, int Hkv, int d, int P);
 
 /* Two-stream forward (arxiv.science abstract; the mask above).
@@ -185,7 +190,8 @@ bdlm_status bdlm_attn_bwd(const void* Qc, const void* Kc, const void* Vc,
  *    library's device code, so make the first call before any stream
  *    capture.
  *  - Every call shares the one array per device and leaves its contents
- *    behind; each call clears the status word and rewrites D before use.
+ *    behind; each call clears the status word and the work counters and
+ *    rewrites D before use.
  *    Calls that overlap on the GPU (different streams, no ordering) race on
  *    the array and must not be issued.
  *  - No cudaMalloc, cudaFree or allocating library routine is called.  With

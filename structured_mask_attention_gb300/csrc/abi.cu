@@ -102,7 +102,8 @@ bdlm_status cuda_fail(cudaError_t e, const char* what) {
   return fail(BDLM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-constexpr size_t kWsHeader = 256;  // status word + padding
+constexpr size_t kWsHeader = 256;  // status word, the kernels' work counters, padding
+static_assert(kHeaderClearBytes <= (int)kWsHeader, "header words outside the header");
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -221,7 +222,7 @@ uint64_t wait_limit_ns() {
 }
 
 // BDLM_SCHED=naive: work items in natural order, round robin over the grid
-// (the load-balancing ablation); otherwise longest first, boustrophedon.
+// (the load-balancing ablation); otherwise longest first, claimed in list order.
 // Read on every call, so one process can time both.
 int naive_schedule() {
   const char* s = std::getenv("BDLM_SCHED");
@@ -229,7 +230,7 @@ int naive_schedule() {
 }
 
 bdlm_status clear_status(void* ws, cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(ws, 0, 4, st);
+  cudaError_t e = cudaMemsetAsync(ws, 0, kHeaderClearBytes, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
   return BDLM_OK;
 }

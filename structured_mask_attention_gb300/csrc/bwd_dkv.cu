@@ -20,6 +20,7 @@
 // dS^T from dP^T, which releases dK(k) and dP^T(k+1).  With every MMA at
 // N = 128 the pipe stays busy while either half of the elementwise work runs.
 #include "bwd_common.cuh"
+#include "sched.cuh"
 
 namespace bdlm {
 namespace {
@@ -31,7 +32,11 @@ constexpr int KBN = 128;  // query rows per step
 constexpr int QNS = 2;    // Q/dO stages
 
 enum { KV_KF = 0, KV_KE = 1, KV_QF = 2, KV_QE = 4, KV_SF = 6, KV_DPF = 7, KV_PF = 8, KV_DSF = 9, KV_ACCDONE = 10,
-       KV_ACCE = 11, KV_NBAR = 12 };
+       KV_ACCE = 11,
+       KV_IF = 12, KV_IE = 12 + kRingSlots, KV_NBAR = 12 + 2 * kRingSlots };
+// The 256 bytes after the tiles: barriers, the TMEM address, the abort flag,
+// the work-item ring's slots.
+static_assert(8 * KV_NBAR + 8 + 8 * kRingSlots <= 256, "barrier area overflows");
 
 template <int HD>
 struct DkvLayout {
@@ -192,6 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + LY::kBar + 8 * KV_NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + LY::kBar + 8 * KV_NBAR + 4);
   auto BAR = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+  const ItemRing ring{BAR(KV_IF), BAR(KV_IE),
+                      reinterpret_cast<volatile int64_t*>(base_ptr + LY::kBar + 8 * KV_NBAR + 8)};
   const Role R = role();
 
   if (threadIdx.x == 0) {
@@ -207,6 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(KV_DSF), kEwThreads);
     mbar_init(BAR(KV_ACCDONE), 1);
     mbar_init(BAR(KV_ACCE), kEwThreads);
+    for (int s = 0; s < kRingSlots; ++s) {
+      mbar_init(BAR(KV_IF + s), 1);
+      mbar_init(BAR(KV_IE + s), 1 + kEwThreads);  // the MMA thread and every elementwise thread
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -227,7 +238,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t itn = 0, qc = 0;
     bool ok = true;
     for (int64_t rnd = 0; ok; ++rnd) {
-      const int64_t idx = sched_item(p.g, rnd, cta, grid);
+      // lane 0 claims and publishes the item; the warp takes it from lane 0
+      int64_t idx = 0;
+      if (R.lane == 0) {
+        idx = claim_item(p.g, status + kSchedWordDkv, rnd, cta, grid);
+        ok = ring_put(ring, rnd, idx, wd, 93);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      if (!ok) break;
       if (idx >= n_items) break;
       const DkvGeo t = dkv_geo<VL, ROWS>(p, vt, idx);
       if (t.n == 0) continue;
@@ -298,7 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t itn = 0, qc = 0;
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
-        const int64_t idx = sched_item(p.g, rnd, cta, grid);
+        int64_t idx;
+        if (!ring_get(ring, rnd, idx, wd, 94)) { ok = false; break; }
         if (idx >= n_items) break;
         const DkvGeo t = dkv_geo<VL, ROWS>(p, vt, idx);
         if (t.n == 0) continue;
@@ -365,7 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     const uint64_t sl2x2 = f2(p.scale_log2, p.scale_log2), nlog2e = f2(-kLog2e, -kLog2e);
     for (int64_t rnd = 0; ok; ++rnd) {
-      const int64_t idx = sched_item(p.g, rnd, cta, grid);
+      int64_t idx;
+      if (!ring_get(ring, rnd, idx, wd, 95)) { ok = false; break; }
       if (idx >= n_items) break;
       const DkvGeo t = dkv_geo<VL, ROWS>(p, vt, idx);
       if (t.n == 0) continue;
@@ -482,6 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
+  if (threadIdx.x == 0) sched_release(status + kSchedWordDkv, grid);
   if (*abort_flag) drain_after_abort(200);
   if (R.warp == 1) {
     tc_fence_after();

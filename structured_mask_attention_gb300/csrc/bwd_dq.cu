@@ -19,6 +19,7 @@
 // next reuses a buffer is issued after the dQ MMA reading its dS (the tensor
 // pipe runs in issue order).  Every output row is written once.
 #include "bwd_common.cuh"
+#include "sched.cuh"
 
 namespace bdlm {
 namespace {
@@ -31,7 +32,10 @@ constexpr int KNS = 3;    // K stages
 constexpr int VNS = 2;    // V stages
 
 enum { DQ_QF = 0, DQ_QE = 1, DQ_KF = 2, DQ_KE = 5, DQ_VF = 8, DQ_VE = 10, DQ_DPF = 12, DQ_DPFREE = 13,
-       DQ_DSF = 14, DQ_DONE = 16, DQ_OE = 17, DQ_NBAR = 18 };
+       DQ_DSF = 14, DQ_DONE = 16, DQ_OE = 17, DQ_IF = 18, DQ_IE = 18 + kRingSlots, DQ_NBAR = 18 + 2 * kRingSlots };
+// The 256 bytes after the tiles: barriers, the TMEM address, the abort flag,
+// the work-item ring's slots.
+static_assert(8 * DQ_NBAR + 8 + 8 * kRingSlots <= 256, "barrier area overflows");
 
 template <int HD>
 struct DqLayout {
@@ -113,6 +117,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + LY::kBar + 8 * DQ_NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + LY::kBar + 8 * DQ_NBAR + 4);
   auto BAR = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+  const ItemRing ring{BAR(DQ_IF), BAR(DQ_IE),
+                      reinterpret_cast<volatile int64_t*>(base_ptr + LY::kBar + 8 * DQ_NBAR + 8)};
   const Role R = role();
 
   if (threadIdx.x == 0) {
@@ -131,6 +137,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(DQ_DPFREE), kEwThreads);
     mbar_init(BAR(DQ_DONE), 1);
     mbar_init(BAR(DQ_OE), kEwThreads);
+    for (int s = 0; s < kRingSlots; ++s) {
+      mbar_init(BAR(DQ_IF + s), 1);
+      mbar_init(BAR(DQ_IE + s), 1 + kEwThreads);  // the MMA thread and every elementwise thread
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -153,7 +163,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t itn = 0, g = 0;  // items with work, global step count
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
-        const int64_t idx = sched_item(p.g, rnd, cta, grid);
+        const int64_t idx = claim_item(p.g, status + kSchedWordDq, rnd, cta, grid);
+        if (!ring_put(ring, rnd, idx, wd, 96)) { ok = false; break; }
         if (idx >= n_items) break;
         const DqGeo t = dq_geo<VL, ROWS>(p, vt, idx);
         if (t.n == 0) continue;
@@ -198,7 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ks = 0, kph = 0;  // K stage of step g and its phase parity
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
-        const int64_t idx = sched_item(p.g, rnd, cta, grid);
+        int64_t idx;
+        if (!ring_get(ring, rnd, idx, wd, 97)) { ok = false; break; }
         if (idx >= n_items) break;
         const DqGeo t = dq_geo<VL, ROWS>(p, vt, idx);
         if (t.n == 0) continue;
@@ -264,7 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t itn = 0, g = 0;
     bool ok = true;
     for (int64_t rnd = 0; ok; ++rnd) {
-      const int64_t idx = sched_item(p.g, rnd, cta, grid);
+      int64_t idx;
+      if (!ring_get(ring, rnd, idx, wd, 98)) { ok = false; break; }
       if (idx >= n_items) break;
       const DqGeo t = dq_geo<VL, ROWS>(p, vt, idx);
       // (one sequence: its length and offset come from the parameters)
@@ -355,6 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
+  if (threadIdx.x == 0) sched_release(status + kSchedWordDq, grid);
   if (*abort_flag) drain_after_abort(200);
   if (R.warp == 1) {
     tc_fence_after();

@@ -45,6 +45,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "sched.cuh"
 
 namespace bdlm {
 namespace {
@@ -66,7 +67,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 enum { B_QF = 0, B_QE = 1, B_KF = 2, B_KE = 4, B_VF = 6, B_VE = 8, B_SF = 10, B_PF = 12, B_OD = 14, B_OE = 16,
-       B_COUNT = 18 };
+       B_IF = 18, B_IE = 18 + kRingSlots, B_COUNT = 18 + 2 * kRingSlots };
+// The 256 bytes after the tiles: barriers, the TMEM address, the abort flag,
+// the work-item ring's slots.
+static_assert(8 * B_COUNT + 8 + 8 * kRingSlots <= 256, "barrier area overflows");
 
 template <int HD>
 struct Layout {
@@ -212,6 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + LY::kBar + 8 * B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + LY::kBar + 8 * B_COUNT + 4);
   auto BAR = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+  const ItemRing ring{BAR(B_IF), BAR(B_IE),
+                      reinterpret_cast<volatile int64_t*>(base_ptr + LY::kBar + 8 * B_COUNT + 8)};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -227,6 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(B_PF + s), 128);
       mbar_init(BAR(B_OD + s), 1);
       mbar_init(BAR(B_OE + s), 128);
+    }
+    for (int s = 0; s < kRingSlots; ++s) {
+      mbar_init(BAR(B_IF + s), 1);
+      mbar_init(BAR(B_IE + s), 1 + 256);  // the MMA thread and every softmax thread
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -254,7 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t itn = 0, kc = 0;
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
-        const int64_t idx = sched_item(p.g, rnd, cta, grid);
+        const int64_t idx = claim_item(p.g, p.status + kSchedWordFwd, rnd, cta, grid);
+        if (!ring_put(ring, rnd, idx, wd, 90)) { ok = false; break; }
         if (idx >= n_items) break;
         const ItemGeo g = item_geo<VL, ROWS>(p, vt, rows, idx);
         if (g.n == 0) continue;
@@ -314,7 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t itn = 0, kc = 0;
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
-        const int64_t idx = sched_item(p.g, rnd, cta, grid);
+        int64_t idx;
+        if (!ring_get(ring, rnd, idx, wd, 91)) { ok = false; break; }
         if (idx >= n_items) break;
         const ItemGeo g = item_geo<VL, ROWS>(p, vt, rows, idx);
         if (g.n == 0) continue;
@@ -370,7 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t sc = 0, itn = 0;
     bool ok = true;
     for (int64_t rnd = 0; ok; ++rnd) {
-      const int64_t idx = sched_item(p.g, rnd, cta, grid);
+      int64_t idx;
+      if (!ring_get(ring, rnd, idx, wd, 92)) { ok = false; break; }
       if (idx >= n_items) break;
       const ItemGeo g = item_geo<VL, ROWS>(p, vt, rows, idx);
       // (one sequence: its length and offset come from the parameters, so
@@ -534,6 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
+  if (threadIdx.x == 0) sched_release(p.status + kSchedWordFwd, grid);
   if (*abort_flag) drain_after_abort(200);
   if (warp == 1) {
     tc_fence_after();

@@ -350,9 +350,8 @@ BDLM_HD int sweep_rotation(int64_t idx, int nc) {
 }
 
 // Below this many key tiles per key stream (six grid rounds) the dK/dV list
-// stays tile-major: blocks then cover tiles of very different lengths and
-// unbalance the grid (host simulation of the snake assignment: 32 % spread
-// at L = 16k).
+// stays tile-major: blocks would then cover tiles of very different lengths,
+// and the long items of a late block can end after everything else.
 BDLM_HD int64_t kv_blocked_min_tiles(const Geom& g) { return 6 * (int64_t)g.round_items; }
 
 // The geometry of one sequence of a packed batch: rows [off, off + L) of the
@@ -364,20 +363,6 @@ BDLM_HD Geom seq_geom(const Geom& all, int64_t L) {
   g.kv_end = L;
   g.include_local = 1;
   return g;
-}
-
-// Persistent-grid assignment: CTA `cta` of `grid` takes, in round r, the item
-// r*grid + cta on even rounds and r*grid + (grid-1-cta) on odd rounds.  Over
-// a longest-first list this boustrophedon order evens the CTAs' totals.
-BDLM_HD int64_t snake_item(int64_t round, int cta, int grid) {
-  const int pos = (round & 1) ? (grid - 1 - cta) : cta;
-  return round * grid + pos;
-}
-
-// Item of CTA `cta` in round r: the boustrophedon order above, or plain
-// round robin for the natural-order schedule (load-balancing ablation).
-BDLM_HD int64_t sched_item(const Geom& g, int64_t round, int cta, int grid) {
-  return g.naive_order ? round * grid + cta : snake_item(round, cta, grid);
 }
 
 // dK/dV work items: (key stream, key/value head, key tile).  Clean key tiles
@@ -429,8 +414,7 @@ BDLM_HD KVItem kv_item(const Geom& g, int tk, int64_t idx) {
     return it;
   }
   // long range: blocks of g.round_items tiles, one KV head after the other
-  // inside a block; a block of one head is one grid round, and the snake
-  // assignment pairs each round's long items with the next round's short ones
+  // inside a block; a block of one head is about one grid round
   const int64_t R = g.round_items;
   const int64_t bi = i / (R * g.Hkv);
   const int64_t t0 = bi * R;

@@ -53,6 +53,13 @@ struct FwdRef {
   const float* n;
 };
 
+// Words (uint32) of the workspace header that the kernels use: word 0 is the
+// status word; from kSchedWordFwd / Dkv / Dq on, each attention kernel's work
+// item counter and its count of finished CTAs (two words each; sched.cuh).
+// The host zeroes the first kHeaderClearBytes of the header before each call.
+constexpr int kSchedWordFwd = 8, kSchedWordDkv = 10, kSchedWordDq = 12;
+constexpr int kHeaderClearBytes = 64;
+
 // Tile sizes of the tensor-core forward: items of 256 query rows (two
 // 128-row sub-tiles sharing their key tiles), 128 keys per step.
 constexpr int kFwdTileQ = 128;

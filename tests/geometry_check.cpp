@@ -5,6 +5,9 @@
 // exits non-zero if any.
 #include <cstdio>
 #include <cstdlib>
+#include <functional>
+#include <queue>
+#include <utility>
 #include <vector>
 
 #include "geometry.cuh"
@@ -121,19 +124,22 @@ static void check_kv(const Geom& g, int tk) {
   }
 }
 
-// The persistent grid's assignment visits every list index once.
-static void check_sched(const Geom& g, int grid, int64_t rounds) {
-  std::vector<unsigned char> seen((size_t)(grid * rounds), 0);
-  for (int64_t r = 0; r < rounds; ++r)
-    for (int c = 0; c < grid; ++c) {
-      const int64_t idx = sched_item(g, r, c, grid);
-      const bool ok = idx >= r * grid && idx < (r + 1) * grid;
-      CHECK(ok, "sched round %lld cta %d -> %lld", (long long)r, c, (long long)idx);
-      if (ok) {
-        CHECK(!seen[(size_t)idx], "sched index %lld repeated", (long long)idx);
-        seen[(size_t)idx] = 1;
-      }
-    }
+// Per-CTA totals when the persistent CTAs claim a list's items in order,
+// each item going to the CTA that becomes free first (the kernels' dynamic
+// claiming, every CTA equally fast, ties to the lowest index).  With this
+// greedy rule no CTA ends more than one item's cost after another.
+static std::vector<double> claim_totals(const std::vector<double>& costs, int grid) {
+  typedef std::pair<double, int> Slot;
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
+  for (int c = 0; c < grid; ++c) free_at.push(Slot(0.0, c));
+  std::vector<double> tot((size_t)grid, 0.0);
+  for (double cost : costs) {
+    const Slot s = free_at.top();
+    free_at.pop();
+    tot[(size_t)s.second] = s.first + cost;
+    free_at.push(Slot(tot[(size_t)s.second], s.second));
+  }
+  return tot;
 }
 
 // Brute-force visibility (the mask, with the call's key restriction and,
@@ -201,19 +207,16 @@ static void check_ranges(const Geom& g, int t) {
     }
 }
 
-// Per-CTA totals of the persistent assignment over a work list, with the
-// list's own costs (visible key tiles of a query item; query rows reading a
-// key tile): the boustrophedon order over a longest-first (or blocked) list
-// keeps every CTA within `slack` items' worth of the mean.
+// Per-CTA totals of the dynamic claiming over a work list, with the list's
+// own costs (visible key tiles of a query item; query rows reading a key
+// tile): over a longest-first (or blocked) list every CTA ends within
+// max_over_mean of the mean, and within one item of every other CTA.
 static void check_balance(const Geom& g, int grid, bool kv, double max_over_mean) {
   const int tq = 256, tk = 128;
   const int64_t n = kv ? kv_items(g, tk) : q_items(g, tq);
-  std::vector<double> tot((size_t)grid, 0.0);
+  std::vector<double> costs;
   double cmax = 0.0, sum = 0.0;
-  for (int64_t r = 0; r * grid < n; ++r)
-    for (int c = 0; c < grid; ++c) {
-      const int64_t idx = sched_item(g, r, c, grid);
-      if (idx >= n) continue;
+  for (int64_t idx = 0; idx < n; ++idx) {
       double cost;
       if (kv) {
         const KVItem it = kv_item(g, tk, idx);
@@ -226,16 +229,17 @@ static void check_balance(const Geom& g, int grid, bool kv, double max_over_mean
         const QTileRanges q = qtile_ranges(g, it.stream, r0, imin64(r0 + tq, g.L), tk);
         cost = (double)((q.c1 - q.c0) + (q.n1 - q.n0));
       }
-      tot[(size_t)c] += cost;
+      costs.push_back(cost);
       cmax = cost > cmax ? cost : cmax;
       sum += cost;
-    }
+  }
+  const std::vector<double> tot = claim_totals(costs, grid);
   double mx = 0.0, mn = 1e300;
   for (double t : tot) { mx = t > mx ? t : mx; mn = t < mn ? t : mn; }
   const double mean = sum / grid;
   CHECK(mx <= mean * max_over_mean, "balance %s grid=%d L=%lld: max %.0f mean %.0f (ratio %.4f)", kv ? "kv" : "q",
         grid, (long long)g.L, mx, mean, mx / mean);
-  CHECK(mx - mn <= 2 * cmax, "spread %s grid=%d L=%lld: max %.0f min %.0f item %.0f", kv ? "kv" : "q", grid,
+  CHECK(mx - mn <= cmax, "spread %s grid=%d L=%lld: max %.0f min %.0f item %.0f", kv ? "kv" : "q", grid,
         (long long)g.L, mx, mn, cmax);
 }
 
@@ -244,20 +248,18 @@ static void check_balance(const Geom& g, int grid, bool kv, double max_over_mean
 static void check_balance_rows(const Geom& g, const RowRange& rows, int grid, int tq) {
   const int tk = 128;
   const int64_t n = q_items_rows(g, rows, tq);
-  std::vector<double> tot((size_t)grid, 0.0);
+  std::vector<double> costs;
   double sum = 0.0, cmax = 0.0;
-  for (int64_t r = 0; r * grid < n; ++r)
-    for (int c = 0; c < grid; ++c) {
-      const int64_t idx = sched_item(g, r, c, grid);
-      if (idx >= n) continue;
-      const QItem it = q_item_rows(g, rows, tq, idx);
-      const int64_t r0 = it.qtile * tq;
-      const QTileRanges q = qtile_ranges(g, it.stream, r0, imin64(r0 + tq, g.L), tk);
-      const double cost = (double)((q.c1 - q.c0) + (q.n1 - q.n0));
-      tot[(size_t)c] += cost;
-      sum += cost;
-      cmax = cost > cmax ? cost : cmax;
-    }
+  for (int64_t idx = 0; idx < n; ++idx) {
+    const QItem it = q_item_rows(g, rows, tq, idx);
+    const int64_t r0 = it.qtile * tq;
+    const QTileRanges q = qtile_ranges(g, it.stream, r0, imin64(r0 + tq, g.L), tk);
+    const double cost = (double)((q.c1 - q.c0) + (q.n1 - q.n0));
+    costs.push_back(cost);
+    sum += cost;
+    cmax = cost > cmax ? cost : cmax;
+  }
+  const std::vector<double> tot = claim_totals(costs, grid);
   double mx = 0.0;
   for (double t : tot) mx = t > mx ? t : mx;
   CHECK(mx <= sum / grid + 2 * cmax, "rows balance grid=%d L=%lld tq=%d rows c[%d,%d) n[%d,%d): max %.0f mean %.0f item %.0f",
@@ -298,8 +300,6 @@ int main() {
         }
         Geom g{L, B, 16, 8, 0, L, 1};
         g.naive_order = naive;
-        check_sched(g, 152, 7);
-        check_sched(g, 37, 5);
       }
   // the work-order blocking follows the grid: one round of the persistent
   // grid per block, for devices of 132, 148 and 152 SMs
@@ -317,7 +317,6 @@ int main() {
         gs.include_local = 0;
         check_kv(gs, 128);
         check_q(gs, 128);
-        check_sched(g, grid, 9);
         if (L >= 131072) {
           check_balance(g, grid, false, 1.02);
           check_balance(g, grid, true, 1.05);

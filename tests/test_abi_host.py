@@ -5,7 +5,7 @@ tiles (checked against the oracle's explicit mask)."""
 from __future__ import annotations
 
 import ctypes
-import math
+import heapq
 
 import numpy as np
 import pytest
@@ -139,21 +139,22 @@ def test_worklist_covers_exactly_visible_tiles(lib, L, B, Hq, Hkv, tq, tk, kb, k
             assert costs[i] <= max(costs[:i]) + slack
 
 
-def test_snake_assignment_balances_clean_costs(lib):
-    """The persistent kernels give CTA c items c, 2G-1-c, 2G+c, ... of the
-    longest-first list; per-CTA totals stay within one item of each other."""
+def test_claiming_in_list_order_balances_clean_costs(lib):
+    """The persistent CTAs claim the longest-first list's items in order, each
+    item going to the CTA that is free first: per-CTA totals stay within one
+    item of each other and within 1 % of the mean."""
     L, B, Hq, Hkv = 131072, 512, 16, 8
     items = m.bdlm_worklist(L, B, Hq, Hkv)
-    costs = np.array([it[7] for it in items])
+    costs = [it[7] for it in items]
     G = 148
+    free_at = [(0, c) for c in range(G)]
     tot = np.zeros(G)
-    for r in range(math.ceil(len(costs) / G)):
-        for c in range(G):
-            pos = c if r % 2 == 0 else G - 1 - c
-            i = r * G + pos
-            if i < len(costs):
-                tot[c] += costs[i]
-    assert tot.max() - tot.min() <= costs.max()
+    for cost in costs:
+        t, c = heapq.heappop(free_at)
+        tot[c] = t + cost
+        heapq.heappush(free_at, (tot[c], c))
+    assert tot.sum() == sum(costs)
+    assert tot.max() - tot.min() <= max(costs)
     assert tot.max() / tot.mean() < 1.01
 
 

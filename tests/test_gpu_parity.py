@@ -224,6 +224,37 @@ def test_deterministic(lib):
         assert torch.equal(a, b)
 
 
+def test_work_claiming_leaves_counters_zero_and_order_free(lib, monkeypatch):
+    """The persistent CTAs claim items from counters in the workspace header
+    (words 8-13: item counter and finished-CTA count of the forward, dK/dV
+    and dQ): after each call the last CTA has zeroed them again, even when a
+    call finds them dirty (the call clears them first), and the outputs equal
+    those of the static round-robin ablation order (BDLM_SCHED=naive) bit
+    for bit, since every item writes its own outputs."""
+    m = lib
+    L, B, Hq, Hkv, d = 2048, 256, 4, 2, 128
+    X = make_numpy(L, Hq, Hkv, d, seed=13)
+    dev = {k: to_dev(v, torch) for k, v in X.items()}
+    ins = [dev[k] for k in NAMES[:6]]
+    wsf = torch.full((m.bdlm_workspace_size(m.OP_FWD, L, B, Hq, Hkv, d),), 0x5A, dtype=torch.uint8, device="cuda")
+    wsb = torch.full((m.bdlm_workspace_size(m.OP_BWD, L, B, Hq, Hkv, d),), 0x5A, dtype=torch.uint8, device="cuda")
+    outs = []
+    for naive in (False, True, False):
+        if naive:
+            monkeypatch.setenv("BDLM_SCHED", "naive")
+        f = m.bdlm_attn_fwd(*ins, B, workspace=wsf)
+        g = m.bdlm_attn_bwd(*ins, f[0], f[1], dev["dOc"], dev["dOn"], f[2], f[3], B, workspace=wsb)
+        torch.cuda.synchronize()
+        monkeypatch.delenv("BDLM_SCHED", raising=False)
+        for ws in (wsf, wsb):
+            words = ws[:64].view(torch.int32).cpu()
+            assert int(words[0]) == 0  # status word: no wait expired
+            assert words[8:14].tolist() == [0] * 6
+        outs.append([t.clone() for t in (*f, *g)])
+    for a, b, c in zip(*outs):
+        assert torch.equal(a, b) and torch.equal(a, c)
+
+
 def test_watchdog_reports_timeout(lib):
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
     assert lib.bdlm_watchdog_selftest(ws, 20000) == 7
