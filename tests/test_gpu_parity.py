@@ -228,9 +228,12 @@ def test_work_claiming_leaves_counters_zero_and_order_free(lib, monkeypatch):
     """The persistent CTAs claim items from counters in the workspace header
     (words 8-13: item counter and finished-CTA count of the forward, dK/dV
     and dQ): after each call the last CTA has zeroed them again, even when a
-    call finds them dirty (the call clears them first), and the outputs equal
-    those of the static round-robin ablation order (BDLM_SCHED=naive) bit
-    for bit, since every item writes its own outputs."""
+    call finds them dirty (the call clears them first).  Which CTA runs an
+    item does not change its outputs: two runs agree bit for bit.  The
+    natural-order ablation (BDLM_SCHED=naive, static round robin) lists the
+    items in another order, and a query item's clean-key sweep starts at a
+    tile set by its list index, so its sums run in another order: equal to
+    rounding."""
     m = lib
     L, B, Hq, Hkv, d = 2048, 256, 4, 2, 128
     X = make_numpy(L, Hq, Hkv, d, seed=13)
@@ -252,7 +255,9 @@ def test_work_claiming_leaves_counters_zero_and_order_free(lib, monkeypatch):
             assert words[8:14].tolist() == [0] * 6
         outs.append([t.clone() for t in (*f, *g)])
     for a, b, c in zip(*outs):
-        assert torch.equal(a, b) and torch.equal(a, c)
+        assert torch.equal(a, c)
+        ref = a.float()
+        assert (b.float() - ref).abs().max().item() <= 2e-2 * max(ref.abs().max().item(), 1e-6)
 
 
 def test_watchdog_reports_timeout(lib):
