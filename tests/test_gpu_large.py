@@ -164,8 +164,8 @@ def _group_oracle(X, outs, grads, kvh, G, B, sc, full_bwd, dkv_clean_blocks=()):
 
 
 def _full_size_case(m, name, lognormal=0.0, groups=(0,), n_rows=12, full_group=None, full_bwd=True,
-                    dkv_clean_blocks=()):
-    w = WORKLOADS[name]
+                    dkv_clean_blocks=(), shape=None):
+    w = shape if shape is not None else WORKLOADS[name]
     L, B, Hq, Hkv, d = w["L"], w["B"], w["Hq"], w["Hkv"], w["d"]
     G = Hq // Hkv
     X = make_torch(L, Hq, Hkv, d, seed=0, lognormal_sigma=lognormal, device="cuda")
@@ -219,6 +219,16 @@ def test_long_128k_workload(lib):
     N = WORKLOADS["long-128k"]["L"] // WORKLOADS["long-128k"]["B"]
     _full_size_case(lib, "long-128k", groups=(0, 5), n_rows=8, full_group=6, full_bwd=False,
                     dkv_clean_blocks=(0, N // 2))
+
+
+def test_head_dim_64_long_lists(lib):
+    """d = 64 (the kernels' other head size) at L = 65536, B = 512, 8/4 heads:
+    256 query tiles per stream, so the forward and dQ lists are blocked per
+    KV head, and every CTA claims many items of each list.  Invariants over
+    all heads, sampled rows of KV groups 0 and 3, tail and long-accumulation
+    dK/dV blocks."""
+    shape = {"L": 65536, "B": 512, "Hq": 8, "Hkv": 4, "d": 64}
+    _full_size_case(lib, "d64-64k", groups=(0, 3), n_rows=8, shape=shape)
 
 
 @pytest.mark.parametrize("B", SHARDED_BLOCK_SIZES)
