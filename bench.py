@@ -179,9 +179,9 @@ def sources_digest(paths):
     return h.hexdigest()[:16]
 
 
-def committed_traffic(kernel):
-    """DRAM bytes per full-size launch from the committed ncu summary, if it
-    was taken on the current kernel sources (else None)."""
+def committed_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources and on this workload (else None)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
@@ -194,6 +194,8 @@ def committed_traffic(kernel):
     if not srcs or not all(os.path.exists(os.path.join(ROOT, s)) for s in srcs):
         return None
     if sources_digest(srcs) != ent.get("sources_sha256_16"):
+        return None
+    if ent.get("workload") != workload:
         return None
     return ent.get("dram_bytes_per_launch_full")
 
@@ -285,7 +287,7 @@ def run_native(args, rank, world, local_rank):
         ev = lambda: torch.cuda.Event()
         in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
 
-        def e2e_run(nsteps):
+        def e2e_run(nsteps, spans=None):
             for i in range(nsteps):
                 si = i & 1
                 dX, fo, go = sets[si]
@@ -298,9 +300,14 @@ def run_native(args, rank, world, local_rank):
                 stream.wait_event(in_done[si])
                 if i >= 2:
                     stream.wait_event(out_done[si])
+                if spans is not None:
+                    spans.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+                    spans[-1][0].record(stream)
                 Oc, On, LSEc, LSEn = m.bdlm_attn_fwd(*[dX[k] for k in names], B, sc, out=fo, workspace=ws_f)
                 m.bdlm_attn_bwd(*[dX[k] for k in names], Oc, On, dX["dOc"], dX["dOn"], LSEc, LSEn, B, sc,
                                 out=go, workspace=ws_b)
+                if spans is not None:
+                    spans[-1][1].record(stream)
                 comp_done[si].record(stream)
                 s_out.wait_event(comp_done[si])
                 with torch.cuda.stream(s_out):
@@ -328,18 +335,25 @@ def run_native(args, rank, world, local_rank):
         k2 = max(3, args.steps)
         barrier()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        spans = []
+        e2e_clocks = ClockSampler(local_rank)
         a.record(stream)
         s_in.wait_stream(stream)
-        e2e_run(k2)
+        e2e_run(k2, spans)
         b.record(stream)
         torch.cuda.synchronize()
+        e2e_clk = e2e_clocks.stop()
+        compute_ms = statistics.median(x.elapsed_time(y) for x, y in spans)
         barrier()
         ems = job_time_ms(a.elapsed_time(b) / k2, world, dev)
         e2e = {"value": round(job_rate(useful_flops(L, B, Hq, d), world, ems) / 1e12, 3), "unit": "TFLOP/s",
                "ms_per_step": round(ems, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "tokens_per_s": round(job_rate(2 * L, world, ems), 1), "steps": k2,
                "pipelined": "uploads and downloads overlap neighbouring steps' compute (two buffer sets)",
-               "h2d_gbs_alone": round(h2d_gbs, 1), "d2h_gbs_alone": round(d2h_gbs, 1)}
+               "h2d_gbs_alone": round(h2d_gbs, 1), "d2h_gbs_alone": round(d2h_gbs, 1),
+               # the device's own time per step inside this loop (median), and the
+               # clocks while it ran: what the copies leave to the computation
+               "compute_ms_per_step": round(compute_ms, 3), "clocks": e2e_clk}
         del sets, h_in, h_out
 
     # ---- roofline of the dominant kernel
@@ -356,7 +370,7 @@ def run_native(args, rank, world, local_rank):
             # executed FLOP per launch (recomputed products included) against the sustained peak
             tf_k = alg[k] / (ms_k * 1e-3) / 1e12
             e.update({"tflops": round(tf_k, 1), "frac": round(tf_k / peak_tf, 4),
-                      "traffic": committed_traffic(k)})
+                      "traffic": committed_traffic(k, args.workload)})
         elif k == "bdlm_preprocess" and ms_k > 0:
             # one launch per stream: reads O and dO (bf16), writes D (fp32)
             e["gbs"] = round((2 * 2 * L * Hq * d + 4 * L * Hq) / (ms_k * 1e-3) / 1e9, 1)
@@ -365,7 +379,7 @@ def run_native(args, rank, world, local_rank):
     dom_ms = ktimes[dom][1] / ktimes[dom][0]
     achieved = alg[dom] / (dom_ms * 1e-3) / 1e12
     roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf,
-                "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4), "traffic": committed_traffic(dom),
+                "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4), "traffic": committed_traffic(dom, args.workload),
                 "peak_source": f"{peak_src} bf16_tflops_sustained" + (" (of measured)" if peak_src == "measured"
                                                                       else " (of fallback)"),
                 "algorithmic_flop_per_launch": alg[dom]}
