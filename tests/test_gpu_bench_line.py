@@ -1,7 +1,8 @@
 """The bench's JSON line on the small profiling workload (profile-16k,
-L = 16384), end to end: every key the line promises is there and consistent (device throughput, the roofline of
-the dominant kernel, the fp64 oracle's rate on the host, the end-to-end rate
-through the public calls with host buffers, clocks, launch count)."""
+L = 16384), end to end: every key the line promises is there and consistent
+(device throughput, the roofline of the dominant kernel, the fp64 oracle's
+rate on the host, the end-to-end rate through the public calls with host
+buffers, clocks, launch count)."""
 from __future__ import annotations
 
 import json
