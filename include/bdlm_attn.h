@@ -364,7 +364,8 @@ bdlm_status bdlm_attn_bwd_varlen(const void* Qc, const void* Kc, const void* Vc,
                                  bdlm_dtype g_dtype, void* workspace, size_t ws_bytes,
                                  bdlm_stream stream);
 
-/* Host-only: the forward work list in launch order, for inspection and tests.
+/* Host-only: the forward work list in the order the persistent CTAs claim
+ * its items, for inspection and tests.
  * One item per (query tile of tile_q rows, query head, stream), longest
  * first: query tiles from the last to the first.  With at least
  * 6 * 152 / (2 Hq / Hkv) query tiles they go in blocks of 152 / (2 Hq / Hkv)
