@@ -368,8 +368,9 @@ bdlm_status bdlm_attn_bwd_varlen(const void* Qc, const void* Kc, const void* Vc,
  * its items, for inspection and tests.
  * One item per (query tile of tile_q rows, query head, stream), longest
  * first: query tiles from the last to the first.  With at least
- * 6 * 152 / (2 Hq / Hkv) query tiles they go in blocks of 152 / (2 Hq / Hkv)
- * tiles, and inside a block the items of one KV head (its query heads, both
+ * 6 * G / (2 Hq / Hkv) query tiles they go in blocks of G / (2 Hq / Hkv)
+ * tiles (G = 152 here, a GB300's SM count; the kernels use the grid they
+ * run on), and inside a block the items of one KV head (its query heads, both
  * streams) come together, one KV head after the other, so that the items a
  * persistent grid runs at the same time read the same keys; otherwise the two
  * streams of one head are adjacent, then the heads.  Along the list the
