@@ -124,6 +124,30 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ host memory placement
+def gpu_local_cpus(dev):
+    """The CPUs of the GPU's own NUMA node, from sysfs (None if unknown).
+    Pinned host buffers allocated by a thread on one of these CPUs live in
+    the memory next to the GPU; on a node with more than one CPU socket,
+    buffers on the other socket's memory are read by the GPU's copy engines
+    at a fraction of the link's rate."""
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(dev)
+        path = "/sys/bus/pci/devices/%04x:%02x:%02x.0/local_cpulist" % (p.pci_domain_id, p.pci_bus_id,
+                                                                        p.pci_device_id)
+        with open(path) as fh:
+            txt = fh.read().strip()
+        cpus = set()
+        for part in txt.split(","):
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+        cpus &= os.sched_getaffinity(0)
+        return cpus or None
+    except (AttributeError, OSError, ValueError, RuntimeError):
+        return None
+
+
 # ------------------------------------------------------------------ oracle sample
 def oracle_sample(L, B, Hq, Hkv, d, budget_s, seed=0):
     """Times the fp64 oracle on the last blocks of one query head of the
@@ -273,10 +297,19 @@ def run_native(args, rank, world, local_rank):
     if not args.no_e2e:
         pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
         keys = (*names, "dOc", "dOn")
-        h_in = {k: pin(X[k]) for k in keys}
+        # allocate the pinned buffers from a CPU next to the GPU, so that their
+        # pages sit in the GPU's NUMA node (the affinity is restored afterwards)
+        local_cpus = gpu_local_cpus(dev)
+        saved_cpus = os.sched_getaffinity(0)
+        if local_cpus:
+            os.sched_setaffinity(0, local_cpus)
+        try:
+            h_in = {k: pin(X[k]) for k in keys}
+            h_out = [pin(t) for t in (*fout, *gout)]
+        finally:
+            os.sched_setaffinity(0, saved_cpus)
         for k in h_in:
             h_in[k].copy_(X[k])
-        h_out = [pin(t) for t in (*fout, *gout)]
         h2d = sum(t.numel() * t.element_size() for t in h_in.values())
         d2h = sum(t.numel() * t.element_size() for t in h_out)
         sets = []
@@ -353,7 +386,9 @@ def run_native(args, rank, world, local_rank):
                "h2d_gbs_alone": round(h2d_gbs, 1), "d2h_gbs_alone": round(d2h_gbs, 1),
                # the device's own time per step inside this loop (median), and the
                # clocks while it ran: what the copies leave to the computation
-               "compute_ms_per_step": round(compute_ms, 3), "clocks": e2e_clk}
+               "compute_ms_per_step": round(compute_ms, 3), "clocks": e2e_clk,
+               "host_buffers": ("pinned, allocated from the GPU's NUMA-node CPUs (%d CPUs)" % len(local_cpus)
+                                if local_cpus else "pinned (the GPU's NUMA node is not known)")}
         del sets, h_in, h_out
 
     # ---- roofline of the dominant kernel

@@ -83,12 +83,6 @@ BDLM_HD void noisy_interval(const Geom& g, int stream, int64_t i, int64_t& lo, i
   }
 }
 
-// True unless the range is the default (every row of both streams).
-BDLM_HD bool range_restricts(const RowRange& r) {
-  const RowRange all;
-  return r.lo[0] != all.lo[0] || r.lo[1] != all.lo[1] || r.hi[0] != all.hi[0] || r.hi[1] != all.hi[1];
-}
-
 // A row range's bounds for `stream` (selected, not indexed, so that a local
 // copy stays in registers).
 BDLM_HD int64_t range_lo(const RowRange& r, int stream) { return stream ? r.lo[1] : r.lo[0]; }
