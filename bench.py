@@ -289,10 +289,12 @@ def run_native(args, rank, world, local_rank):
     # ---- end to end through the public API with host buffers
     # Every step copies its inputs from pinned host memory to the device and
     # reads all of its results (O, LSE, dQ, dK, dV of both streams) back.
-    # Steps are pipelined the way a training loop feeds an accelerator: the
-    # inputs of step i+1 go up (copy stream) and the results of step i-1 come
-    # down (second copy stream) while step i computes, with two device buffer
-    # sets.  The timed region runs from the first upload to the last download.
+    # Steps are pipelined the way a training loop feeds an accelerator, with
+    # two device buffer sets and two copy streams: step i+1's Q, K, V go up
+    # while step i computes, its dO while its own forward runs; step i's O and
+    # LSE come down while its backward runs, its gradients while step i+1
+    # computes.  The timed region runs from the first upload to the last
+    # download.
     e2e = None
     if not args.no_e2e:
         pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
@@ -318,35 +320,51 @@ def run_native(args, rank, world, local_rank):
                          tuple(torch.empty_like(t) for t in fout), tuple(torch.empty_like(t) for t in gout)))
         s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
         ev = lambda: torch.cuda.Event()
-        in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        # per buffer set: Q/K/V up, dO up, forward done, step done, O/LSE down, gradients down
+        qkv_in, do_in, fwd_done, comp_done = [ev(), ev()], [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        fo_out, go_out = [ev(), ev()], [ev(), ev()]
+        h_fo, h_go = h_out[:len(fout)], h_out[len(fout):]
 
         def e2e_run(nsteps, spans=None):
             for i in range(nsteps):
                 si = i & 1
                 dX, fo, go = sets[si]
                 if i >= 2:
-                    s_in.wait_event(comp_done[si])
+                    s_in.wait_event(comp_done[si])  # step i-2 no longer reads this set's inputs
                 with torch.cuda.stream(s_in):
-                    for k in keys:
+                    for k in names:
                         dX[k].copy_(h_in[k], non_blocking=True)
-                    in_done[si].record(s_in)
-                stream.wait_event(in_done[si])
+                    qkv_in[si].record(s_in)
+                    for k in ("dOc", "dOn"):  # needed by the backward only
+                        dX[k].copy_(h_in[k], non_blocking=True)
+                    do_in[si].record(s_in)
+                stream.wait_event(qkv_in[si])
                 if i >= 2:
-                    stream.wait_event(out_done[si])
+                    stream.wait_event(fo_out[si])  # step i-2's O / LSE are on the host
                 if spans is not None:
                     spans.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
                     spans[-1][0].record(stream)
                 Oc, On, LSEc, LSEn = m.bdlm_attn_fwd(*[dX[k] for k in names], B, sc, out=fo, workspace=ws_f)
+                fwd_done[si].record(stream)
+                stream.wait_event(do_in[si])
+                if i >= 2:
+                    stream.wait_event(go_out[si])  # step i-2's gradients are on the host
                 m.bdlm_attn_bwd(*[dX[k] for k in names], Oc, On, dX["dOc"], dX["dOn"], LSEc, LSEn, B, sc,
                                 out=go, workspace=ws_b)
                 if spans is not None:
                     spans[-1][1].record(stream)
                 comp_done[si].record(stream)
+                # O and LSE go down while the backward runs, the gradients after it
+                s_out.wait_event(fwd_done[si])
+                with torch.cuda.stream(s_out):
+                    for hd, dv in zip(h_fo, fo):
+                        hd.copy_(dv, non_blocking=True)
+                    fo_out[si].record(s_out)
                 s_out.wait_event(comp_done[si])
                 with torch.cuda.stream(s_out):
-                    for hd, dv in zip(h_out, (*fo, *go)):
+                    for hd, dv in zip(h_go, go):
                         hd.copy_(dv, non_blocking=True)
-                    out_done[si].record(s_out)
+                    go_out[si].record(s_out)
             stream.wait_stream(s_out)
 
         # link bandwidth, for the record (one upload, one download, alone)
@@ -382,7 +400,9 @@ def run_native(args, rank, world, local_rank):
         e2e = {"value": round(job_rate(useful_flops(L, B, Hq, d), world, ems) / 1e12, 3), "unit": "TFLOP/s",
                "ms_per_step": round(ems, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "tokens_per_s": round(job_rate(2 * L, world, ems), 1), "steps": k2,
-               "pipelined": "uploads and downloads overlap neighbouring steps' compute (two buffer sets)",
+               "pipelined": ("two buffer sets; a step's Q/K/V go up during the previous step, its dO during "
+                             "its forward, its O/LSE come down during its backward, its gradients during "
+                             "the next step"),
                "h2d_gbs_alone": round(h2d_gbs, 1), "d2h_gbs_alone": round(d2h_gbs, 1),
                # the device's own time per step inside this loop (median), and the
                # clocks while it ran: what the copies leave to the computation
