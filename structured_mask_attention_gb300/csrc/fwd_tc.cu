@@ -72,6 +72,8 @@ enum { B_QF = 0, B_QE = 1, B_KF = 2, B_KE = 4, B_VF = 6, B_VE = 8, B_SF = 10, B_
 // the work-item ring's slots.
 static_assert(8 * B_COUNT + 8 + 8 * kRingSlots <= 256, "barrier area overflows");
 
+constexpr int kGeoBytes = 512;  // kRingSlots ItemGeo
+
 template <int HD>
 struct Layout {
   static constexpr int kTile = 128 * HD * 2;  // 128 rows x HD bf16 (Q sub-tile, K, V alike)
@@ -79,7 +81,8 @@ struct Layout {
   static constexpr int kK = 2 * kTile;        // K stages 0, 1
   static constexpr int kV = 4 * kTile;        // V stages 0, 1
   static constexpr int kBar = 6 * kTile;
-  static constexpr int kBytes = kBar + 256;
+  static constexpr int kGeo = kBar + 256;  // the work-item ring's geometry slots
+  static constexpr int kBytes = kGeo + kGeoBytes;
   // 1024 bytes of slack for alignment; never below 120 KB so that a second
   // CTA cannot share the SM (each CTA holds all 512 TMEM columns).
   static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
@@ -93,6 +96,7 @@ struct ItemGeo {
   int rot;    // the clean-key sweep starts at clean tile c0 + rot
   int64_t off, L;  // first row of the item's sequence in the packed tensors, its length
 };
+static_assert(kRingSlots * sizeof(ItemGeo) <= kGeoBytes, "geometry slots overflow");
 
 // VL: packed variable-length batch (a separate instantiation, so that the
 // one-sequence kernel keeps its register budget).
@@ -218,6 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto BAR = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
   const ItemRing ring{BAR(B_IF), BAR(B_IE),
                       reinterpret_cast<volatile int64_t*>(base_ptr + LY::kBar + 8 * B_COUNT + 8)};
+  // each ring slot also carries its item's geometry, computed once by the
+  // producer; the softmax warps keep their slot until the item's epilogue
+  ItemGeo* geo_slot = reinterpret_cast<ItemGeo*>(base_ptr + LY::kGeo);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -265,9 +272,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
         const int64_t idx = claim_item(p.g, p.status + kSchedWordFwd, rnd, cta, grid);
-        if (!ring_put(ring, rnd, idx, wd, 90)) { ok = false; break; }
+        if (!ring_acquire(ring, rnd, wd, 90)) { ok = false; break; }
+        ItemGeo g;
+        if (idx < n_items) {
+          g = item_geo<VL, ROWS>(p, vt, rows, idx);
+          geo_slot[rnd & (kRingSlots - 1)] = g;
+        }
+        ring_publish(ring, rnd, idx);
         if (idx >= n_items) break;
-        const ItemGeo g = item_geo<VL, ROWS>(p, vt, rows, idx);
         if (g.n == 0) continue;
         if (itn > 0 && !mbar_wait(BAR(B_QE), (itn - 1) & 1, wd, 1)) { ok = false; break; }
         mbar_arrive_expect_tx(BAR(B_QF), 2 * LY::kTile);
@@ -326,9 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
         int64_t idx;
-        if (!ring_get(ring, rnd, idx, wd, 91)) { ok = false; break; }
+        if (!ring_wait(ring, rnd, idx, wd, 91)) { ok = false; break; }
         if (idx >= n_items) break;
-        const ItemGeo g = item_geo<VL, ROWS>(p, vt, rows, idx);
+        const ItemGeo g = geo_slot[rnd & (kRingSlots - 1)];
+        ring_release(ring, rnd);
         if (g.n == 0) continue;
         if (!mbar_wait(BAR(B_QF), itn & 1, wd, 4)) { ok = false; break; }
         if (!mbar_wait(BAR(B_KF + (kc & 1)), (kc >> 1) & 1, wd, 5)) { ok = false; break; }
@@ -383,9 +396,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int64_t rnd = 0; ok; ++rnd) {
       int64_t idx;
-      if (!ring_get(ring, rnd, idx, wd, 92)) { ok = false; break; }
+      if (!ring_wait(ring, rnd, idx, wd, 92)) { ok = false; break; }
       if (idx >= n_items) break;
-      const ItemGeo g = item_geo<VL, ROWS>(p, vt, rows, idx);
+      const ItemGeo g = geo_slot[rnd & (kRingSlots - 1)];  // the slot stays ours until the epilogue
       // (one sequence: its length and offset come from the parameters, so
       // that they occupy no registers across the loop)
       const int64_t seqL = VL ? g.L : p.g.L, seq0 = VL ? g.off : 0;
@@ -411,6 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           lse_out[lrow] = -INFINITY;
         }
+        ring_release(ring, rnd);
         continue;
       }
       // loop state in 32-bit (rows and keys are TMA coordinates, < 2^31):
@@ -495,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       ok = mbar_wait(BAR(B_OD + t), itn & 1, wd, 13);
-      const ItemGeo ge = item_geo<VL, ROWS>(p, vt, rows, idx);
+      const ItemGeo ge = geo_slot[rnd & (kRingSlots - 1)];
       const int64_t seqL_e = VL ? ge.L : p.g.L, seq0_e = VL ? ge.off : 0;
       const int64_t re = ge.r0 + t * BM + row;
       const bool ve = re < seqL_e && (!ROWS || row_in(rows, ge.stream, re));
@@ -504,6 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* lse_e = (ge.stream ? p.LSEn : p.LSEc) + (int64_t)ge.head * lstride_e;
       void* obase_e = ge.stream ? p.On : p.Oc;
       const int64_t oofs_e = (lrow_e * p.g.Hq + ge.head) * HD;
+      ring_release(ring, rnd);  // the item's geometry is in registers now
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();

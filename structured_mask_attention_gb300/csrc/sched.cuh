@@ -38,26 +38,50 @@ __device__ __forceinline__ int64_t claim_item(const Geom& g, uint32_t* counter, 
   return g.naive_order ? rnd * grid + cta : (int64_t)atomicAdd(counter, 1u);
 }
 
+// Producer, in two parts for rings whose slots carry more than the index
+// (the caller writes its own part of slot rnd % kRingSlots in between):
+// waits for round rnd's slot to be free ...
+__device__ __forceinline__ bool ring_acquire(const ItemRing& r, int64_t rnd, const Watchdog& wd, uint32_t site) {
+  const uint32_t s = (uint32_t)rnd & (kRingSlots - 1);
+  const uint32_t use = (uint32_t)(rnd / kRingSlots);
+  return use == 0 || mbar_wait(r.empty + 8 * s, (use - 1) & 1, wd, site);
+}
+// ... and publishes round rnd's item.
+__device__ __forceinline__ void ring_publish(const ItemRing& r, int64_t rnd, int64_t idx) {
+  const uint32_t s = (uint32_t)rnd & (kRingSlots - 1);
+  r.slot[s] = idx;
+  mbar_arrive(r.full + 8 * s);
+}
+
 // Producer: publishes round rnd's item (waits for its slot to be free).
 __device__ __forceinline__ bool ring_put(const ItemRing& r, int64_t rnd, int64_t idx, const Watchdog& wd,
                                          uint32_t site) {
-  const uint32_t s = (uint32_t)rnd & (kRingSlots - 1);
-  const uint32_t use = (uint32_t)(rnd / kRingSlots);
-  if (use > 0 && !mbar_wait(r.empty + 8 * s, (use - 1) & 1, wd, site)) return false;
-  r.slot[s] = idx;
-  mbar_arrive(r.full + 8 * s);
+  if (!ring_acquire(r, rnd, wd, site)) return false;
+  ring_publish(r, rnd, idx);
   return true;
 }
 
-// Consumer thread: round rnd's item.  (Every consumer thread arrives on its
-// own, with no warp-wide step, so that a thread that gives up after a wait
-// limit never leaves its warp's other lanes waiting for it.)
-__device__ __forceinline__ bool ring_get(const ItemRing& r, int64_t rnd, int64_t& idx, const Watchdog& wd,
-                                         uint32_t site) {
+// Consumer thread, in two parts: waits for round rnd's item ...  (Every
+// consumer thread arrives on its own, with no warp-wide step, so that a
+// thread that gives up after a wait limit never leaves its warp's other
+// lanes waiting for it.)
+__device__ __forceinline__ bool ring_wait(const ItemRing& r, int64_t rnd, int64_t& idx, const Watchdog& wd,
+                                          uint32_t site) {
   const uint32_t s = (uint32_t)rnd & (kRingSlots - 1);
   if (!mbar_wait(r.full + 8 * s, (uint32_t)(rnd / kRingSlots) & 1, wd, site)) return false;
   idx = r.slot[s];
-  mbar_arrive(r.empty + 8 * s);
+  return true;
+}
+// ... and, once it no longer reads the slot, frees it.
+__device__ __forceinline__ void ring_release(const ItemRing& r, int64_t rnd) {
+  mbar_arrive(r.empty + 8 * ((uint32_t)rnd & (kRingSlots - 1)));
+}
+
+// Consumer thread: round rnd's item, its slot freed at once.
+__device__ __forceinline__ bool ring_get(const ItemRing& r, int64_t rnd, int64_t& idx, const Watchdog& wd,
+                                         uint32_t site) {
+  if (!ring_wait(r, rnd, idx, wd, site)) return false;
+  ring_release(r, rnd);
   return true;
 }
 
