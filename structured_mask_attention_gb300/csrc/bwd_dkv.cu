@@ -48,7 +48,8 @@ struct DkvLayout {
   static constexpr int kdO = kQ + QNS * kTile;
   static constexpr int kStat = kdO + QNS * kTile;  // per stage: LSE[128] then D[128], fp32
   static constexpr int kBar = kStat + QNS * 2 * KBN * 4;
-  static constexpr int kBytes = kBar + 256;
+  static constexpr int kGeo = kBar + 256;  // the work-item ring's geometry slots
+  static constexpr int kBytes = kGeo + 512;
   static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
 };
 
@@ -61,6 +62,7 @@ struct DkvGeo {
   int per_head, n;                 // steps per head, total steps
   int64_t off, L;                  // first row of the item's sequence in the packed tensors, its length
 };
+static_assert(kRingSlots * sizeof(DkvGeo) <= 512, "geometry slots overflow");
 
 // VL: packed variable-length batch; ROWS: the call computes a row range
 // (separate instantiations).
@@ -199,6 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto BAR = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
   const ItemRing ring{BAR(KV_IF), BAR(KV_IE),
                       reinterpret_cast<volatile int64_t*>(base_ptr + LY::kBar + 8 * KV_NBAR + 8)};
+  // each ring slot also carries its item's geometry, computed once by the producer
+  DkvGeo* geo_slot = reinterpret_cast<DkvGeo*>(base_ptr + LY::kGeo);
   const Role R = role();
 
   if (threadIdx.x == 0) {
@@ -242,13 +246,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t idx = 0;
       if (R.lane == 0) {
         idx = claim_item(p.g, status + kSchedWordDkv, rnd, cta, grid);
-        ok = ring_put(ring, rnd, idx, wd, 93);
+        ok = ring_acquire(ring, rnd, wd, 93);
+        if (ok) {
+          if (idx < n_items) geo_slot[rnd & (kRingSlots - 1)] = dkv_geo<VL, ROWS>(p, vt, idx);
+          ring_publish(ring, rnd, idx);
+        }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       idx = __shfl_sync(0xffffffffu, idx, 0);
       if (!ok) break;
       if (idx >= n_items) break;
-      const DkvGeo t = dkv_geo<VL, ROWS>(p, vt, idx);
+      // (lane 0 wrote the slot; the slot is not reused before this warp
+      // acquires it again, kRingSlots rounds on)
+      __syncwarp();
+      const DkvGeo t = geo_slot[rnd & (kRingSlots - 1)];
       if (t.n == 0) continue;
       if (itn > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(BAR(KV_KE), (itn - 1) & 1, wd, 41));
@@ -318,9 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
         int64_t idx;
-        if (!ring_get(ring, rnd, idx, wd, 94)) { ok = false; break; }
+        if (!ring_wait(ring, rnd, idx, wd, 94)) { ok = false; break; }
         if (idx >= n_items) break;
-        const DkvGeo t = dkv_geo<VL, ROWS>(p, vt, idx);
+        const DkvGeo t = geo_slot[rnd & (kRingSlots - 1)];
+        ring_release(ring, rnd);
         if (t.n == 0) continue;
         if (!mbar_wait(BAR(KV_KF), itn & 1, wd, 43)) { ok = false; break; }
         const uint32_t q_base = qc;
@@ -386,9 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t sl2x2 = f2(p.scale_log2, p.scale_log2), nlog2e = f2(-kLog2e, -kLog2e);
     for (int64_t rnd = 0; ok; ++rnd) {
       int64_t idx;
-      if (!ring_get(ring, rnd, idx, wd, 95)) { ok = false; break; }
+      if (!ring_wait(ring, rnd, idx, wd, 95)) { ok = false; break; }
       if (idx >= n_items) break;
-      const DkvGeo t = dkv_geo<VL, ROWS>(p, vt, idx);
+      const DkvGeo t = geo_slot[rnd & (kRingSlots - 1)];
+      ring_release(ring, rnd);
       if (t.n == 0) continue;
       const int64_t j = t.j0 + row;
       // query-row bounds as 32-bit values (rows are TMA coordinates, < 2^31):

@@ -46,7 +46,8 @@ struct DqLayout {
   static constexpr int kK = kdO + kTile;
   static constexpr int kV = kK + KNS * kTile;
   static constexpr int kBar = kV + VNS * kTile;
-  static constexpr int kBytes = kBar + 256;
+  static constexpr int kGeo = kBar + 256;  // the work-item ring's geometry slots
+  static constexpr int kBytes = kGeo + 512;
   static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
 };
 
@@ -58,6 +59,7 @@ struct DqGeo {
   int rot;         // the clean-key sweep starts at clean tile c0 + rot
   int64_t off, L;  // first row of the item's sequence in the packed tensors, its length
 };
+static_assert(kRingSlots * sizeof(DqGeo) <= 512, "geometry slots overflow");
 
 // VL: packed variable-length batch (a separate instantiation).
 template <bool VL, bool ROWS>
@@ -119,6 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto BAR = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
   const ItemRing ring{BAR(DQ_IF), BAR(DQ_IE),
                       reinterpret_cast<volatile int64_t*>(base_ptr + LY::kBar + 8 * DQ_NBAR + 8)};
+  // each ring slot also carries its item's geometry, computed once by the producer
+  DqGeo* geo_slot = reinterpret_cast<DqGeo*>(base_ptr + LY::kGeo);
   const Role R = role();
 
   if (threadIdx.x == 0) {
@@ -164,9 +168,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
         const int64_t idx = claim_item(p.g, status + kSchedWordDq, rnd, cta, grid);
-        if (!ring_put(ring, rnd, idx, wd, 96)) { ok = false; break; }
+        if (!ring_acquire(ring, rnd, wd, 96)) { ok = false; break; }
+        DqGeo t;
+        if (idx < n_items) {
+          t = dq_geo<VL, ROWS>(p, vt, idx);
+          geo_slot[rnd & (kRingSlots - 1)] = t;
+        }
+        ring_publish(ring, rnd, idx);
         if (idx >= n_items) break;
-        const DqGeo t = dq_geo<VL, ROWS>(p, vt, idx);
         if (t.n == 0) continue;
         if (itn > 0 && !mbar_wait(BAR(DQ_QE), (itn - 1) & 1, wd, 21)) { ok = false; break; }
         mbar_arrive_expect_tx(BAR(DQ_QF), 2 * LY::kTile);
@@ -210,9 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int64_t rnd = 0; ok; ++rnd) {
         int64_t idx;
-        if (!ring_get(ring, rnd, idx, wd, 97)) { ok = false; break; }
+        if (!ring_wait(ring, rnd, idx, wd, 97)) { ok = false; break; }
         if (idx >= n_items) break;
-        const DqGeo t = dq_geo<VL, ROWS>(p, vt, idx);
+        const DqGeo t = geo_slot[rnd & (kRingSlots - 1)];
+        ring_release(ring, rnd);
         if (t.n == 0) continue;
         if (!mbar_wait(BAR(DQ_QF), itn & 1, wd, 24)) { ok = false; break; }
         // stage of the previous step (read by its dQ MMA)
@@ -277,9 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int64_t rnd = 0; ok; ++rnd) {
       int64_t idx;
-      if (!ring_get(ring, rnd, idx, wd, 98)) { ok = false; break; }
+      if (!ring_wait(ring, rnd, idx, wd, 98)) { ok = false; break; }
       if (idx >= n_items) break;
-      const DqGeo t = dq_geo<VL, ROWS>(p, vt, idx);
+      const DqGeo t = geo_slot[rnd & (kRingSlots - 1)];
+      ring_release(ring, rnd);
       // (one sequence: its length and offset come from the parameters)
       const int64_t seqL = VL ? t.L : p.g.L, seq0 = VL ? t.off : 0;
       const int64_t r = t.r0 + row;  // row within the item's sequence
